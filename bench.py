@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta rule library on one GB300 (or N replicas under torchrun).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+
+One step = the whole prefill path on the prefill workload (B=2 sequences x T=4096 tokens, H=16
+heads, d_k=d_v=128, bf16 q/k/v, fp32 gates, fused RMSNorm*SiLU gate): gate preparation
+(gdn_decay_from_logits) followed by the chunked prefill (gdn_chunk_fwd).  The decode workload
+(256 sequences x 32 heads, fp32 state of 128x128, bf16 q/k/v) is timed in the same run and reported
+in the "decode" object.  Inputs are resident in HBM before the timed region; L2 (129 MB) is flushed
+by writing a 512 MB buffer before every timed prefill step; the decode state (512 MiB) is larger
+than L2.  Times are CUDA events on the launching stream; value is whole-job tokens/s (max time over
+ranks).  The "e2e" object is the same metric through the C ABI with host buffers: pinned-host
+inputs copied in and the output and final state copied out inside every timed step.
+
+--impl reference times the fp64 CPU oracle (the only reference this method has) on a bounded
+sample of the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+C_CHUNK = 64
+
+
+def prefill_flops_per_token_head(d, C=C_CHUNK):
+    """Five C x C x d products (K K^T, Q K^T, W, U, (QK^T*D) V_new), three C x d x d products
+    (W S^T, Q S^T, V_new^T K), and the triangular solve (C^3/3 per chunk), per token."""
+    return 10 * C * d + 6 * d * d + C * C / 3.0
+
+
+def prefill_bytes(total_T, H, d, num_seqs, qkv_bytes=2, out_bytes=2, gated=True, init_state=False):
+    """Algorithmic HBM bytes of one gdn_chunk_fwd call: q, k, v, g, beta, z, out once, and the
+    final (plus initial) state once per (sequence, head)."""
+    per_tok_head = 3 * d * qkv_bytes + 8 + (d * 4 if gated else 0) + d * out_bytes
+    states = num_seqs * H * d * d * 4 * (2 if init_state else 1)
+    return total_T * H * per_tok_head + states
+
+
+def decode_bytes(N, H, d, qkv_bytes=2, out_bytes=2):
+    """Per (sequence, head): state read + write, q, k, v, g, beta, y."""
+    return N * H * (2 * d * d * 4 + 3 * d * qkv_bytes + 8 + d * out_bytes)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# oracle (CPU) timing: the cpu_baseline leg and the --impl reference arm
+# ---------------------------------------------------------------------------------------------
+
+def time_oracle(inp, heads, threads):
+    """Time the oracle (recurrence + gate) on the given heads of the prefill inputs."""
+    import numpy as np
+    import oracle
+    q, k, v = (inp[n][:, heads] for n in ("q", "k", "v"))
+    z = inp["z"][:, heads] if inp["z"] is not None else None
+    n, T = inp["num_seqs"], inp["total_T"] // inp["num_seqs"]
+    cu = np.arange(0, inp["total_T"] + 1, T, dtype=np.int32)
+    t0 = time.perf_counter()
+    g, beta = oracle.gates_from_logits(inp["a"][:, heads], inp["A_log"][heads], b=inp["b"][:, heads])
+    y, S = oracle.recurrence(q, k, v, g, beta, cu_seqlens=cu, threads=threads)
+    if z is not None:
+        oracle.gate_rmsnorm_silu(y, z)
+    return time.perf_counter() - t0
+
+
+def oracle_rate(inp, H, seconds_budget=20.0, threads=None):
+    """Tokens/s of the oracle on the full workload, estimated from a bounded sample of heads."""
+    threads = threads or os.cpu_count() or 1
+    # a one-head probe sizes the sample so that the measurement takes roughly the budget
+    t1 = time_oracle(inp, [0], 1)
+    per_head_parallel = t1 / min(threads, inp["num_seqs"])
+    n_heads = max(1, min(H, int(seconds_budget / max(per_head_parallel, 1e-6) / 2)))
+    heads = list(range(n_heads))
+    th = max(1, min(threads, n_heads * inp["num_seqs"]))
+    t = time_oracle(inp, heads, th)
+    tok_per_s = inp["total_T"] * (n_heads / H) / t
+    sample = (f"{n_heads} of {H} heads x {inp['num_seqs']} sequences x "
+              f"{inp['total_T'] // inp['num_seqs']} tokens (recurrence + gate, fp64), "
+              f"{th} threads, {t:.2f} s; tokens/s scaled to all heads")
+    return tok_per_s, th, sample, t
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU measurements
+# ---------------------------------------------------------------------------------------------
+
+def ev():
+    return torch.cuda.Event(enable_timing=True)
+
+
+def bench_prefill(args, dev):
+    import gated_deltanet_recurrence_gb300 as gdn
+    from gated_deltanet_recurrence_gb300 import synthetic
+    inp_cpu = synthetic.prefill_inputs("prefill")
+    cfg = inp_cpu["cfg"]
+    stream = torch.cuda.current_stream()
+    d_in = {k_: (v_.to(dev) if isinstance(v_, torch.Tensor) else v_) for k_, v_ in inp_cpu.items()}
+    total_T, H, d, n = inp_cpu["total_T"], cfg["H"], cfg["d"], inp_cpu["num_seqs"]
+    g = torch.empty(total_T, H, device=dev)
+    beta = torch.empty(total_T, H, device=dev)
+    out = torch.empty(total_T, H, d, dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty(n, H, d, d, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        gdn.gdn_decay_from_logits(d_in["a"], d_in["A_log"], b=d_in["b"], g_out=g, beta_out=beta)
+        e_mid = ev()
+        e_mid.record(stream)
+        gdn.gdn_chunk_fwd(d_in["q"], d_in["k"], d_in["v"], g, beta, num_seqs=n,
+                          gate_z=d_in["z"], out=out, final_state=Sf)
+        return e_mid
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_get_device_error() == 0
+    step_ms, chunk_ms = [], []
+    barrier(args.world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(args.local)
+    clocks.start()
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        e_mid = step()
+        e1.record(stream)
+        step_ms.append((e0, e_mid, e1))
+    torch.cuda.synchronize()
+    barrier(args.world)
+    clk = clocks.stop()
+    tot = [a.elapsed_time(c) for a, _, c in step_ms]
+    chunk_ms = [b_.elapsed_time(c) for _, b_, c in step_ms]
+    ms = statistics.mean(tot)
+    kms = statistics.mean(chunk_ms)
+    assert gdn.gdn_get_device_error() == 0
+
+    # ---- end to end through the ABI with host buffers ----
+    pinned = {k_: v_.pin_memory() for k_, v_ in inp_cpu.items()
+              if isinstance(v_, torch.Tensor) and k_ in ("q", "k", "v", "a", "A_log", "b", "z")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_h.numel() * out_h.element_size() + Sf_h.numel() * Sf_h.element_size()
+
+    def e2e_step():
+        for k_, t in pinned.items():
+            d_in[k_].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        Sf_h.copy_(Sf, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e2e_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e = statistics.mean(a.elapsed_time(b_) for a, b_ in e2e_ms)
+    return dict(ms=ms, kernel_ms=kms, clocks=clk, e2e_ms=e2e, h2d=h2d, d2h=d2h, total_T=total_T,
+                H=H, d=d, num_seqs=n, inp=inp_cpu, launches=2 * args.steps)
+
+
+def bench_decode(args, dev):
+    import gated_deltanet_recurrence_gb300 as gdn
+    from gated_deltanet_recurrence_gb300 import synthetic
+    inp = synthetic.decode_inputs("decode")
+    cfg = inp["cfg"]
+    N, H, d = cfg["N"], cfg["H"], cfg["d"]
+    stream = torch.cuda.current_stream()
+    q, k, v, a, A_log, b = (inp[x].to(dev) for x in ("q", "k", "v", "a", "A_log", "b"))
+    state = inp["state"].to(dev)
+    g = torch.empty(N, H, device=dev)
+    beta = torch.empty(N, H, device=dev)
+    out = torch.empty(N, H, d, dtype=torch.bfloat16, device=dev)
+    gdn.gdn_decay_from_logits(a, A_log, b=b, g_out=g, beta_out=beta)
+    for _ in range(args.warmup):
+        gdn.gdn_recurrent_step(q, k, v, g, beta, state, out=out)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(args.steps, 20)):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        gdn.gdn_decay_from_logits(a, A_log, b=b, g_out=g, beta_out=beta)
+        e_mid = ev()
+        e_mid.record(stream)
+        gdn.gdn_recurrent_step(q, k, v, g, beta, state, out=out)
+        e1.record(stream)
+        times.append((e0, e_mid, e1))
+    torch.cuda.synchronize()
+    assert gdn.gdn_get_device_error() == 0
+    step_ms = statistics.mean(x.elapsed_time(z) for x, _, z in times)
+    kern_ms = statistics.mean(y.elapsed_time(z) for _, y, z in times)
+    return dict(ms=step_ms, kernel_ms=kern_ms, N=N, H=H, d=d)
+
+
+def run_gdn(args):
+    dev = torch.device("cuda", args.local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    pf = bench_prefill(args, dev)
+    dc = bench_decode(args, dev)
+    world = args.world
+    ms = max_over_ranks(pf["ms"], world)
+    e2e_ms = max_over_ranks(pf["e2e_ms"], world)
+    dms = max_over_ranks(dc["ms"], world)
+    tokens = pf["total_T"] * world
+    value = tokens / (ms / 1e3)
+
+    # roofline of the dominant kernel (the chunked prefill), achieved from its event times
+    th = pf["total_T"] * pf["H"]
+    flops = th * prefill_flops_per_token_head(pf["d"])
+    byts = prefill_bytes(pf["total_T"], pf["H"], pf["d"], pf["num_seqs"])
+    k_s = pf["kernel_ms"] / 1e3
+    # The prefill kernel in this build runs its products on the CUDA cores in fp32, so its
+    # ceiling is the fp32 FMA rate: 152 SMs x 128 FMA/clk x 2 FLOP x max SM clock.
+    alu_peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    roof = {"bound": "alu", "achieved": flops / k_s / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
+            "frac": flops / k_s / 1e12 / alu_peak, "traffic": None,
+            "kernel": "prefill_simt_kernel", "algorithmic_flops": flops, "algorithmic_bytes": byts,
+            "hbm_gbs_achieved": byts / k_s / 1e9, "peak_source": f"fp32 FMA rate at max clock"}
+    dbytes = decode_bytes(dc["N"], dc["H"], dc["d"])
+    d_gbs = dbytes / (dc["kernel_ms"] / 1e3) / 1e9
+    decode = {"metric": "decode tokens/s", "value": dc["N"] * world / (dms / 1e3), "unit": "tokens/s",
+              "ms_per_step": dms, "kernel_ms": dc["kernel_ms"],
+              "config": {"workload": "decode", "N": dc["N"], "H": dc["H"], "d_k": dc["d"], "d_v": dc["d"],
+                         "state": "fp32", "qkv": "bf16"},
+              "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": d_gbs / peaks["hbm_gbs"], "traffic": None,
+                           "kernel": "decode_kernel", "algorithmic_bytes": dbytes,
+                           "peak_source": f"{peak_src} hbm_gbs"}}
+    line = {
+        "metric": "prefill tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill", "num_seqs": pf["num_seqs"], "seq_len": pf["total_T"] // pf["num_seqs"],
+                   "H": pf["H"], "d_k": pf["d"], "d_v": pf["d"], "chunk": C_CHUNK, "gate": "rmsnorm_silu",
+                   "step": "gdn_decay_from_logits + gdn_chunk_fwd", "l2": "flushed (512 MB write) before each step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "decode": decode,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": pf["h2d"],
+                "d2h_bytes_per_step": pf["d2h"], "ms_per_step": e2e_ms},
+        "gpu_launches": pf["launches"],
+        "clocks": pf["clocks"],
+        "peaks": {"source": peak_src, "hbm_gbs": peaks.get("hbm_gbs"), "bf16_tflops": peaks.get("bf16_tflops")},
+    }
+    if args.rank == 0 and not args.no_cpu_baseline:
+        rate, th, sample, _ = oracle_rate(pf["inp"], pf["H"], seconds_budget=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                                "sample": sample}
+    if args.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    if args.rank != 0:
+        return
+    from gated_deltanet_recurrence_gb300 import synthetic
+    inp = synthetic.prefill_inputs("prefill")
+    cfg = inp["cfg"]
+    rates = []
+    for _ in range(args.warmup):
+        oracle_rate(inp, cfg["H"], seconds_budget=3.0)
+    last = None
+    for _ in range(args.steps):
+        last = oracle_rate(inp, cfg["H"], seconds_budget=3.0)
+        rates.append(last[0])
+    value = statistics.mean(rates)
+    line = {"impl": "reference", "metric": "prefill tokens/s", "value": value, "unit": "tokens/s",
+            "n_gpus": args.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": inp["total_T"] / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill", "num_seqs": inp["num_seqs"],
+                       "seq_len": inp["total_T"] // inp["num_seqs"], "H": cfg["H"], "d_k": cfg["d"],
+                       "d_v": cfg["d"], "gate": "rmsnorm_silu"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last[1], "kind": "oracle",
+                             "sample": last[2]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0, help="budget of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("note: warm-up raised to 3 steps", file=sys.stderr)
+        args.warmup = 3
+    args.world, args.rank, args.local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args)
+        else:
+            run_gdn(args)
+    finally:
+        if args.world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

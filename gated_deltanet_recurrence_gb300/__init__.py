@@ -1,0 +1,19 @@
+"""Gated delta rule kernels for GB300 (sm_103a): chunked prefill, one-token decode, gated norm.
+
+The compute lives in libgdn.so (hand-written CUDA, C ABI in include/gdn.h); this package only
+builds it and binds it.  Import is cheap: the library is loaded on the first call.
+"""
+from ._binding import (  # noqa: F401
+    GDN_BF16,
+    GDN_F32,
+    GdnError,
+    gdn_chunk_fwd,
+    gdn_decay_from_logits,
+    gdn_gate_rmsnorm_silu,
+    gdn_get_device_error,
+    gdn_recurrent_step,
+    lib,
+)
+
+__all__ = ["gdn_chunk_fwd", "gdn_recurrent_step", "gdn_gate_rmsnorm_silu", "gdn_decay_from_logits",
+           "gdn_get_device_error", "GdnError", "lib", "GDN_F32", "GDN_BF16"]

@@ -1,0 +1,208 @@
+"""ctypes binding of libgdn.so: same names as the C ABI (include/gdn.h), torch tensors in.
+
+Argument marshalling only: shapes are read from the tensors, outputs that the caller does not
+pass are allocated with torch, and the call goes to the library on the current torch CUDA stream
+(or the stream given).  Every computation happens in the library's CUDA kernels; there is no
+fallback: if libgdn.so is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libgdn.so")
+
+GDN_F32, GDN_BF16 = 0, 1
+STATUS = {0: "GDN_OK", -1: "GDN_ERR_ARG", -2: "GDN_ERR_DTYPE", -3: "GDN_ERR_CU_SEQLENS",
+          -4: "GDN_ERR_WORKSPACE", -5: "GDN_ERR_LAUNCH", -6: "GDN_ERR_TIMEOUT",
+          -7: "GDN_ERR_UNSUPPORTED", -8: "GDN_ERR_CUDA"}
+
+_lib = None
+_lock = threading.Lock()
+
+_vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_i, _f, _sz, _l = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
+
+SIGNATURES = {
+    "gdn_chunk_fwd": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
+                           _fp, _fp, _f, _vp, _i, _vp, _sz, _vp]),
+    "gdn_chunk_fwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "gdn_recurrent_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
+                                _f, _vp, _i, _vp]),
+    "gdn_gate_rmsnorm_silu": (_i, [_vp, _i, _fp, _fp, _f, _vp, _i, _l, _i, _vp]),
+    "gdn_decay_from_logits": (_i, [_fp, _fp, _fp, _fp, _fp, _fp, _l, _i, _vp]),
+    "gdn_get_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
+    "gdn_status_string": (ctypes.c_char_p, [_i]),
+}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} returned {status} ({STATUS.get(status, 'unknown')})")
+
+
+def lib():
+    """Load libgdn.so (building it first if it is missing or older than its sources)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            from . import build as _build
+            if _build.is_stale():
+                _build.build()
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libgdn.so not found at {LIB_PATH}")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _torch_dt(code: int):
+    return torch.bfloat16 if code == GDN_BF16 else torch.float32
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("all tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("all tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _f32(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise GdnError(fn, rc)
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0, use_qk_l2norm=True,
+                  initial_state=None, final_state=None, output_final_state=True, gate_z=None,
+                  norm_weight=None, norm_eps=1e-6, out=None, out_dtype=None, workspace=None,
+                  stream=None):
+    """Chunked prefill.  q, k [total_T, H, d_k]; v [total_T, H, d_v]; g, beta [total_T, H] fp32;
+    cu_seqlens int32 [num_seqs+1] (device) or None with num_seqs equal sequences (default 1).
+    Returns (out, final_state); final_state is allocated unless given or not requested."""
+    total_T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        num_seqs = cu_seqlens.numel() - 1
+    elif num_seqs is None:
+        num_seqs = 1
+    dt = _dt(q)
+    if _dt(k) != dt or _dt(v) != dt:
+        raise TypeError("q, k, v must share one dtype")
+    odt = dt if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if out is None:
+        out = torch.empty((total_T, H, d_v), dtype=_torch_dt(odt), device=q.device)
+    else:
+        odt = _dt(out)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((num_seqs, H, d_v, d_k), dtype=torch.float32, device=q.device)
+    for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state),
+                    ("final_state", final_state), ("gate_z", gate_z), ("norm_weight", norm_weight)):
+        _f32(t, name)
+    L = lib()
+    ws_need = L.gdn_chunk_fwd_workspace_size(num_seqs, total_T, H, d_k, d_v, dt)
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    rc = L.gdn_chunk_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs, total_T,
+                         H, d_k, d_v, dt, float(scale), int(bool(use_qk_l2norm)), _p(initial_state),
+                         _p(final_state), _p(gate_z), _p(norm_weight), float(norm_eps), _p(out), odt,
+                         _p(workspace), workspace.numel() if workspace is not None else 0,
+                         _stream(stream))
+    _check("gdn_chunk_fwd", rc)
+    return out, final_state
+
+
+def gdn_recurrent_step(q, k, v, g, beta, state, scale=0.0, use_qk_l2norm=True, gate_z=None,
+                       norm_weight=None, norm_eps=1e-6, out=None, out_dtype=None, stream=None):
+    """One decode token: q, k [N, H, d_k]; v [N, H, d_v]; g, beta [N, H]; state [N, H, d_v, d_k]
+    fp32 updated in place.  Returns out [N, H, d_v]."""
+    N, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = _dt(q)
+    odt = dt if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if out is None:
+        out = torch.empty((N, H, d_v), dtype=_torch_dt(odt), device=q.device)
+    else:
+        odt = _dt(out)
+    for name, t in (("g", g), ("beta", beta), ("state", state), ("gate_z", gate_z),
+                    ("norm_weight", norm_weight)):
+        _f32(t, name)
+    rc = lib().gdn_recurrent_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state), N, H, d_k, d_v,
+                                  dt, float(scale), int(bool(use_qk_l2norm)), _p(gate_z),
+                                  _p(norm_weight), float(norm_eps), _p(out), odt, _stream(stream))
+    _check("gdn_recurrent_step", rc)
+    return out
+
+
+def gdn_gate_rmsnorm_silu(y, z, norm_weight=None, eps=1e-6, out=None, out_dtype=None, stream=None):
+    """out = w * y / rms(y) * silu(z) over the last dimension of y (fp32 or bf16)."""
+    d_v = y.shape[-1]
+    rows = y.numel() // d_v if d_v else 0
+    odt = _dt(y) if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if out is None:
+        out = torch.empty(y.shape, dtype=_torch_dt(odt), device=y.device)
+    else:
+        odt = _dt(out)
+    _f32(z, "z")
+    _f32(norm_weight, "norm_weight")
+    rc = lib().gdn_gate_rmsnorm_silu(_p(y), _dt(y), _p(z), _p(norm_weight), float(eps), _p(out), odt,
+                                     rows, d_v, _stream(stream))
+    _check("gdn_gate_rmsnorm_silu", rc)
+    return out
+
+
+def gdn_decay_from_logits(a, A_log, dt_bias=None, b=None, g_out=None, beta_out=None, stream=None):
+    """g = -exp(A_log) softplus(a + dt_bias) and beta = sigmoid(b); a, b [total_T, H] fp32."""
+    total_T, H = a.shape
+    for name, t in (("a", a), ("A_log", A_log), ("dt_bias", dt_bias), ("b", b)):
+        _f32(t, name)
+    if g_out is None:
+        g_out = torch.empty_like(a)
+    if b is not None and beta_out is None:
+        beta_out = torch.empty_like(b)
+    rc = lib().gdn_decay_from_logits(_p(a), _p(A_log), _p(dt_bias), _p(b), _p(g_out), _p(beta_out),
+                                     total_T, H, _stream(stream))
+    _check("gdn_decay_from_logits", rc)
+    return (g_out, beta_out) if b is not None else g_out
+
+
+def gdn_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side status word."""
+    st = ctypes.c_int(0)
+    _check("gdn_get_device_error", lib().gdn_get_device_error(_stream(stream), ctypes.byref(st)))
+    return st.value

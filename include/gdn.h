@@ -1,0 +1,146 @@
+/*
+ * gdn.h -- C ABI of the GB300 gated delta rule library (libgdn.so).
+ *
+ * The method (page titles of the sources):
+ *   "[LLM Algorithms-2] Gated DeltaNet", sections 4 and 5: per head a matrix state
+ *   S (d_v x d_k) is updated token by token,
+ *       S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   y_t = S_t q_t,
+ *   which is the same as: decay S by alpha_t, predict S k_t, write beta_t (v_t - S k_t) k_t^T.
+ *   "6.6 Gated DeltaNet", 6.6.3-6.6.4: alpha_t = exp(-A softplus(a_t)), beta_t = sigmoid(b_t),
+ *   q and k are L2-normalised (x / sqrt(sum x^2 + 1e-6)) and q is scaled by 1/sqrt(d_k).
+ *   "5. 线性注意力", "门控 RMSNorm": o = w * RMSNorm(y) * SiLU(z).
+ *   "5. 线性注意力", "Delta Rule 的 Chunk 实现": the chunked form used for prefill.
+ *
+ * Conventions for every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major and contiguous,
+ *     16-byte aligned.  The library never allocates, frees or keeps device memory between
+ *     calls, and never synchronises the stream except in gdn_get_device_error.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - The return value is GDN_OK (0) or a negative gdn_status.  Argument errors are found on
+ *     the host before anything is launched.  Errors that only the device can see (a malformed
+ *     cu_seqlens array) are recorded in a device error word: the kernels then write nothing
+ *     for the affected sequence, and gdn_get_device_error() reports and clears the word.
+ *   - Token tensors are packed: q, k [total_T, H, d_k]; v, out [total_T, H, d_v];
+ *     gates g, beta [total_T, H] fp32; states [num_seqs, H, d_v, d_k] fp32 (d_k contiguous,
+ *     the orientation of "[LLM Algorithms-2] Gated DeltaNet" section 1: y = S q).
+ *   - Supported head sizes: d_k = d_v in {64, 128}.  Other sizes return GDN_ERR_UNSUPPORTED.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and of outputs.  Gates, states and the gate input z are fp32. */
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_ARG = -1,          /* null required pointer, non-positive or inconsistent size      */
+    GDN_ERR_DTYPE = -2,        /* dtype value not in gdn_dtype                                  */
+    GDN_ERR_CU_SEQLENS = -3,   /* cu_seqlens not monotone / outside [0, total_T] (device-side)  */
+    GDN_ERR_WORKSPACE = -4,    /* workspace missing or smaller than the _workspace_size answer  */
+    GDN_ERR_LAUNCH = -5,       /* a kernel launch failed (cudaGetLastError after the launch)    */
+    GDN_ERR_TIMEOUT = -6,      /* a bounded device-side wait gave up (device-side)              */
+    GDN_ERR_UNSUPPORTED = -7,  /* head size or feature combination the kernels do not cover     */
+    GDN_ERR_CUDA = -8          /* a CUDA runtime call other than a launch failed                */
+} gdn_status;
+
+/*
+ * gdn_chunk_fwd -- chunked prefill (chunk size 64) over packed, variable-length sequences.
+ * Source: "5. 线性注意力", "Delta Rule 的 Chunk 实现" (stages 1-3) for the algorithm, and
+ * "[LLM Algorithms-2] Gated DeltaNet" sections 4-5 for the result it must equal.
+ *
+ *   q, k          [total_T, H, d_k], qkv_dtype.  Raw; normalised in-kernel when use_qk_l2norm.
+ *   v             [total_T, H, d_v], qkv_dtype.
+ *   g             [total_T, H] fp32, log-decay (g = log alpha <= 0; see gdn_decay_from_logits).
+ *   beta          [total_T, H] fp32, update strength in [0, 1].
+ *   cu_seqlens    device int32 [num_seqs + 1], prefix sums of sequence lengths starting at 0
+ *                 and ending at total_T; NULL means num_seqs sequences of total_T / num_seqs
+ *                 tokens (total_T must then be a multiple of num_seqs).  Chunks never cross a
+ *                 sequence boundary; a shorter last chunk is masked.  Empty sequences are allowed.
+ *   scale         multiplies q after normalisation; scale <= 0 selects 1/sqrt(d_k).
+ *   initial_state [num_seqs, H, d_v, d_k] fp32, or NULL for zeros.
+ *   final_state   [num_seqs, H, d_v, d_k] fp32, or NULL (not written).  May alias
+ *                 initial_state (each sequence's state is read before it is written).
+ *   gate_z        [total_T, H, d_v] fp32, or NULL: out = y.  Otherwise
+ *                 out = norm_weight * y / sqrt(mean_dv(y^2) + norm_eps) * z * sigmoid(z).
+ *   norm_weight   [d_v] fp32 or NULL (ones).
+ *   out           [total_T, H, d_v], element type out_dtype.
+ *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte
+ *                 aligned; may be NULL when that size is 0.
+ */
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int d_k, int d_v,
+                  gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
+                  const float* initial_state, float* final_state,
+                  const float* gate_z, const float* norm_weight, float norm_eps,
+                  void* out, gdn_dtype out_dtype,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace gdn_chunk_fwd needs for these sizes (0 when it needs none). */
+size_t gdn_chunk_fwd_workspace_size(int num_seqs, int total_T, int H, int d_k, int d_v,
+                                    gdn_dtype qkv_dtype);
+
+/*
+ * gdn_recurrent_step -- one decode token for N sequences, state updated in place.
+ * Source: "6.6 Gated DeltaNet", 6.6.8 (decode keeps only S); the update of
+ * "[LLM Algorithms-2] Gated DeltaNet" section 4.  One read and one write of each state.
+ *
+ *   q, k   [N, H, d_k] qkv_dtype;  v [N, H, d_v] qkv_dtype;  g, beta [N, H] fp32.
+ *   state  [N, H, d_v, d_k] fp32, read and overwritten with the new state.
+ *   gate_z [N, H, d_v] fp32 or NULL; norm_weight [d_v] or NULL; as in gdn_chunk_fwd.
+ *   out    [N, H, d_v] of out_dtype; must not overlap state.
+ */
+int gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                       const float* beta, float* state, int N, int H, int d_k, int d_v,
+                       gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
+                       const float* gate_z, const float* norm_weight, float norm_eps,
+                       void* out, gdn_dtype out_dtype, void* stream);
+
+/*
+ * gdn_gate_rmsnorm_silu -- the gated output norm on its own.
+ * Source: "5. 线性注意力", "门控 RMSNorm" (RMSNormGated: weight * norm(x) * silu(z)) and
+ * "6.6 Gated DeltaNet" 6.6.2 (o_t = RMSNorm(y_t) * SiLU(g_t)).  The norm is taken in fp32 over
+ * each row of d_v elements; the output is rounded once, to out_dtype.
+ *
+ *   y [rows, d_v] of y_dtype; z [rows, d_v] fp32; norm_weight [d_v] fp32 or NULL (ones);
+ *   out [rows, d_v] of out_dtype (may alias y when the element types match).
+ *   d_v: a multiple of 32, at most 1024.
+ */
+int gdn_gate_rmsnorm_silu(const void* y, gdn_dtype y_dtype, const float* z,
+                          const float* norm_weight, float eps, void* out, gdn_dtype out_dtype,
+                          long rows, int d_v, void* stream);
+
+/*
+ * gdn_decay_from_logits -- gate preparation.
+ * Source: "6.6 Gated DeltaNet" 6.6.3:  alpha = exp(-A softplus(a + dt_bias)) with A = exp(A_log)
+ * per head, kept in log space as g = -exp(A_log) softplus(a + dt_bias); beta = sigmoid(b).
+ *
+ *   a [total_T, H] fp32; A_log [H] fp32; dt_bias [H] fp32 or NULL (zero);
+ *   b [total_T, H] fp32 or NULL (then beta_out is not written and may be NULL);
+ *   g_out, beta_out [total_T, H] fp32.
+ */
+int gdn_decay_from_logits(const float* a, const float* A_log, const float* dt_bias,
+                          const float* b, float* g_out, float* beta_out, long total_T, int H,
+                          void* stream);
+
+/*
+ * gdn_get_device_error -- synchronise `stream`, then read and clear the device error word of the
+ * current device.  *device_status receives GDN_OK or the first device-side gdn_status recorded
+ * since the last call.  Returns GDN_OK, or GDN_ERR_CUDA if the synchronisation itself failed.
+ */
+int gdn_get_device_error(void* stream, int* device_status);
+
+/* Human-readable name of a gdn_status value (static string). */
+const char* gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,130 @@
+"""GPU parity: one-token decode, the gated output norm and the gate preparation, each through the
+C ABI, against the fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_recurrence_gb300 as gdn
+import oracle
+from gated_deltanet_recurrence_gb300 import synthetic
+from tests._util import TOL_BF16, TOL_F32, oracle_gates, rel_l2_states
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode_case(cfg, out_dtype=torch.float32, gate=False, weight=False, use_l2=True, scale=0.0):
+    inp = synthetic.decode_inputs(cfg)
+    g32, b32 = oracle_gates(inp)
+    dev = "cuda"
+    z = torch.randn(inp["q"].shape[:2] + (inp["v"].shape[-1],), generator=torch.Generator().manual_seed(7)) \
+        if gate else None
+    w = torch.linspace(0.5, 1.5, inp["v"].shape[-1]) if weight else None
+    state = inp["state"].to(dev)
+    out = gdn.gdn_recurrent_step(inp["q"].to(dev), inp["k"].to(dev), inp["v"].to(dev), g32.to(dev),
+                                 b32.to(dev), state, scale=scale, use_qk_l2norm=use_l2,
+                                 gate_z=z.to(dev) if gate else None,
+                                 norm_weight=w.to(dev) if weight else None, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    y_ref, S_ref = oracle.recurrent_step(inp["q"], inp["k"], inp["v"], g32, b32, inp["state"],
+                                         scale=None if scale <= 0 else scale, use_qk_l2norm=use_l2)
+    if gate:
+        y_ref = oracle.gate_rmsnorm_silu(y_ref, z, w)
+    return out.float().cpu(), state.cpu(), y_ref, S_ref
+
+
+def _rel_rows(x, ref):
+    """max over (seq, head) of the relative L2 error over d_v"""
+    x = x.double().numpy().reshape(-1, x.shape[-1])
+    ref = np.asarray(ref).reshape(x.shape)
+    return float(np.max(np.linalg.norm(x - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)))
+
+
+def test_decode_full_size_bf16():
+    """Decode workload: 256 sequences x 32 heads x 128^2 fp32 state, bf16 q/k/v."""
+    y, S, y_ref, S_ref = _decode_case("decode")
+    err_y, err_S = _rel_rows(y, y_ref), rel_l2_states(S, S_ref)
+    assert err_y <= TOL_BF16 and err_S <= TOL_BF16
+    # fp32 arithmetic on exactly upcast inputs: far inside the bf16 tolerance
+    assert err_y < 1e-5 and err_S < 1e-5, (err_y, err_S)
+
+
+def test_decode_bf16_output_and_gate():
+    y, S, y_ref, S_ref = _decode_case("decode", out_dtype=torch.bfloat16, gate=True, weight=True)
+    assert _rel_rows(y, y_ref) <= TOL_BF16
+    assert rel_l2_states(S, S_ref) < 1e-5
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("use_l2", [True, False])
+def test_decode_fp32_inputs(d, use_l2):
+    cfg = synthetic.workload("decode", N=37, H=3, d=d, dtype=torch.float32, seed=11)
+    y, S, y_ref, S_ref = _decode_case(cfg, use_l2=use_l2, scale=0.3 if not use_l2 else 0.0)
+    assert _rel_rows(y, y_ref) <= TOL_F32
+    assert rel_l2_states(S, S_ref) <= TOL_F32
+
+
+def test_decode_gate_fp32_d64():
+    cfg = synthetic.workload("decode", N=5, H=4, d=64, dtype=torch.float32, seed=12)
+    y, S, y_ref, S_ref = _decode_case(cfg, gate=True)
+    assert _rel_rows(y, y_ref) <= TOL_F32
+
+
+def test_decode_repeated_steps_follow_the_recurrence():
+    """Ten decode steps on the kept state equal the oracle's token loop over the ten tokens."""
+    N, H, d, T = 6, 2, 128, 10
+    gen = torch.Generator().manual_seed(13)
+    q, k, v = (torch.randn(T, N, H, d, generator=gen).bfloat16() for _ in range(3))
+    a, b = torch.randn(T, N, H, generator=gen) - 1, torch.randn(T, N, H, generator=gen)
+    A_log = torch.rand(H, generator=gen) * np.log(8)
+    S0 = torch.randn(N, H, d, d, generator=gen) * 0.02
+    state = S0.cuda()
+    outs = []
+    gs, bs = [], []
+    for t in range(T):
+        g_t, b_t = oracle.gates_from_logits(a[t], A_log, b=b[t])
+        g_t, b_t = torch.from_numpy(g_t).float(), torch.from_numpy(b_t).float()
+        gs.append(g_t)
+        bs.append(b_t)
+        outs.append(gdn.gdn_recurrent_step(q[t].cuda(), k[t].cuda(), v[t].cuda(), g_t.cuda(),
+                                           b_t.cuda(), state, out_dtype=torch.float32).cpu())
+    # the same tokens as N sequences of length T in the oracle's packed layout
+    perm = lambda x: x.transpose(0, 1).reshape(N * T, *x.shape[2:])  # noqa: E731
+    cu = np.arange(0, N * T + 1, T, dtype=np.int32)
+    y_ref, S_ref = oracle.recurrence(perm(q), perm(k), perm(v), perm(torch.stack(gs)),
+                                     perm(torch.stack(bs)), cu_seqlens=cu, initial_state=S0)
+    y = perm(torch.stack(outs))
+    assert _rel_rows(y, y_ref) < 1e-4
+    assert rel_l2_states(state.cpu(), S_ref) < 1e-4
+
+
+@pytest.mark.parametrize("d_v", [64, 128, 96, 256])
+@pytest.mark.parametrize("dtypes", [(torch.float32, torch.float32), (torch.bfloat16, torch.bfloat16),
+                                    (torch.float32, torch.bfloat16)])
+def test_gate_rmsnorm_silu(d_v, dtypes):
+    y_dt, o_dt = dtypes
+    gen = torch.Generator().manual_seed(d_v)
+    rows = 1000
+    y = torch.randn(rows, d_v, generator=gen).to(y_dt)
+    z = torch.randn(rows, d_v, generator=gen)
+    w = torch.randn(d_v, generator=gen)
+    out = gdn.gdn_gate_rmsnorm_silu(y.cuda(), z.cuda(), w.cuda(), eps=1e-6, out_dtype=o_dt).float().cpu()
+    ref = oracle.gate_rmsnorm_silu(y, z, w, eps=1e-6)
+    tol = TOL_F32 if o_dt == torch.float32 else TOL_BF16
+    assert _rel_rows(out, ref) <= tol
+
+
+def test_decay_from_logits():
+    gen = torch.Generator().manual_seed(3)
+    T, H = 4097, 16
+    a = torch.randn(T, H, generator=gen) * 3 - 1
+    a[0, :4] = torch.tensor([-60.0, 0.0, 25.0, 80.0])
+    b = torch.randn(T, H, generator=gen) * 3
+    A_log = torch.rand(H, generator=gen) * np.log(8)
+    dt = torch.randn(H, generator=gen)
+    g, beta = gdn.gdn_decay_from_logits(a.cuda(), A_log.cuda(), dt.cuda(), b.cuda())
+    g_ref, beta_ref = oracle.gates_from_logits(a, A_log, dt_bias=dt, b=b)
+    np.testing.assert_allclose(g.cpu().double().numpy(), g_ref, rtol=2e-6, atol=1e-30)
+    np.testing.assert_allclose(beta.cpu().double().numpy(), beta_ref, rtol=2e-6, atol=1e-30)
+    g_only = gdn.gdn_decay_from_logits(a.cuda(), A_log.cuda())
+    np.testing.assert_allclose(g_only.cpu().double().numpy(), oracle.gates_from_logits(a, A_log),
+                               rtol=2e-6, atol=1e-30)
