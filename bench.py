@@ -206,13 +206,15 @@ def bench_prefill(args, dev):
     out = torch.empty(total_T, H, d, dtype=torch.bfloat16, device=dev)
     Sf = torch.empty(n, H, d, d, device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ws_bytes = gdn.lib().gdn_chunk_fwd_workspace_size(n, total_T, H, d, d, gdn.GDN_BF16)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
 
     def step():
         gdn.gdn_decay_from_logits(d_in["a"], d_in["A_log"], b=d_in["b"], g_out=g, beta_out=beta)
         e_mid = ev()
         e_mid.record(stream)
         gdn.gdn_chunk_fwd(d_in["q"], d_in["k"], d_in["v"], g, beta, num_seqs=n,
-                          gate_z=d_in["z"], out=out, final_state=Sf)
+                          gate_z=d_in["z"], out=out, final_state=Sf, workspace=ws)
         return e_mid
 
     for _ in range(args.warmup):
@@ -309,7 +311,17 @@ def run_gdn(args):
     dev = torch.device("cuda", args.local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
+    if args.only == "decode":
+        dc = bench_decode(args, dev)
+        if args.rank == 0:
+            print(json.dumps({"decode_ms": dc["ms"], "decode_kernel_ms": dc["kernel_ms"]}), flush=True)
+        return
     pf = bench_prefill(args, dev)
+    if args.only == "prefill":
+        if args.rank == 0:
+            print(json.dumps({"prefill_ms": pf["ms"], "prefill_kernel_ms": pf["kernel_ms"],
+                              "e2e_ms": pf["e2e_ms"]}), flush=True)
+        return
     dc = bench_decode(args, dev)
     world = args.world
     ms = max_over_ranks(pf["ms"], world)
@@ -399,6 +411,8 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="budget of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="time only one workload (profiling runs); the driver uses the default")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: warm-up raised to 3 steps", file=sys.stderr)

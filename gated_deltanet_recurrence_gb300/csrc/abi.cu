@@ -67,10 +67,17 @@ int gdn_get_device_error(void* stream, int* device_status) {
     return GDN_OK;
 }
 
+// The tensor-core path (bf16, d = 128) keeps per-chunk intermediates (W, U^T, the decayed Q K^T
+// and per-token factors, about 41 KB per chunk and head) in the caller's workspace; the fp32
+// CUDA-core path needs none.
+static bool uses_tc_path(int num_seqs, int total_T, int H, int d_k, int d_v, int qkv_dtype) {
+    return qkv_dtype == GDN_BF16 && d_k == 128 && d_v == 128 && total_T > 0 && num_seqs > 0 && H > 0;
+}
+
 size_t gdn_chunk_fwd_workspace_size(int num_seqs, int total_T, int H, int d_k, int d_v,
                                     gdn_dtype qkv_dtype) {
-    (void)num_seqs; (void)total_T; (void)H; (void)d_k; (void)d_v; (void)qkv_dtype;
-    return 0;
+    if (!uses_tc_path(num_seqs, total_T, H, d_k, d_v, qkv_dtype)) return 0;
+    return gdn::prefill_tc_workspace_bytes(num_seqs, total_T, H);
 }
 
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -105,6 +112,9 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.err = device_error_ptr();
     if (!a.err) return GDN_ERR_CUDA;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_WORKSPACE;
+    if (uses_tc_path(num_seqs, total_T, H, d_k, d_v, qkv_dtype) && gdn::prefill_tc_supported(a))
+        return launch_status(gdn::launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
     return launch_status(gdn::launch_prefill_simt(a, static_cast<cudaStream_t>(stream)));
 }
 

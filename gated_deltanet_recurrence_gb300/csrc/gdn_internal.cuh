@@ -98,4 +98,9 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t s);
 
+// tensor-core prefill (bf16 q/k/v, d_k = d_v = 128): workspace size, availability, launch
+size_t prefill_tc_workspace_bytes(int num_seqs, int total_T, int H);
+bool prefill_tc_supported(const PrefillArgs& a);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
 }  // namespace gdn

@@ -72,9 +72,12 @@ def test_workspace_size_is_consistent():
     L = gdn.lib()
     for (n, T, H) in [(1, 256, 2), (2, 8192, 16), (64, 262144, 16)]:
         ws = L.gdn_chunk_fwd_workspace_size(n, T, H, 128, 128, 1)
-        assert ws >= 0
-        if ws > 0:
-            assert _chunk(num_seqs=n, total_T=T, H=H, ws=NUL, wsb=0) == -4
+        assert ws > 0                               # bf16, d = 128: tensor-core path
+        assert _chunk(num_seqs=n, total_T=T, H=H, dt=1, odt=1, ws=NUL, wsb=0) == -4
+        assert _chunk(num_seqs=n, total_T=T, H=H, dt=1, odt=1, ws=P, wsb=ws - 1) == -4
+        # fp32 inputs and d = 64 run the CUDA-core path, which needs none
+        assert L.gdn_chunk_fwd_workspace_size(n, T, H, 128, 128, 0) == 0
+        assert L.gdn_chunk_fwd_workspace_size(n, T, H, 64, 64, 1) == 0
 
 
 def test_recurrent_step_rejects_bad_arguments():
