@@ -8,6 +8,7 @@ from ._binding import (  # noqa: F401
     GDN_F32,
     GdnError,
     gdn_chunk_fwd,
+    gdn_chunk_fwd_noalloc,
     gdn_decay_from_logits,
     gdn_gate_rmsnorm_silu,
     gdn_get_device_error,
@@ -15,5 +16,5 @@ from ._binding import (  # noqa: F401
     lib,
 )
 
-__all__ = ["gdn_chunk_fwd", "gdn_recurrent_step", "gdn_gate_rmsnorm_silu", "gdn_decay_from_logits",
+__all__ = ["gdn_chunk_fwd", "gdn_chunk_fwd_noalloc", "gdn_recurrent_step", "gdn_gate_rmsnorm_silu", "gdn_decay_from_logits",
            "gdn_get_device_error", "GdnError", "lib", "GDN_F32", "GDN_BF16"]

@@ -35,6 +35,8 @@ SIGNATURES = {
                                 _f, _vp, _i, _vp]),
     "gdn_gate_rmsnorm_silu": (_i, [_vp, _i, _fp, _fp, _f, _vp, _i, _l, _i, _vp]),
     "gdn_decay_from_logits": (_i, [_fp, _fp, _fp, _fp, _fp, _fp, _l, _i, _vp]),
+    "gdn_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
+                                   _fp, _fp, _f, _vp, _i, _vp]),
     "gdn_get_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "gdn_status_string": (ctypes.c_char_p, [_i]),
 }
@@ -144,6 +146,33 @@ def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0, u
                          _p(workspace), workspace.numel() if workspace is not None else 0,
                          _stream(stream))
     _check("gdn_chunk_fwd", rc)
+    return out, final_state
+
+
+def gdn_chunk_fwd_noalloc(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0,
+                          use_qk_l2norm=True, initial_state=None, final_state=None, gate_z=None,
+                          norm_weight=None, norm_eps=1e-6, out=None, stream=None):
+    """gdn_chunk_fwd with the library's fixed scratch array instead of a workspace; `out` and
+    `final_state` must be passed in (this call allocates nothing, here or in the library)."""
+    total_T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if out is None:
+        raise ValueError("gdn_chunk_fwd_noalloc needs a preallocated `out`")
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        num_seqs = cu_seqlens.numel() - 1
+    elif num_seqs is None:
+        num_seqs = 1
+    dt = _dt(q)
+    for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state),
+                    ("final_state", final_state), ("gate_z", gate_z), ("norm_weight", norm_weight)):
+        _f32(t, name)
+    rc = lib().gdn_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs,
+                                     total_T, H, d_k, d_v, dt, float(scale), int(bool(use_qk_l2norm)),
+                                     _p(initial_state), _p(final_state), _p(gate_z), _p(norm_weight),
+                                     float(norm_eps), _p(out), _dt(out), _stream(stream))
+    _check("gdn_chunk_fwd_noalloc", rc)
     return out, final_state
 
 

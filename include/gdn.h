@@ -130,6 +130,32 @@ int gdn_decay_from_logits(const float* a, const float* A_log, const float* dt_bi
                           void* stream);
 
 /*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call; it exists for callers that have no allocator at hand
+ * when they run the prefill (code running inside a framework that owns the device memory pool,
+ * a process that must not grow its footprint after start-up, a host program holding only raw
+ * pointers to buffers owned elsewhere), so cannot provide gdn_chunk_fwd's workspace.
+ *
+ * Arguments, layouts and results are those of gdn_chunk_fwd, without the workspace.  The scratch
+ * lives in a fixed array of GDN_NOALLOC_SCRATCH_BYTES inside the library's device image, which
+ * every GPU that loads libgdn.so holds until the process exits; nothing is allocated or freed.
+ *   - Sizes whose workspace need (gdn_chunk_fwd_workspace_size) exceeds GDN_NOALLOC_SCRATCH_BYTES
+ *     are rejected with GDN_ERR_WORKSPACE before anything is launched.
+ *   - All calls share the one array per device and it keeps the last call's contents (the call
+ *     writes every scratch word before reading it, so nothing needs clearing).  Calls that overlap
+ *     on the GPU race on it: order them on one stream.
+ *   - The first call on a device looks up the array's device address; make that first call before
+ *     any stream capture that contains this entry point.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, const int32_t* cu_seqlens, int num_seqs, int total_T,
+                          int H, int d_k, int d_v, gdn_dtype qkv_dtype, float scale,
+                          int use_qk_l2norm, const float* initial_state, float* final_state,
+                          const float* gate_z, const float* norm_weight, float norm_eps,
+                          void* out, gdn_dtype out_dtype, void* stream);
+
+/*
  * gdn_get_device_error -- synchronise `stream`, then read and clear the device error word of the
  * current device.  *device_status receives GDN_OK or the first device-side gdn_status recorded
  * since the last call.  Returns GDN_OK, or GDN_ERR_CUDA if the synchronisation itself failed.
