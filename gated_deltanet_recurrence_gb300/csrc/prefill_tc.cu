@@ -25,7 +25,7 @@
 //                       the state epilogue (the serial chain: V_new, then S), warps 8-11 the
 //                       output epilogue (O and the fused RMSNorm * SiLU gate).  The state S is fp32 in TMEM (lanes = rows d_v,
 //                       columns = d_k) and is mirrored as a bf16 operand tile in shared memory.
-//   TMEM per state CTA: S [0,128), two buffers of S [W;Q]^T [128,384), two of A1 Aqk^T [384,512).
+//   TMEM per state CTA: S [0,128), two buffers of S W^T [128,256), two of O (tokens as rows) [256,512).
 //
 // Every mbarrier wait is bounded; on a timeout the kernel records GDN_ERR_TIMEOUT and its roles
 // stop issuing work, wait (bounded) for what they issued, free TMEM and return.
@@ -48,7 +48,7 @@ constexpr uint64_t kPolls = 2000000000ull;  // bound on any single mbarrier wait
 
 struct WsLayout {
     long nch;          // chunk-head slots = max_chunks * H
-    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, total;
+    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, total;
 };
 
 __host__ __device__ inline long max_chunks(int num_seqs, int total_T) { return (long)total_T / kC + num_seqs; }
@@ -66,6 +66,8 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
     w.off_Ut = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kD * kC);
     w.off_Aqk = o;   o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kC);
     w.off_scal = o;  o = al(o + sizeof(float) * w.nch * 4 * kC);
+    w.off_Qt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^gc qs) Q
+    w.off_Kt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^(glast-gc) kinv) K
     w.total = o;
     return w;
 }
@@ -84,6 +86,8 @@ struct TcArgs {
     __nv_bfloat16* Ut;
     __nv_bfloat16* Aqk;
     float* scal;
+    __nv_bfloat16* Qt;
+    __nv_bfloat16* Kt;
     const float* initial_state;
     float* final_state;
     const float* z;
@@ -144,8 +148,15 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
 
 // ---- shared helpers --------------------------------------------------------------------------------
 
-// logistic function for the output gate (its result is rounded to the output type right after)
-__device__ __forceinline__ float fast_sigmoid(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+// SiLU for the output gate, from sigma(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh
+// approximation (relative error near 5e-4, below the bf16 rounding of the output that follows):
+// x sigma(x) = h + h tanh(h) with h = x / 2.
+__device__ __forceinline__ float fast_silu(float x) {
+    const float hx = 0.5f * x;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hx));
+    return fmaf(hx, t, hx);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
@@ -178,13 +189,14 @@ __device__ __forceinline__ void ld_sw128_chunk(const uint8_t* tile, int row, int
 
 namespace prep {
 constexpr int kThreads = 128;
-constexpr int LD = kC + 1;  // padded fp32 64x64 tiles
+constexpr int LDA = kC + 1;  // A (fp32 64x64): odd stride, conflict-free row/column access
+constexpr int LD = kC + 4;   // T and the block scratch: rows stay 16-byte aligned for float4 loads
 constexpr uint32_t oKQ = 0;          // 2 atom columns x (K rows 0-63, Q rows 64-127) = 32 KB
 constexpr uint32_t oV = 32768;       // 2 atom columns x 64 rows = 16 KB
 constexpr uint32_t oTP = 49152;      // T' (bf16 SW128 64x64) 8 KB
 constexpr uint32_t oTPP = 57344;     // T'' 8 KB
 constexpr uint32_t oAf = 65536;      // A (fp32 64 x 65); later the W staging tile (bf16 64x128)
-constexpr uint32_t oTf = oAf + 4 * kC * LD;       // T (fp32 64 x 65)
+constexpr uint32_t oTf = oAf + 16896;             // T (fp32 64 x 68), 1 KB past A
 constexpr uint32_t oSc = oTf + 4 * kC * LD;       // gc, beta, kinv, qs (fp32 x 64 each)
 constexpr uint32_t oBar = oSc + 4 * 4 * kC;       // 2 mbarriers + TMEM base
 constexpr uint32_t kBytes = oBar + 64;
@@ -192,11 +204,29 @@ constexpr uint32_t kSmem = kBytes + 1024;          // + alignment slack
 constexpr uint32_t kTmemCols = 256;
 }  // namespace prep
 
-// Blocked inverse of the unit lower-triangular 64x64 matrix I + A (A strictly lower, fp32 in Af with
-// row stride LD) into Tf.  Diagonal 16x16 blocks by forward substitution (one warp per block, one
-// lane per column), then block rows 1..3 by T_bj = -T_bb sum_{k=j}^{b-1} A_bk T_kj.
+// C[16 x 16] (+)= P[16 x 16] Q[16 x 16] for one warp: lane l owns row l / 2 and the 8 columns
+// 8 (l % 2) .. 8 (l % 2) + 7 of C, kept in registers.  P and Q are fp32 tiles in shared memory
+// with row strides LDP and LDQ (LDQ a multiple of 4: each 8-column half row is two 16-byte loads).
+template <int LDP, int LDQ>
+__device__ __forceinline__ void warp_mm16(const float* P, const float* Q, float (&c)[8], int lane) {
+    const int ii = lane >> 1, c0 = (lane & 1) * 8;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float p = P[ii * LDP + k];
+        const float4 q0 = *reinterpret_cast<const float4*>(Q + k * LDQ + c0);
+        const float4 q1 = *reinterpret_cast<const float4*>(Q + k * LDQ + c0 + 4);
+        c[0] = fmaf(p, q0.x, c[0]); c[1] = fmaf(p, q0.y, c[1]); c[2] = fmaf(p, q0.z, c[2]); c[3] = fmaf(p, q0.w, c[3]);
+        c[4] = fmaf(p, q1.x, c[4]); c[5] = fmaf(p, q1.y, c[5]); c[6] = fmaf(p, q1.z, c[6]); c[7] = fmaf(p, q1.w, c[7]);
+    }
+}
+
+// Blocked inverse of the unit lower-triangular 64x64 matrix I + A (A strictly lower, fp32 in Af
+// with row stride LDA) into Tf (row stride LD).  The four diagonal 16x16 blocks by forward
+// substitution (one warp per block, one lane per column); then block rows 1..3 in order,
+// T_bj = -T_bb sum_{k=j}^{b-1} A_bk T_kj, one warp per block (b, j) with the 16x16 products held
+// in registers; X is a per-warp 16 x LD scratch (warps 0-2 only: 3 x 16 x 68 x 4 B = 13 KB).
 __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid) {
-    constexpr int LD = prep::LD;
+    constexpr int LD = prep::LD, LDA = prep::LDA;
     const int warp = tid >> 5, lane = tid & 31;
     {   // diagonal blocks
         const int b0 = warp * 16;
@@ -205,11 +235,13 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
             float t[16];
 #pragma unroll
             for (int ii = 0; ii < 16; ++ii) {
-                float acc = 0.f;
+                float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < ii; ++m)
-                    if (m >= jj) acc += Af[(b0 + ii) * LD + b0 + m] * t[m];
-                t[ii] = ii < jj ? 0.f : (ii == jj ? 1.f : -acc);
+                for (int m = 0; m < ii; ++m) {
+                    const float v = m >= jj ? Af[(b0 + ii) * LDA + b0 + m] * t[m] : 0.f;
+                    if (m & 1) acc1 += v; else acc0 += v;
+                }
+                t[ii] = ii < jj ? 0.f : (ii == jj ? 1.f : -(acc0 + acc1));
             }
 #pragma unroll
             for (int ii = 0; ii < 16; ++ii) Tf[(b0 + ii) * LD + b0 + jj] = t[ii];
@@ -221,23 +253,25 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
         }
     }
     bar_sync(2, prep::kThreads);
+    float* Xw = X + warp * 16 * LD;
+    const int ii = lane >> 1, c0 = (lane & 1) * 8;
     for (int b = 1; b < 4; ++b) {
-        const int nel = b * 256;  // elements of block row b left of the diagonal
-        // X_bj = sum_{k=j}^{b-1} A_bk T_kj   (16 x 16 each), stored in X[16][b*16]
-        for (int e = tid; e < nel; e += prep::kThreads) {
-            const int ii = e / (b * 16), col = e % (b * 16);  // col in [0, 16b)
-            const int j = col / 16;
-            float acc = 0.f;
-            for (int m = j * 16; m < b * 16; ++m) acc += Af[(b * 16 + ii) * LD + m] * Tf[m * LD + col];
-            X[ii * LD + col] = acc;
-        }
-        bar_sync(2, prep::kThreads);
-        for (int e = tid; e < nel; e += prep::kThreads) {
-            const int ii = e / (b * 16), col = e % (b * 16);
-            float acc = 0.f;
+        const int j = warp;  // block column handled by this warp (warps j >= b idle in this row)
+        if (j < b) {
+            float c[8];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc += Tf[(b * 16 + ii) * LD + b * 16 + m] * X[m * LD + col];
-            Tf[(b * 16 + ii) * LD + col] = -acc;
+            for (int e = 0; e < 8; ++e) c[e] = 0.f;
+            for (int k = j; k < b; ++k)
+                warp_mm16<LDA, LD>(Af + (b * 16) * LDA + k * 16, Tf + (k * 16) * LD + j * 16, c, lane);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Xw[ii * LD + c0 + e] = c[e];
+            __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[e] = 0.f;
+            warp_mm16<LD, LD>(Tf + (b * 16) * LD + b * 16, Xw, c, lane);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Tf[(b * 16 + ii) * LD + j * 16 + c0 + e] = -c[e];
+            __syncwarp();
         }
         bar_sync(2, prep::kThreads);
     }
@@ -381,7 +415,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             const float gi = gcs[i], f = bts[i] * kinv[i];
 #pragma unroll
             for (int j = 0; j < 64; ++j)
-                Af[i * LD + j] = j < i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
+                Af[i * LDA + j] = j < i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
             // per-token factors for the state pass
             float* sc = a.scal + gh * 4 * kC;
             const float glast = gcs[kC - 1];
@@ -405,22 +439,39 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                                      pack_bf16x2(v[6], v[7]));
             }
         }
+        // ---- scaled operand rows for the state pass: K~ = diag(e^(glast-gc) kinv) K (thread i < 64),
+        //      Q~ = diag(e^gc qs) Q (thread 64 + i); one 256-byte row per thread ----
+        {
+            const int i = tid & 63, isq = tid >> 6;
+            const float f = isq ? __expf(gcs[i]) * qsv[i] : __expf(gcs[kC - 1] - gcs[i]) * kinv[i];
+            const uint8_t* src = sm + oKQ + (isq ? 8192 : 0);
+            uint4* dst = reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)i * kD);
+#pragma unroll
+            for (int c16 = 0; c16 < 16; ++c16) {
+                float v[8];
+                ld_sw128_chunk(src + (c16 >> 3) * 16384, i, c16 & 7, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= f;
+                dst[c16] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                      pack_bf16x2(v[6], v[7]));
+            }
+        }
         __syncthreads();
         // ---- T = (I + A)^-1 (the 16 x 48 fp32 scratch of the block steps lives in the T' tile,
         //      which is written only after the inverse is complete) ----
-        unit_lower_inverse(Af, Tf, reinterpret_cast<float*>(sm + oTP), tid);
+        unit_lower_inverse(Af, Tf, reinterpret_cast<float*>(sm + oTP), tid);  // scratch: T' / T'' tiles
         // ---- T' = T diag(beta e^gc kinv) and T'' = T diag(beta) as bf16 SW128 operand tiles ----
+        if (tid < kC) qsv[tid] = bts[tid] * __expf(gcs[tid]) * kinv[tid];  // q factors no longer needed
+        __syncthreads();
         {
             const int i = tid & 63, which = tid >> 6;
             uint8_t* dst = sm + (which ? oTPP : oTP);
-            float v[8];
-            for (int c8 = 0; c8 < 8; ++c8) {
+            const float* cfv = which ? bts : qsv;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = c8 * 8 + e;
-                    const float cf = which ? bts[j] : bts[j] * __expf(gcs[j]) * kinv[j];
-                    v[e] = Tf[i * LD + j] * cf;
-                }
+            for (int c8 = 0; c8 < 8; ++c8) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = Tf[i * LD + c8 * 8 + e] * cfv[c8 * 8 + e];
                 st_sw128_chunk(dst, i, c8, v);
             }
         }
@@ -499,28 +550,29 @@ constexpr int kThreads = 384;               // 12 warps = 3 warpgroups
 constexpr int kRegsLow = 80, kRegsHigh = 208;
 constexpr uint32_t oS = 0;                  // S bf16 operand: 2 atom columns x 128 rows = 32 KB
 constexpr uint32_t oA1 = 32768;             // V_new^T bf16 [128 x 64] SW128 = 16 KB
-constexpr uint32_t oA2 = 49152;             // V_new^T diag(kfac) = 16 KB
-constexpr uint32_t oStage = 65536;          // two stages
+constexpr uint32_t oStage = 49152;          // two stages
 // stage layout
-constexpr uint32_t sWQ = 0;                 // 2 atom columns x (W rows 0-63, Q rows 64-127) = 32 KB
-constexpr uint32_t sK = 32768;              // 2 atom columns x 64 rows = 16 KB
+constexpr uint32_t sWQ = 0;                 // 2 atom columns x (W rows 0-63, Q~ rows 64-127) = 32 KB
+constexpr uint32_t sK = 32768;              // K~: 2 atom columns x 64 rows = 16 KB
 constexpr uint32_t sAqk = 49152;            // 64 x 64 = 8 KB
-constexpr uint32_t sScal = 57344;           // 4 x 64 fp32 = 1 KB
-constexpr uint32_t kStage = 58368;          // multiple of 1024
-constexpr uint32_t oOt = oStage + 2 * kStage;    // output tile fp32 [64 tokens][128] = 32 KB
-constexpr uint32_t oQs = oOt + 32768;            // output row factors of the current chunk (64 fp32)
-constexpr uint32_t oBar = oQs + 256;
+constexpr uint32_t kStage = 57344;          // multiple of 1024
+constexpr uint32_t oZ = oStage + 2 * kStage;     // gate input z, two buffers of 4 boxes of
+                                                 // [64 tokens][32 fp32] SW128 = 2 x 32 KB
+constexpr uint32_t oBar = oZ + 2 * 32768;
 constexpr uint32_t kBytes = oBar + 256;
 constexpr uint32_t kSmem = kBytes + 1024;
-constexpr uint32_t kStageTx = 32768 + 16384 + 8192 + 1024;
+constexpr uint32_t kStageTx = 32768 + 16384 + 8192;
 // barriers
-enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF, DA1, A12, SFULL, DA2_0, DA2_1, DO_0, DO_1, DAE_0, DAE_1, NBAR };
+enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF, DA1, A12, SFULL, DO_0, DO_1, DOE_0, DOE_1, ZFULL0, ZFULL1, NBAR };
 constexpr uint32_t kTmemCols = 512;
 }  // namespace st
 
+// TMEM columns of the state CTA: S [0,128); S W^T (M=128, 64 columns) x 2 buffers [128,256);
+// O = Q~ S^T + Aqk V_new (M=64, rows = tokens, 128 columns) x 2 buffers [256,512).
 __global__ void __launch_bounds__(st::kThreads, 1)
-chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                   const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mAqk, TcArgs a) {
+chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constant__ CUtensorMap mKt,
+                   const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mAqk,
+                   const __grid_constant__ CUtensorMap mZ, TcArgs a) {
     using namespace st;
     extern __shared__ uint8_t smraw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
@@ -529,8 +581,6 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 8 * NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oBar + 8 * NBAR + 4);
-    float* otile = reinterpret_cast<float*>(sm + oOt);
-    float* qs_s = reinterpret_cast<float*>(sm + oQs);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x;
@@ -541,11 +591,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     const int first = a.chunk_first[n];
 
     if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) {
-            uint32_t cnt = 1;
-            if (i == EMPTY0 || i == EMPTY1) cnt = 2;  // MMA commit + state epilogue
-            mbar_init(&bars[i], cnt);
-        }
+        for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -557,7 +603,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tbase;
-    const uint32_t tS = tm, tDA0 = tm + 128, tDO0 = tm + 384;
+    const uint32_t tS = tm, tDA0 = tm + 128, tDO0 = tm + 256;
 
     auto stage_ptr = [&](int s) { return sm + oStage + s * kStage; };
     auto fail = [&]() {
@@ -575,19 +621,14 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 if (c >= 2 && !mbar_wait(&bars[EMPTY0 + s], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
                 if (*abort_flag) break;
                 uint8_t* sp = stage_ptr(s);
-                const long gh = (long)(first + c) * a.H + h;
-                const int t0 = (int)(bos + (long)c * kC);
+                const int row = (int)(((long)(first + c) * a.H + h) * kC);
                 mbar_arrive_expect_tx(&bars[FULL0 + s], kStageTx);
                 for (int ac = 0; ac < 2; ++ac) {
-                    tma_load_2d(sp + sWQ + ac * 16384, &mW, &bars[FULL0 + s], ac * 64, (int)(gh * kC));
-                    tma_load_3d(sp + sWQ + ac * 16384 + 8192, &mQ, &bars[FULL0 + s], ac * 64, h, t0);
-                    tma_load_3d(sp + sK + ac * 8192, &mK, &bars[FULL0 + s], ac * 64, h, t0);
+                    tma_load_2d(sp + sWQ + ac * 16384, &mW, &bars[FULL0 + s], ac * 64, row);
+                    tma_load_2d(sp + sWQ + ac * 16384 + 8192, &mQt, &bars[FULL0 + s], ac * 64, row);
+                    tma_load_2d(sp + sK + ac * 8192, &mKt, &bars[FULL0 + s], ac * 64, row);
                 }
-                tma_load_2d(sp + sAqk, &mAqk, &bars[FULL0 + s], 0, (int)(gh * kC));
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                    ::"r"(smem_u32(sp + sScal)), "l"(a.scal + gh * 4 * kC), "r"(1024u), "r"(smem_u32(&bars[FULL0 + s]))
-                    : "memory");
+                tma_load_2d(sp + sAqk, &mAqk, &bars[FULL0 + s], 0, row);
             }
             // drain: wait until the last issued stages have landed before the CTA may exit
             for (int c = max(0, nck - 2); c < nck; ++c) mbar_wait(&bars[FULL0 + (c & 1)], (c >> 1) & 1, kPolls);
@@ -598,42 +639,43 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
             // descriptors: the K step adds (bytes >> 4) to the start-address field
             const uint64_t dS = sdesc_sw128(smem_u32(sm + oS), 16, 1024);
             const uint64_t dA1 = sdesc_sw128(smem_u32(sm + oA1), 16, 1024);
-            const uint64_t dA2 = sdesc_sw128(smem_u32(sm + oA2), 16, 1024);
             const uint64_t dStage0 = sdesc_sw128(smem_u32(stage_ptr(0)), 16, 1024);
             const uint64_t dStageK0 = sdesc_sw128(smem_u32(stage_ptr(0) + sK), 8192, 1024);
-            constexpr uint32_t kIdA = idesc_bf16(128, 64, 0, 0), kIdS = idesc_bf16(128, 128, 0, 1);
+            constexpr uint32_t kIdW = idesc_bf16(128, 64, 0, 0);   // S W^T
+            constexpr uint32_t kIdO = idesc_bf16(64, 128, 0, 0);   // Q~ S^T and Aqk V_new
+            constexpr uint32_t kIdS = idesc_bf16(128, 128, 0, 1);  // V_new^T K~ (K~ MN-major)
             for (int c = 0; c < nck; ++c) {
                 const int s = c & 1, b = c & 1;
                 const uint64_t dSt = dStage0 + (uint64_t)((s * kStage) >> 4);
                 const uint64_t dK = dStageK0 + (uint64_t)((s * kStage) >> 4);
                 if (!mbar_wait(&bars[FULL0 + s], (c >> 1) & 1, kPolls)) { fail(); break; }
                 if (!mbar_wait(&bars[SBF], c & 1, kPolls)) { fail(); break; }
-                if (c >= 2 && !mbar_wait(&bars[DAE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
+                if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
                 if (*abort_flag) break;
                 tc_fence_after();
-                const uint32_t tDA = tDA0 + b * 128, tDO = tDO0 + b * 64;
-                // S [W;Q]^T, W part first (the serial chain needs it)
+                const uint32_t tDA = tDA0 + b * 64, tDO = tDO0 + b * 128;
+                // the serial chain first: S W^T
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-                    mma_bf16_ss(tDA, dS + off, dSt + sWQ / 16 + off, kIdA, k > 0);
+                    mma_bf16_ss(tDA, dS + off, dSt + sWQ / 16 + off, kIdW, k > 0);
                 }
                 mma_commit(&bars[DA1]);
+                // while the state epilogue forms V_new: O = Q~ S^T (tokens as rows, M = 64)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-                    mma_bf16_ss(tDA + 64, dS + off, dSt + (sWQ + 8192) / 16 + off, kIdA, k > 0);
+                    mma_bf16_ss(tDO, dSt + (sWQ + 8192) / 16 + off, dS + off, kIdO, k > 0);
                 }
-                mma_commit(&bars[DA2_0 + b]);
                 if (!mbar_wait(&bars[A12], c & 1, kPolls)) { fail(); break; }
                 tc_fence_after();
-                // S += (V_new^T diag(kfac)) K      (K is the MN-major B operand)
+                // S += V_new^T K~   (TMEM S was pre-decayed by this chunk's gamma)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_bf16_ss(tS, dA2 + k * 2, dK + k * 128, kIdS, 1);
+                for (int k = 0; k < 4; ++k) mma_bf16_ss(tS, dA1 + k * 2, dK + k * 128, kIdS, 1);
                 mma_commit(&bars[SFULL]);
-                // O_intra^T = V_new^T Aqk^T
+                // O += Aqk V_new   (B = V_new^T rows, K-major)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_bf16_ss(tDO, dA1 + k * 2, dSt + sAqk / 16 + k * 2, kIdA, k > 0);
+                for (int k = 0; k < 4; ++k) mma_bf16_ss(tDO, dSt + sAqk / 16 + k * 2, dA1 + k * 2, kIdO, 1);
                 mma_commit(&bars[DO_0 + b]);
                 mma_commit(&bars[EMPTY0 + s]);
             }
@@ -651,11 +693,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
         {
             const float* src = a.initial_state ? a.initial_state + ((long)unit * kD + r) * kD : nullptr;
             float* dst = (nck == 0 && a.final_state) ? a.final_state + ((long)unit * kD + r) * kD : nullptr;
-            float g0 = 0.f;
-            if (nck > 0) {
-                if (mbar_wait(&bars[FULL0], 0, kPolls)) g0 = reinterpret_cast<const float*>(stage_ptr(0) + sScal)[3 * kC];
-                else fail();
-            }
+            const float g0 = nck > 0 ? __ldg(a.scal + ((long)first * a.H + h) * 4 * kC + 3 * kC) : 0.f;
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
                 float f[32];
@@ -693,9 +731,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
             for (int c8 = 0; c8 < 8; ++c8) up_next[c8] = __ldg(src + c8);
         }
         for (int c = 0; c < nck; ++c) {
-            const int s = c & 1, b = c & 1;
-            const uint8_t* sp = stage_ptr(s);
-            const float* scal = reinterpret_cast<const float*>(sp + sScal);
+            const int b = c & 1;
             const long gh = (long)(first + c) * a.H + h;
             const bool last = (c + 1 == nck);
             // U^T row r comes straight from the workspace, loaded one chunk ahead; so does the next
@@ -709,13 +745,16 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) up_next[c8] = __ldg(src + c8);
             }
-            if (!mbar_wait(&bars[DA1], c & 1, kPolls)) { fail(); break; }
+            // A failed (timed-out) wait skips the work but still reaches the group barrier, so the
+            // whole group leaves the loop together.
+            bool ok = mbar_wait(&bars[DA1], c & 1, kPolls);
+            if (!ok) fail();
             tc_fence_after();
             // ---- V_new^T row r = U^T row r - (S W^T) row r, 32 tokens at a time ----
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = 0; hf < 2 && ok; ++hf) {
                 uint32_t v[32];
-                tmem_ld32(tDA0 + b * 128 + lrow + 32 * hf, v);
+                tmem_ld32(tDA0 + b * 64 + lrow + 32 * hf, v);
                 tmem_wait_ld();
                 float u[32];
 #pragma unroll
@@ -731,23 +770,17 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 }
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(sm + oA1, r, 4 * hf + c8, u + 8 * c8);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) u[i] *= scal[kC + 32 * hf + i];
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(sm + oA2, r, 4 * hf + c8, u + 8 * c8);
             }
             fence_async_smem();
             tc_fence_before();
-            bar_sync(1, 128);
-            if (r == 0) {
-                mbar_arrive(&bars[A12]);
-                mbar_arrive(&bars[EMPTY0 + s]);
-            }
-            if (!mbar_wait(&bars[SFULL], c & 1, kPolls)) { fail(); break; }
+            if (bar_sync_or(1, 128, *abort_flag != 0)) break;
+            if (r == 0) mbar_arrive(&bars[A12]);
+            ok = mbar_wait(&bars[SFULL], c & 1, kPolls);
+            if (!ok) fail();
             tc_fence_after();
             // ---- S: mirror as bf16 operand, pre-decay by the next chunk's gamma ----
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
+            for (int blk = 0; blk < 4 && ok; ++blk) {
                 uint32_t v[32];
                 tmem_ld32(tS + lrow + blk * 32, v);
                 tmem_wait_ld();
@@ -774,99 +807,110 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 tmem_wait_st();
                 fence_async_smem();
                 tc_fence_before();
-                bar_sync(1, 128);
+                if (bar_sync_or(1, 128, *abort_flag != 0)) break;
                 if (r == 0) mbar_arrive(&bars[SBF]);
             }
         }
     } else {
         // ================= output epilogue (O and the gate) =================
-        // Phase 1 (thread = column r = TMEM lane): o[r][i] = qsc_i (Q S^T)[i][r] + (Aqk V_new)[i][r]
-        // into the fp32 tile otile[i][r].  Phase 2 (warp = token row): RMS over the row, gate with
-        // z, vectorised stores.  Reads nothing from the operand ring, so it never holds it up.
+        // O has tokens as rows (M = 64): token i lives in TMEM lane 32 (i / 16) + i % 16, so each of
+        // lanes 0-15 of the four warps owns one whole output row: the RMS over d_v is a private sum,
+        // z comes from a TMA-filled shared tile and the row is stored contiguously.
         const int q4 = warp & 3;
-        const int r = q4 * 32 + lane;
-        const int wq = warp - 8;               // 0..3 within the group
+        const int i = q4 * 16 + lane;          // token row of this thread (valid for lane < 16)
+        const bool rowthr = lane < 16;
         const uint32_t lrow = static_cast<uint32_t>(q4 * 32) << 16;
         const long tok_stride = (long)a.H * kD;
-        float4 w4 = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (a.w) w4 = *reinterpret_cast<const float4*>(a.w + 4 * lane);
-        float qa_n = 0.f, qb_n = 0.f;
-        float4 zf_n[kC / 4];
-        auto og_prefetch = [&](int cn) {
-            const long ghn = (long)(first + cn) * a.H + h;
-            const long tn = bos + (long)cn * kC;
-            const int Ln = (eos - tn < kC) ? (int)(eos - tn) : kC;
-            if (wq == 0) {
-                qa_n = __ldg(a.scal + ghn * 4 * kC + lane);
-                qb_n = __ldg(a.scal + ghn * 4 * kC + 32 + lane);
-            }
-#pragma unroll
-            for (int m = 0; m < kC / 4; ++m) {
-                const int i = wq + 4 * m;
-                zf_n[m] = (a.z && i < Ln)
-                              ? __ldg(reinterpret_cast<const float4*>(a.z + (tn + i) * tok_stride + (long)h * kD) + lane)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        const bool leader = (warp == 8 && lane == 0);
+        // z of chunk c goes to buffer c & 1; it is requested two chunks ahead
+        auto issue_z = [&](int cz) {
+            const int t0z = (int)(bos + (long)cz * kC);
+            uint64_t* zb = &bars[ZFULL0 + (cz & 1)];
+            mbar_arrive_expect_tx(zb, 32768);
+            for (int cb = 0; cb < 4; ++cb)
+                tma_load_3d(sm + oZ + (cz & 1) * 32768 + cb * 8192, &mZ, zb, cb * 32, h, t0z);
         };
-        if (nck > 0) og_prefetch(0);
+        if (a.z && leader) {
+            if (nck > 0) issue_z(0);
+            if (nck > 1) issue_z(1);
+        }
         for (int c = 0; c < nck; ++c) {
             const int b = c & 1;
             const long t0 = bos + (long)c * kC;
             const int L = (eos - t0 < kC) ? (int)(eos - t0) : kC;
-            const long gh = (long)(first + c) * a.H + h;
-            (void)gh;
-            // this chunk's row factors and z rows were loaded one chunk ago; start the next chunk's
-            const float qa = qa_n, qb = qb_n;
-            float4 zf[kC / 4];
-#pragma unroll
-            for (int m = 0; m < kC / 4; ++m) zf[m] = zf_n[m];
-            if (c + 1 < nck) og_prefetch(c + 1);
-            if (!mbar_wait(&bars[DA2_0 + b], (c >> 1) & 1, kPolls)) { fail(); break; }
-            if (!mbar_wait(&bars[DO_0 + b], (c >> 1) & 1, kPolls)) { fail(); break; }
+            bool ok = mbar_wait(&bars[DO_0 + b], (c >> 1) & 1, kPolls);
+            if (!ok) fail();
             tc_fence_after();
-            if (wq == 0) {
-                qs_s[lane] = qa;
-                qs_s[32 + lane] = qb;
-            }
-            bar_sync(4, 128);                  // qs_s of this chunk is visible
+            float o[kD];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t p[32], q[32];
-                tmem_ld32(tDA0 + b * 128 + 64 + 32 * hf + lrow, p);
-                tmem_ld32(tDO0 + b * 64 + 32 * hf + lrow, q);
+            for (int blk = 0; blk < 4 && ok; ++blk) {
+                uint32_t v[32];
+                tmem_ld32(tDO0 + b * 128 + blk * 32 + lrow, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    otile[(32 * hf + i) * kD + r] = qs_s[32 * hf + i] * __uint_as_float(p[i]) + __uint_as_float(q[i]);
+                for (int j = 0; j < 32; ++j) o[blk * 32 + j] = __uint_as_float(v[j]);
             }
             tc_fence_before();
-            bar_sync(4, 128);
-            if (r == 0) mbar_arrive(&bars[DAE_0 + b]);
+            if (bar_sync_or(4, 128, *abort_flag != 0)) break;
+            if (leader) mbar_arrive(&bars[DOE_0 + b]);
+            float rinv = 1.0f;
+            const uint8_t* zt = sm + oZ + (c & 1) * 32768;
+            if (a.z) {
+                ok = mbar_wait(&bars[ZFULL0 + (c & 1)], (c >> 1) & 1, kPolls);
+                if (!ok) fail();
+                float part[8];
 #pragma unroll
-            for (int m = 0; m < kC / 4; ++m) {
-                const int i = wq + 4 * m;
-                const float4 o = *reinterpret_cast<const float4*>(otile + i * kD + 4 * lane);
-                float4 res = o;
-                if (a.z) {
-                    float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
-                    ss = warp_sum(ss);
-                    const float rinv = rsqrtf(ss / kD + a.eps);
-                    const float4 z = zf[m];
-                    res.x = w4.x * o.x * rinv * z.x * fast_sigmoid(z.x);
-                    res.y = w4.y * o.y * rinv * z.y * fast_sigmoid(z.y);
-                    res.z = w4.z * o.z * rinv * z.z * fast_sigmoid(z.z);
-                    res.w = w4.w * o.w * rinv * z.w * fast_sigmoid(z.w);
-                }
-                const long off = (t0 + i) * tok_stride + (long)h * kD + 4 * lane;
-                if (i >= L) continue;
-                if (a.out_dtype == GDN_BF16) {
-                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + off) =
-                        make_uint2(pack_bf16x2(res.x, res.y), pack_bf16x2(res.z, res.w));
-                } else {
-                    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) = res;
+                for (int e = 0; e < 8; ++e) part[e] = 0.f;
+#pragma unroll
+                for (int j = 0; j < kD; ++j) part[j & 7] = fmaf(o[j], o[j], part[j & 7]);
+                const float ss = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                rinv = rsqrtf(ss / kD + a.eps);
+            }
+            if (ok && rowthr && i < L) {
+                const long off = (t0 + i) * tok_stride + (long)h * kD;
+#pragma unroll
+                for (int c8 = 0; c8 < 16; ++c8) {   // 8 columns = two 16-byte chunks of the z tile
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = o[8 * c8 + e];
+                    if (a.z) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int c4 = 2 * c8 + hh, cb = c4 >> 3, ch = c4 & 7;
+                            const float4 z = *reinterpret_cast<const float4*>(zt + cb * 8192 + i * 128 + ((ch ^ (i & 7)) << 4));
+                            float4 w = make_float4(rinv, rinv, rinv, rinv);
+                            if (a.w) {
+                                const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w) + c4);
+                                w = make_float4(wv.x * rinv, wv.y * rinv, wv.z * rinv, wv.w * rinv);
+                            }
+                            y[4 * hh] *= w.x * fast_silu(z.x);
+                            y[4 * hh + 1] *= w.y * fast_silu(z.y);
+                            y[4 * hh + 2] *= w.z * fast_silu(z.z);
+                            y[4 * hh + 3] *= w.w * fast_silu(z.w);
+                        }
+                    }
+                    if (a.out_dtype == GDN_BF16) {
+                        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off)[c8] =
+                            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                       pack_bf16x2(y[6], y[7]));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) + 2 * c8;
+                        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+                        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+                    }
                 }
             }
-            bar_sync(4, 128);                  // otile and qs_s are reused by the next chunk
+            if (a.z) {
+                // every row has read its z: the buffer may be refilled
+                if (bar_sync_or(4, 128, *abort_flag != 0)) break;
+                if (leader && c + 2 < nck) issue_z(c + 2);
+            }
+        }
+        // a z tile still in flight (only after a timeout) must land before the CTA exits; its
+        // completion is the one phase nobody waited for, so any completion state will do
+        if (a.z && leader && *abort_flag) {
+            for (int zb = 0; zb < 2; ++zb)
+                for (int ph = 0; ph < 2; ++ph) mbar_wait(&bars[ZFULL0 + zb], ph, 1000000u);
         }
     }
     }  // epilogue warpgroups
@@ -899,6 +943,17 @@ bool map_tokens(CUtensorMap* m, const void* base, int total_T, int H) {
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return get_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_z(CUtensorMap* m, const float* base, int total_T, int H) {
+    // gate input z [total_T, H, 128] fp32 -> dims (128, H, total_T), box (32, 1, 64), 128-byte swizzle
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)H * kD * 4};
+    cuuint32_t box[3] = {32, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    return get_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -936,14 +991,22 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.Ut = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Ut);
     a.Aqk = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Aqk);
     a.scal = reinterpret_cast<float*>(ws + L.off_scal);
+    a.Qt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Qt);
+    a.Kt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Kt);
     a.initial_state = p.initial_state; a.final_state = p.final_state;
     a.z = p.z; a.w = p.w; a.eps = p.eps; a.out = p.out; a.out_dtype = p.out_dtype; a.err = p.err;
 
-    CUtensorMap mQ, mK, mV, mW, mAqk;
+    CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ;
     if (!map_tokens(&mQ, p.q, p.total_T, p.H) || !map_tokens(&mK, p.k, p.total_T, p.H) ||
         !map_tokens(&mV, p.v, p.total_T, p.H) || !map_rows(&mW, a.W, L.nch * kC, kD, 64) ||
-        !map_rows(&mAqk, a.Aqk, L.nch * kC, kC, 64))
+        !map_rows(&mAqk, a.Aqk, L.nch * kC, kC, 64) || !map_rows(&mQt, a.Qt, L.nch * kC, kD, 64) ||
+        !map_rows(&mKt, a.Kt, L.nch * kC, kD, 64))
         return cudaErrorInvalidValue;
+    if (p.z) {
+        if (!map_z(&mZ, p.z, p.total_T, p.H)) return cudaErrorInvalidValue;
+    } else {
+        mZ = mQ;  // never dereferenced without a gate
+    }
 
     chunk_map_kernel<<<1, 1024, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
@@ -955,7 +1018,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmem);
     if (e != cudaSuccess) return e;
-    chunk_state_kernel<<<(unsigned)((long)p.num_seqs * p.H), st::kThreads, st::kSmem, s>>>(mQ, mK, mW, mAqk, a);
+    chunk_state_kernel<<<(unsigned)((long)p.num_seqs * p.H), st::kThreads, st::kSmem, s>>>(mQt, mKt, mW, mAqk, mZ, a);
     return cudaGetLastError();
 }
 
