@@ -32,6 +32,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_fp16.h>
+
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -156,6 +158,17 @@ __device__ __forceinline__ float fast_silu(float x) {
     float t;
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hx));
     return fmaf(hx, t, hx);
+}
+
+// SiLU of two values at once with the packed half-precision tanh (inputs are the gate's z, of order
+// one; the result is rounded to the output type right after): x sigma(x) = h + h tanh(h), h = x / 2.
+__device__ __forceinline__ float2 fast_silu2(float x0, float x1) {
+    const float h0 = 0.5f * x0, h1 = 0.5f * x1;
+    __half2 hh = __floats2half2_rn(h0, h1);
+    uint32_t t;
+    asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<uint32_t*>(&hh)));
+    const float2 tf = __half22float2(*reinterpret_cast<__half2*>(&t));
+    return make_float2(fmaf(h0, tf.x, h0), fmaf(h1, tf.y, h1));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -750,26 +763,29 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             bool ok = mbar_wait(&bars[DA1], c & 1, kPolls);
             if (!ok) fail();
             tc_fence_after();
-            // ---- V_new^T row r = U^T row r - (S W^T) row r, 32 tokens at a time ----
-#pragma unroll
-            for (int hf = 0; hf < 2 && ok; ++hf) {
-                uint32_t v[32];
-                tmem_ld32(tDA0 + b * 64 + lrow + 32 * hf, v);
+            // ---- V_new^T row r = U^T row r - (S W^T) row r ----
+            if (ok) {
+                uint32_t v[2][32];
+                tmem_ld32(tDA0 + b * 64 + lrow, v[0]);
+                tmem_ld32(tDA0 + b * 64 + lrow + 32, v[1]);
                 tmem_wait_ld();
-                float u[32];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    const uint4 q = up[4 * hf + c8];
-                    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                for (int hf = 0; hf < 2; ++hf) {
+                    float u[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-                        u[8 * c8 + 2 * e] = f.x - __uint_as_float(v[8 * c8 + 2 * e]);
-                        u[8 * c8 + 2 * e + 1] = f.y - __uint_as_float(v[8 * c8 + 2 * e + 1]);
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const uint4 q = up[4 * hf + c8];
+                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+                            u[8 * c8 + 2 * e] = f.x - __uint_as_float(v[hf][8 * c8 + 2 * e]);
+                            u[8 * c8 + 2 * e + 1] = f.y - __uint_as_float(v[hf][8 * c8 + 2 * e + 1]);
+                        }
                     }
-                }
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(sm + oA1, r, 4 * hf + c8, u + 8 * c8);
+                    for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(sm + oA1, r, 4 * hf + c8, u + 8 * c8);
+                }
             }
             fence_async_smem();
             tc_fence_before();
@@ -779,28 +795,29 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             if (!ok) fail();
             tc_fence_after();
             // ---- S: mirror as bf16 operand, pre-decay by the next chunk's gamma ----
+            if (ok) {
+                uint32_t v[4][32];
 #pragma unroll
-            for (int blk = 0; blk < 4 && ok; ++blk) {
-                uint32_t v[32];
-                tmem_ld32(tS + lrow + blk * 32, v);
+                for (int blk = 0; blk < 4; ++blk) tmem_ld32(tS + lrow + blk * 32, v[blk]);
                 tmem_wait_ld();
-                float f[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-                if (last) {
-                    if (a.final_state) {
-                        float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
+                for (int blk = 0; blk < 4; ++blk) {
+                    float* f = reinterpret_cast<float*>(v[blk]);
+                    if (last) {
+                        if (a.final_state) {
+                            float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            st_sw128_chunk(Sb + (blk >> 1) * 16384, r, (blk & 1) * 4 + c8, f + 8 * c8);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) f[j] *= gnext;
+                        tmem_st32(tS + lrow + blk * 32, v[blk]);
                     }
-                } else {
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        st_sw128_chunk(Sb + (blk >> 1) * 16384, r, (blk & 1) * 4 + c8, f + 8 * c8);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(gnext * f[j]);
-                    tmem_st32(tS + lrow + blk * 32, v);
                 }
             }
             if (!last) {
@@ -813,15 +830,19 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
         }
     } else {
         // ================= output epilogue (O and the gate) =================
-        // O has tokens as rows (M = 64): token i lives in TMEM lane 32 (i / 16) + i % 16, so each of
-        // lanes 0-15 of the four warps owns one whole output row: the RMS over d_v is a private sum,
-        // z comes from a TMA-filled shared tile and the row is stored contiguously.
+        // O has tokens as rows (M = 64): token i lives in TMEM lane 32 (i / 16) + i % 16 of its
+        // warp's quarter.  Lane l < 16 reads its row and hands the upper 64 columns to lane l + 16,
+        // so all 32 lanes gate 64 columns each; the RMS over d_v is a private sum; z comes from a
+        // TMA-filled shared tile; finished rows are staged in that tile and written back with one
+        // coalesced 256-byte store per row.
         const int q4 = warp & 3;
-        const int i = q4 * 16 + lane;          // token row of this thread (valid for lane < 16)
-        const bool rowthr = lane < 16;
+        const int i = q4 * 16 + (lane & 15);   // token row of this lane
+        const int half = lane >> 4;            // columns 64 * half .. 64 * half + 63
         const uint32_t lrow = static_cast<uint32_t>(q4 * 32) << 16;
         const long tok_stride = (long)a.H * kD;
         const bool leader = (warp == 8 && lane == 0);
+        const bool bf16_out = a.out_dtype == GDN_BF16;
+        constexpr int kStageRow = 272;         // staged bf16 row stride in bytes (256 + 16 padding)
         // z of chunk c goes to buffer c & 1; it is requested two chunks ahead
         auto issue_z = [&](int cz) {
             const int t0z = (int)(bos + (long)cz * kC);
@@ -838,72 +859,94 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             const int b = c & 1;
             const long t0 = bos + (long)c * kC;
             const int L = (eos - t0 < kC) ? (int)(eos - t0) : kC;
+            uint8_t* zt = sm + oZ + (c & 1) * 32768;
             bool ok = mbar_wait(&bars[DO_0 + b], (c >> 1) & 1, kPolls);
             if (!ok) fail();
             tc_fence_after();
-            float o[kD];
+            uint32_t v[4][32];
+            float ss = 0.f;
+            {
+                if (ok) {
 #pragma unroll
-            for (int blk = 0; blk < 4 && ok; ++blk) {
-                uint32_t v[32];
-                tmem_ld32(tDO0 + b * 128 + blk * 32 + lrow, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) o[blk * 32 + j] = __uint_as_float(v[j]);
-            }
-            tc_fence_before();
-            if (bar_sync_or(4, 128, *abort_flag != 0)) break;
-            if (leader) mbar_arrive(&bars[DOE_0 + b]);
-            float rinv = 1.0f;
-            const uint8_t* zt = sm + oZ + (c & 1) * 32768;
-            if (a.z) {
-                ok = mbar_wait(&bars[ZFULL0 + (c & 1)], (c >> 1) & 1, kPolls);
-                if (!ok) fail();
+                    for (int blk = 0; blk < 4; ++blk) tmem_ld32(tDO0 + b * 128 + blk * 32 + lrow, v[blk]);
+                    tmem_wait_ld();
+                }
                 float part[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part[e] = 0.f;
 #pragma unroll
-                for (int j = 0; j < kD; ++j) part[j & 7] = fmaf(o[j], o[j], part[j & 7]);
-                const float ss = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                rinv = rsqrtf(ss / kD + a.eps);
-            }
-            if (ok && rowthr && i < L) {
-                const long off = (t0 + i) * tok_stride + (long)h * kD;
+                for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
-                for (int c8 = 0; c8 < 16; ++c8) {   // 8 columns = two 16-byte chunks of the z tile
-                    float y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = o[8 * c8 + e];
-                    if (a.z) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int c4 = 2 * c8 + hh, cb = c4 >> 3, ch = c4 & 7;
-                            const float4 z = *reinterpret_cast<const float4*>(zt + cb * 8192 + i * 128 + ((ch ^ (i & 7)) << 4));
-                            float4 w = make_float4(rinv, rinv, rinv, rinv);
-                            if (a.w) {
-                                const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w) + c4);
-                                w = make_float4(wv.x * rinv, wv.y * rinv, wv.z * rinv, wv.w * rinv);
-                            }
-                            y[4 * hh] *= w.x * fast_silu(z.x);
-                            y[4 * hh + 1] *= w.y * fast_silu(z.y);
-                            y[4 * hh + 2] *= w.z * fast_silu(z.z);
-                            y[4 * hh + 3] *= w.w * fast_silu(z.w);
-                        }
+                    for (int j = 0; j < 32; ++j) {
+                        const float x = __uint_as_float(v[blk][j]);
+                        part[j & 7] = fmaf(x, x, part[j & 7]);
                     }
-                    if (a.out_dtype == GDN_BF16) {
-                        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + off)[c8] =
-                            make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                       pack_bf16x2(y[6], y[7]));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) + 2 * c8;
-                        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-                        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-                    }
+                ss = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+                ss = __shfl_sync(0xffffffffu, ss, lane & 15);   // lanes >= 16: their row's sum
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {   // lanes >= 16 take the upper 64 columns of lane - 16
+                    const uint32_t up_half = __shfl_up_sync(0xffffffffu, v[2 + (j >> 5)][j & 31], 16);
+                    if (half) v[j >> 5][j & 31] = up_half;
                 }
             }
+            float* o = reinterpret_cast<float*>(&v[0][0]);   // this lane's 64 columns (v[0], v[1])
+            tc_fence_before();
+            if (bar_sync_or(4, 128, *abort_flag != 0)) break;
+            if (leader) mbar_arrive(&bars[DOE_0 + b]);
             if (a.z) {
-                // every row has read its z: the buffer may be refilled
+                ok = mbar_wait(&bars[ZFULL0 + (c & 1)], (c >> 1) & 1, kPolls);
+                if (!ok) fail();
+                const float rinv = rsqrtf(ss / kD + a.eps);
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {        // columns 64 half + 4 c4 .. + 3
+                    const int col = 64 * half + 4 * c4, cb = col >> 5, ch = (col & 31) >> 2;
+                    const float4 z = *reinterpret_cast<const float4*>(zt + cb * 8192 + i * 128 + ((ch ^ (i & 7)) << 4));
+                    float4 w = make_float4(rinv, rinv, rinv, rinv);
+                    if (a.w) {
+                        const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w + col));
+                        w = make_float4(wv.x * rinv, wv.y * rinv, wv.z * rinv, wv.w * rinv);
+                    }
+                    const float2 s01 = fast_silu2(z.x, z.y), s23 = fast_silu2(z.z, z.w);
+                    o[4 * c4] *= w.x * s01.x;
+                    o[4 * c4 + 1] *= w.y * s01.y;
+                    o[4 * c4 + 2] *= w.z * s23.x;
+                    o[4 * c4 + 3] *= w.w * s23.y;
+                }
+            }
+            if (bf16_out) {
+                // stage this half row (128 B) in the chunk's own z buffer, then one warp store per row.
+                // The staged rows overlap z rows of other warps: with a gate, the whole group must
+                // have read its z first; without one the buffer holds no z and each warp only
+                // touches its own staged rows.
+                if (a.z) bar_sync(4, 128);
+                else __syncwarp();
+                uint4* dst = reinterpret_cast<uint4*>(zt + i * kStageRow + half * 128);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    dst[c8] = make_uint4(pack_bf16x2(o[8 * c8], o[8 * c8 + 1]), pack_bf16x2(o[8 * c8 + 2], o[8 * c8 + 3]),
+                                         pack_bf16x2(o[8 * c8 + 4], o[8 * c8 + 5]), pack_bf16x2(o[8 * c8 + 6], o[8 * c8 + 7]));
+                __syncwarp();
+#pragma unroll 4
+                for (int rr = 0; rr < 16; ++rr) {
+                    const int row = q4 * 16 + rr;
+                    if (ok && row < L) {
+                        const uint2 val = *reinterpret_cast<const uint2*>(zt + row * kStageRow + 8 * lane);
+                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (t0 + row) * tok_stride +
+                                                  (long)h * kD + 4 * lane) = val;
+                    }
+                }
+            } else if (ok && i < L) {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + (t0 + i) * tok_stride +
+                                                        (long)h * kD + 64 * half);
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) dst[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
+            }
+            if (a.z) {
+                // every row has read its z and written its output: the buffer may be refilled
                 if (bar_sync_or(4, 128, *abort_flag != 0)) break;
                 if (leader && c + 2 < nck) issue_z(c + 2);
+            } else {
+                __syncwarp();                       // the staged rows are reused two chunks later
             }
         }
         // a z tile still in flight (only after a timeout) must land before the CTA exits; its

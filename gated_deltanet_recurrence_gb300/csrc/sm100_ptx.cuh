@@ -56,18 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, ui
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-// Wait for the phase with the given parity to complete; false once `limit_ns` of wall time has
-// passed without completion.
+// Wait for the phase with the given parity to complete; false once `limit_ns` has passed without
+// completion.  The bound is kept with the SM cycle counter (read cheaply on every poll) converted
+// at the highest SM clock of the part, 2.1 GHz, so it never expires early; at lower clocks it only
+// lasts longer.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity, 100000u)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long limit = static_cast<long long>(limit_ns) * 21 / 10;
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity, 100000u))
-        if (globaltimer_ns() - t0 > limit_ns) return false;
+        if (clock64() - t0 > limit) return false;
     return true;
 }
 

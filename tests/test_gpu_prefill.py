@@ -169,13 +169,15 @@ def test_malformed_cu_seqlens_reported_on_device():
 
 
 def test_gated_output_matches_standalone_gate():
-    """The fused gate epilogue equals the raw output passed through gdn_gate_rmsnorm_silu."""
+    """The fused gate epilogue equals the raw output passed through gdn_gate_rmsnorm_silu.  The
+    fused epilogue of the bf16 path evaluates SiLU with the packed half-precision tanh (relative
+    error near 1e-3), so the two agree to the bf16 output precision (2^-9), not to fp32."""
     inp = synthetic.prefill_inputs(synthetic.workload("prefill", T=200, H=4, seed=35))
     g32, b32 = oracle_gates(inp)
     o_fused, _ = run_gpu(inp, g32, b32, out_dtype=torch.float32)
     y_raw, _ = run_gpu(inp, g32, b32, out_dtype=torch.float32, gate=False)
     o_sep = gdn.gdn_gate_rmsnorm_silu(y_raw.cuda(), inp["z"].cuda(), out_dtype=torch.float32).cpu()
-    assert torch.allclose(o_fused, o_sep, rtol=1e-4, atol=1e-5)
+    assert rel_l2_tokens(o_fused, o_sep, cu_list(inp)) <= 2e-3
 
 
 def test_gate_prep_then_prefill_end_to_end():
