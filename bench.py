@@ -329,7 +329,34 @@ def bench_decode(args, dev):
     assert gdn.gdn_get_device_error() == 0
     step_ms = statistics.mean(x.elapsed_time(z) for x, _, z in times)
     kern_ms = statistics.mean(y.elapsed_time(z) for _, y, z in times)
-    return dict(ms=step_ms, kernel_ms=kern_ms, N=N, H=H, d=d)
+
+    # pooled multi-token decode: the same 256 sequences pick their states from a 512-slot pool
+    # through an index array and run T = 4 tokens each (state read and written once)
+    Tm, slots = 4, 2 * N
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    qm, km, vm = (torch.randn(N, Tm, H, d, generator=gen, device=dev).to(torch.bfloat16) for _ in range(3))
+    gm = -torch.rand(N, Tm, H, generator=gen, device=dev)
+    bm = torch.rand(N, Tm, H, generator=gen, device=dev)
+    pool = torch.randn(slots, H, d, d, generator=gen, device=dev) * 0.02
+    idx = torch.randperm(slots, generator=gen, device=dev)[:N].to(torch.int32)
+    outm = torch.empty(N, Tm, H, d, dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup):
+        gdn.gdn_recurrent_multi_step(qm, km, vm, gm, bm, pool, state_indices=idx, out=outm)
+    torch.cuda.synchronize()
+    mt = []
+    for _ in range(max(args.steps, 20)):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        gdn.gdn_recurrent_multi_step(qm, km, vm, gm, bm, pool, state_indices=idx, out=outm)
+        e1.record(stream)
+        mt.append((e0, e1))
+    torch.cuda.synchronize()
+    assert gdn.gdn_get_device_error() == 0
+    multi_ms = statistics.mean(x.elapsed_time(y) for x, y in mt)
+    multi_bytes = N * H * (2 * d * d * 4 + Tm * (3 * d * 2 + 8 + d * 2)) + N * 4
+    return dict(ms=step_ms, kernel_ms=kern_ms, N=N, H=H, d=d, multi_ms=multi_ms, multi_T=Tm,
+                multi_bytes=multi_bytes, multi_slots=slots)
 
 
 def run_gdn(args):
@@ -380,7 +407,12 @@ def run_gdn(args):
               "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": d_gbs / peaks["hbm_gbs"], "traffic": traffic_record("decode_kernel[decode]"),
                            "kernel": "decode_kernel", "algorithmic_bytes": dbytes,
-                           "peak_source": f"{peak_src} hbm_gbs"}}
+                           "peak_source": f"{peak_src} hbm_gbs"},
+              "multi_token": {"tokens_per_s": dc["N"] * dc["multi_T"] * world / (dc["multi_ms"] / 1e3),
+                              "ms": dc["multi_ms"], "T": dc["multi_T"], "pool_slots": dc["multi_slots"],
+                              "entry_point": "gdn_recurrent_multi_step",
+                              "hbm_gbs": dc["multi_bytes"] / (dc["multi_ms"] / 1e3) / 1e9,
+                              "frac": dc["multi_bytes"] / (dc["multi_ms"] / 1e3) / 1e9 / peaks["hbm_gbs"]}}
     line = {
         "metric": "prefill tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

@@ -33,6 +33,8 @@ SIGNATURES = {
     "gdn_chunk_fwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "gdn_recurrent_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
                                 _f, _vp, _i, _vp]),
+    "gdn_recurrent_multi_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _ip, _i, _i, _i, _i, _i, _i, _f,
+                                      _i, _fp, _fp, _f, _vp, _i, _vp]),
     "gdn_gate_rmsnorm_silu": (_i, [_vp, _i, _fp, _fp, _f, _vp, _i, _l, _i, _vp]),
     "gdn_decay_from_logits": (_i, [_fp, _fp, _fp, _fp, _fp, _fp, _l, _i, _vp]),
     "gdn_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
@@ -195,6 +197,34 @@ def gdn_recurrent_step(q, k, v, g, beta, state, scale=0.0, use_qk_l2norm=True, g
                                   dt, float(scale), int(bool(use_qk_l2norm)), _p(gate_z),
                                   _p(norm_weight), float(norm_eps), _p(out), odt, _stream(stream))
     _check("gdn_recurrent_step", rc)
+    return out
+
+
+def gdn_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices=None, scale=0.0,
+                             use_qk_l2norm=True, gate_z=None, norm_weight=None, norm_eps=1e-6,
+                             out=None, out_dtype=None, stream=None):
+    """T decode tokens per sequence on pooled states: q, k [N, T, H, d_k]; v [N, T, H, d_v];
+    g, beta [N, T, H]; state_pool [slots, H, d_v, d_k] fp32 updated in place; state_indices int32
+    [N] (negative = skip) or None.  Returns out [N, T, H, d_v]."""
+    N, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = _dt(q)
+    odt = dt if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
+    if out is None:
+        out = torch.empty((N, T, H, d_v), dtype=_torch_dt(odt), device=q.device)
+    else:
+        odt = _dt(out)
+    if state_indices is not None and state_indices.dtype != torch.int32:
+        raise TypeError("state_indices must be int32")
+    for name, t in (("g", g), ("beta", beta), ("state_pool", state_pool), ("gate_z", gate_z),
+                    ("norm_weight", norm_weight)):
+        _f32(t, name)
+    rc = lib().gdn_recurrent_multi_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool),
+                                        state_pool.shape[0], _p(state_indices), N, T, H, d_k, d_v,
+                                        dt, float(scale), int(bool(use_qk_l2norm)), _p(gate_z),
+                                        _p(norm_weight), float(norm_eps), _p(out), odt,
+                                        _stream(stream))
+    _check("gdn_recurrent_multi_step", rc)
     return out
 
 

@@ -142,6 +142,34 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v, const float*
     return launch_status(gdn::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+int gdn_recurrent_multi_step(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float* state_pool, int num_slots,
+                             const int32_t* state_indices, int N, int T, int H, int d_k, int d_v,
+                             gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
+                             const float* gate_z, const float* norm_weight, float norm_eps,
+                             void* out, gdn_dtype out_dtype, void* stream) {
+    if (!valid_dtype(qkv_dtype) || !valid_dtype(out_dtype)) return GDN_ERR_DTYPE;
+    if (N < 0 || T <= 0 || H <= 0 || num_slots <= 0) return GDN_ERR_ARG;
+    if (!head_size_ok(d_k, d_v)) return GDN_ERR_UNSUPPORTED;
+    if ((long long)N * H > 0x7fffffffLL || (long long)N * T * H * d_k > (1LL << 40)) return GDN_ERR_ARG;
+    if (!state_indices && num_slots < N) return GDN_ERR_ARG;
+    if (N == 0) return GDN_OK;
+    if (!q || !k || !v || !g || !beta || !state_pool || !out) return GDN_ERR_ARG;
+    if (!(norm_eps >= 0.0f) || (gate_z == nullptr && norm_weight != nullptr)) return GDN_ERR_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, state_pool, gate_z, norm_weight, out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return GDN_ERR_ARG;
+    gdn::DecodeMultiArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state_pool; a.num_slots = num_slots;
+    a.idx = state_indices; a.N = N; a.T = T; a.H = H; a.d = d_k; a.qkv_dtype = qkv_dtype;
+    a.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)d_k);
+    a.use_l2 = use_qk_l2norm ? 1 : 0;
+    a.z = gate_z; a.w = norm_weight; a.eps = norm_eps; a.out = out; a.out_dtype = out_dtype;
+    a.err = device_error_ptr();
+    if (!a.err) return GDN_ERR_CUDA;
+    return launch_status(gdn::launch_decode_multi(a, static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_gate_rmsnorm_silu(const void* y, gdn_dtype y_dtype, const float* z,
                           const float* norm_weight, float eps, void* out, gdn_dtype out_dtype,
                           long rows, int d_v, void* stream) {

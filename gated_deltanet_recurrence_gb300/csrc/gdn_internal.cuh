@@ -77,6 +77,14 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+struct DecodeMultiArgs {
+    const void* q; const void* k; const void* v; const float* g; const float* beta;
+    float* state; int num_slots; const int32_t* idx; int N, T, H, d; gdn_dtype qkv_dtype;
+    float scale; int use_l2; const float* z; const float* w; float eps; void* out; gdn_dtype out_dtype;
+    int* err;
+};
+cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t s);
+
 struct GateArgs {
     const void* y; gdn_dtype y_dtype; const float* z; const float* w; float eps;
     void* out; gdn_dtype out_dtype; long rows; int d_v;

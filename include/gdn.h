@@ -103,6 +103,28 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v, const float*
                        void* out, gdn_dtype out_dtype, void* stream);
 
 /*
+ * gdn_recurrent_multi_step -- T decode tokens for each of N sequences whose states live in a pool.
+ * Source: "6.6 Gated DeltaNet" 6.6.8 (decode keeps only the fixed-size state, so a serving batch
+ * indexes into a pool of states) and the update of "[LLM Algorithms-2] Gated DeltaNet" section 4
+ * applied T times in order (speculative / multi-token decode).  Each state is read once, kept on
+ * chip for the T tokens, and written once.
+ *
+ *   q, k   [N, T, H, d_k] qkv_dtype;  v [N, T, H, d_v];  g, beta [N, T, H] fp32.
+ *   state_pool     [num_slots, H, d_v, d_k] fp32, updated in place.
+ *   state_indices  device int32 [N] or NULL (then sequence n uses slot n; num_slots >= N).  A
+ *                  negative index skips the sequence (nothing read or written).  An index
+ *                  >= num_slots is caught on the device: the sequence is skipped and GDN_ERR_ARG is
+ *                  latched in the device error word.  Two sequences must not share a slot.
+ *   gate_z [N, T, H, d_v] fp32 or NULL; norm_weight [d_v] or NULL; out [N, T, H, d_v] of out_dtype.
+ */
+int gdn_recurrent_multi_step(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float* state_pool, int num_slots,
+                             const int32_t* state_indices, int N, int T, int H, int d_k, int d_v,
+                             gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
+                             const float* gate_z, const float* norm_weight, float norm_eps,
+                             void* out, gdn_dtype out_dtype, void* stream);
+
+/*
  * gdn_gate_rmsnorm_silu -- the gated output norm on its own.
  * Source: "5. 线性注意力", "门控 RMSNorm" (RMSNormGated: weight * norm(x) * silu(z)) and
  * "6.6 Gated DeltaNet" 6.6.2 (o_t = RMSNorm(y_t) * SiLU(g_t)).  The norm is taken in fp32 over

@@ -122,3 +122,22 @@ def test_binding_refuses_cpu_tensors():
     g = torch.zeros(4, 2)
     with pytest.raises(ValueError):
         gdn.gdn_chunk_fwd(x, x, x, g, g)
+
+
+def test_recurrent_multi_step_rejects_bad_arguments():
+    L = gdn.lib()
+
+    def ms(**kw):
+        a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, slots=8, idx=NUL, N=4, T=2, H=2, dk=128, dv=128, dt=1,
+                 scale=0.0, l2=1, z=NUL, w=NUL, eps=1e-6, out=P, odt=1, stream=NUL)
+        a.update(kw)
+        return L.gdn_recurrent_multi_step(*a.values())
+
+    assert ms(dt=9) == -2
+    assert ms(T=0) == -1
+    assert ms(slots=0) == -1
+    assert ms(slots=3) == -1          # identity mapping needs a slot per sequence
+    assert ms(N=0) == 0
+    assert ms(dk=64, dv=128) == -7
+    assert ms(S=NUL) == -1
+    assert ms(w=P) == -1
