@@ -15,6 +15,12 @@ Functions and the passages they follow (page titles):
   gate_rmsnorm_silu     "5. 线性注意力", "门控 RMSNorm"; "6.6 Gated DeltaNet" 6.6.2
   gates_from_logits     "6.6 Gated DeltaNet" 6.6.3
   recurrent_step        "6.6 Gated DeltaNet" 6.6.8 (one token on a kept state)
+  short_conv            "5. 线性注意力", "因果卷积(Causal Conv1d)" (depthwise, causal, SiLU)
+
+The forms take q, k with Hk heads and v with H = r * Hk heads (value head h reads
+query/key head h // r, the page's repeat_interleave), and g either [total_T, H]
+(one decay per head) or [total_T, H, dk] (one per key channel, "6.6 Gated
+DeltaNet" 6.6.7; S <- S diag(alpha_t)); the chunked form is scalar only.
 
 Every function has at least one independent pin in tests/test_oracle_pins.py.
 """
@@ -60,7 +66,11 @@ def _load():
             lib.gdn_oracle_forward.restype = ctypes.c_int
             lib.gdn_oracle_forward.argtypes = [
                 ctypes.c_int, dp, dp, dp, dp, dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, ctypes.c_double, ctypes.c_int, dp, dp, dp, ctypes.c_int, ctypes.c_int]
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, dp, dp, dp,
+                ctypes.c_int, ctypes.c_int]
+            lib.gdn_oracle_short_conv.restype = ctypes.c_int
+            lib.gdn_oracle_short_conv.argtypes = [dp, dp, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  dp, dp, dp, ctypes.c_int]
             lib.gdn_oracle_chunk_decay.restype = None
             lib.gdn_oracle_chunk_decay.argtypes = [dp, ctypes.c_int, dp, dp]
             lib.gdn_oracle_gate_rmsnorm_silu.restype = None
@@ -105,9 +115,11 @@ def _cu(cu_seqlens, total_T, batch):
 def _forward(form, q, k, v, g, beta, cu_seqlens=None, batch=None, scale=None, use_qk_l2norm=True,
              initial_state=None, C=64, threads=1):
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
-    total_T, H, dk = q.shape
-    dv = v.shape[2]
-    if k.shape != q.shape or v.shape[:2] != (total_T, H) or g.shape != (total_T, H) \
+    total_T, Hk, dk = q.shape
+    H, dv = v.shape[1], v.shape[2]
+    per_channel = g.ndim == 3
+    if k.shape != q.shape or v.shape[0] != total_T or H % Hk \
+            or g.shape != ((total_T, H, dk) if per_channel else (total_T, H)) \
             or beta.shape != (total_T, H):
         raise ValueError("shape mismatch")
     cu = _cu(cu_seqlens, total_T, batch)
@@ -123,10 +135,11 @@ def _forward(form, q, k, v, g, beta, cu_seqlens=None, batch=None, scale=None, us
     S_final = np.zeros((num_seqs, H, dv, dk), dtype=np.float64)
     rc = _load().gdn_oracle_forward(
         form, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), num_seqs, H, dk, dv, float(scale),
-        int(bool(use_qk_l2norm)), _ptr(S0), _ptr(y), _ptr(S_final), int(C), int(threads))
+        cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), num_seqs, H, Hk, dk, dv, int(per_channel),
+        float(scale), int(bool(use_qk_l2norm)), _ptr(S0), _ptr(y), _ptr(S_final), int(C), int(threads))
     if rc != 0:
-        raise ValueError("oracle rejected its arguments (cu_seqlens not monotone or C <= 0)")
+        raise ValueError("oracle rejected its arguments (cu_seqlens not monotone, C <= 0, or a "
+                         "per-channel decay given to the chunked form)")
     return y, S_final
 
 
@@ -134,7 +147,8 @@ def recurrence(q, k, v, g, beta, cu_seqlens=None, batch=None, scale=None, use_qk
                initial_state=None, threads=1):
     """Token-by-token gated delta rule.
 
-    q, k: [total_T, H, dk]; v: [total_T, H, dv]; g (log-decay), beta: [total_T, H];
+    q, k: [total_T, Hk, dk]; v: [total_T, H, dv] with H a multiple of Hk; beta: [total_T, H];
+    g (log-decay): [total_T, H], or [total_T, H, dk] for a decay per key channel;
     cu_seqlens: [num_seqs+1] or None (then ``batch`` equal sequences);
     initial_state: [num_seqs, H, dv, dk] or None (zeros).
     Returns (y [total_T, H, dv], final_state [num_seqs, H, dv, dk]) in float64.
@@ -204,3 +218,30 @@ def recurrent_step(q, k, v, g, beta, state, scale=None, use_qk_l2norm=True):
     cu = np.arange(N + 1, dtype=np.int32)
     return recurrence(q, k, v, g, beta, cu_seqlens=cu, scale=scale, use_qk_l2norm=use_qk_l2norm,
                       initial_state=state)
+
+
+def short_conv(x, weight, cu_seqlens=None, batch=None, state=None, activation=True):
+    """Causal depthwise convolution (+ SiLU) over the token axis.
+
+    x: [total_T, channels]; weight: [channels, K]; state: [num_seqs, channels, K-1] carried
+    history (oldest first) or None (zeros).  Returns (out [total_T, channels], final state
+    [num_seqs, channels, K-1]) in float64."""
+    x = _f64(x)
+    w = _f64(weight)
+    total_T, channels = x.shape
+    K = w.shape[1]
+    if w.shape[0] != channels or K < 1:
+        raise ValueError("weight must be [channels, K]")
+    cu = _cu(cu_seqlens, total_T, batch)
+    num_seqs = cu.shape[0] - 1
+    st = _f64(state)
+    if st is not None and st.shape != (num_seqs, channels, K - 1):
+        raise ValueError("state shape")
+    out = np.zeros_like(x)
+    st_out = np.zeros((num_seqs, channels, K - 1))
+    rc = _load().gdn_oracle_short_conv(_ptr(x), _ptr(w), cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       num_seqs, channels, K, _ptr(st), _ptr(out), _ptr(st_out),
+                                       int(bool(activation)))
+    if rc != 0:
+        raise ValueError("cu_seqlens not monotone")
+    return out, st_out

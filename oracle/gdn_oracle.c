@@ -16,10 +16,20 @@
  *               "Delta Rule 的 Chunk 实现" (the chunked algorithm)
  *   [LLM-Alg-2] "[LLM Algorithms-2] Gated DeltaNet", sections 2.1, 2.2, 4, 4.3, 5, 7
  *   [GDN-detail]"Gated DeltaNet详解" (recurrent forward with state d_v x d_k)
+ *   [LinAttn-conv] "5. 线性注意力", sub-section "因果卷积(Causal Conv1d)" and the
+ *               forward code after it (depthwise conv, kernel 4, then SiLU; the
+ *               repeat_interleave of the q/k heads when num_v_heads > num_k_heads)
+ *   [GDN-book-mix] "6.6 Gated DeltaNet", 6.6.7 (Kimi Linear: alpha_t a vector
+ *               over the feature channels instead of one scalar per head)
  *
  * Conventions shared by every entry point (all arrays row-major, contiguous):
- *   q, k      [total_T][H][dk]      v, y      [total_T][H][dv]
+ *   q, k      [total_T][Hk][dk]     v, y      [total_T][H][dv]
+ *             value head h reads query/key head h / (H / Hk)   ([LinAttn-conv]
+ *             repeat_interleave; Hk == H is the plain case)
  *   g, beta   [total_T][H]          g is the log-decay, alpha_t = exp(g_t)
+ *   g         [total_T][H][dk]      instead, when the decay is per key channel
+ *             ([GDN-book-mix]; the reading taken: alpha scales the key columns
+ *             of S, S <- S diag(alpha_t), the vector form of alpha_t S)
  *   state     [num_seqs][H][dv][dk] (the [LLM-Alg-2] section 1 orientation:
  *                                    S maps a key to a value, y = S q)
  *   cu_seqlens[num_seqs + 1]        prefix sums of the sequence lengths
@@ -63,6 +73,8 @@ typedef struct {
     int T, dk, dv;
     const double *q, *k, *v, *g, *beta; /* pointers at the slab's first token */
     long qk_stride, v_stride, gate_stride; /* elements between consecutive tokens */
+    long g_stride;                      /* elements between consecutive tokens of g */
+    int g_per_channel;                  /* g holds dk log-decays per token */
     double scale;
     int use_l2;
     const double* S0; /* dv*dk or NULL */
@@ -89,19 +101,24 @@ static void recurrence_slab(const slab_t* s)
     double* qn = (double*)malloc(sizeof(double) * dk);
     double* kn = (double*)malloc(sizeof(double) * dk);
     double* e = (double*)malloc(sizeof(double) * dv);
+    double* al = (double*)malloc(sizeof(double) * dk);
     if (s->S0) memcpy(S, s->S0, sizeof(double) * dv * dk);
 
     for (int t = 0; t < s->T; ++t) {
         const double* qt = s->q + (long)t * s->qk_stride;
         const double* kt = s->k + (long)t * s->qk_stride;
         const double* vt = s->v + (long)t * s->v_stride;
-        double alpha = exp(s->g[(long)t * s->gate_stride]);
+        const double* gt = s->g + (long)t * s->g_stride;
         double beta = s->beta[(long)t * s->gate_stride];
         l2_normalise(qt, qn, dk, s->use_l2);
         l2_normalise(kt, kn, dk, s->use_l2);
         for (int j = 0; j < dk; ++j) qn[j] *= s->scale;
 
-        for (int i = 0; i < dv * dk; ++i) S[i] *= alpha;
+        /* alpha_t S, or S diag(alpha_t) when the decay is per key channel */
+        const double a0 = exp(gt[0]);
+        for (int j = 0; j < dk; ++j) al[j] = s->g_per_channel ? exp(gt[j]) : a0;
+        for (int r = 0; r < dv; ++r)
+            for (int j = 0; j < dk; ++j) S[(long)r * dk + j] *= al[j];
         for (int r = 0; r < dv; ++r) {
             double pred = 0.0;
             for (int j = 0; j < dk; ++j) pred += S[(long)r * dk + j] * kn[j];
@@ -117,7 +134,7 @@ static void recurrence_slab(const slab_t* s)
         }
     }
     if (s->S_out) memcpy(s->S_out, S, sizeof(double) * dv * dk);
-    free(S); free(qn); free(kn); free(e);
+    free(S); free(qn); free(kn); free(e); free(al);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -186,7 +203,7 @@ static void chunked_slab(const slab_t* s, int C)
             for (int j = 0; j < dk; ++j) Q[(long)i * dk + j] *= s->scale;
             for (int r = 0; r < dv; ++r) V[(long)i * dv + r] = s->v[t * s->v_stride + r];
             bt[i] = s->beta[t * s->gate_stride];
-            gg[i] = s->g[t * s->gate_stride];
+            gg[i] = s->g[t * s->g_stride];
         }
         /* stage 1 */
         gdn_oracle_chunk_decay(gg, L, gcum, decay);
@@ -270,6 +287,7 @@ static void chunked_slab(const slab_t* s, int C)
 /*
  * [LLM-Alg-2] section 7: S_t = S_{t-1} A_t + B_t with
  *     A_t = alpha_t (I - beta_t k_t k_t^T)   (dk x dk)
+ *         = diag(alpha_t) (I - beta_t k_t k_t^T) when alpha_t is per key channel
  *     B_t = beta_t v_t k_t^T                 (dv x dk)
  * unrolled to S_t = S_0 A_1...A_t + sum_{i<=t} B_i A_{i+1}...A_t, y_t = S_t q_t.
  * Every product is formed explicitly with dense matrices, for every t; this is
@@ -299,12 +317,14 @@ static void transition_product_slab(const slab_t* s)
 
     for (int t = 0; t < T; ++t) {
         l2_normalise(s->k + (long)t * s->qk_stride, kn, dk, s->use_l2);
-        double alpha = exp(s->g[(long)t * s->gate_stride]);
+        const double* gt = s->g + (long)t * s->g_stride;
         double beta = s->beta[(long)t * s->gate_stride];
         const double* vt = s->v + (long)t * s->v_stride;
-        for (int i = 0; i < dk; ++i)
+        for (int i = 0; i < dk; ++i) {
+            double alpha = exp(s->g_per_channel ? gt[i] : gt[0]);
             for (int j = 0; j < dk; ++j)
                 A[(long)t * dk * dk + (long)i * dk + j] = alpha * ((i == j ? 1.0 : 0.0) - beta * kn[i] * kn[j]);
+        }
         for (int r = 0; r < dv; ++r)
             for (int j = 0; j < dk; ++j) B[(long)t * dv * dk + (long)r * dk + j] = beta * vt[r] * kn[j];
     }
@@ -350,7 +370,7 @@ static void transition_product_slab(const slab_t* s)
 typedef struct {
     const double *q, *k, *v, *g, *beta;
     const int32_t* cu;
-    int num_seqs, H, dk, dv, use_l2, form, C;
+    int num_seqs, H, Hk, dk, dv, g_per_channel, use_l2, form, C;
     double scale;
     const double* S0;
     double* y;
@@ -367,13 +387,16 @@ static void run_unit(job_t* j, long unit)
     s.T = (int)(eos - bos);
     s.dk = j->dk;
     s.dv = j->dv;
-    s.qk_stride = (long)j->H * j->dk;
+    const int hk = h / (j->H / j->Hk); /* repeat_interleave of the query/key heads */
+    s.qk_stride = (long)j->Hk * j->dk;
     s.v_stride = (long)j->H * j->dv;
     s.gate_stride = j->H;
-    s.q = j->q + bos * s.qk_stride + (long)h * j->dk;
-    s.k = j->k + bos * s.qk_stride + (long)h * j->dk;
+    s.g_per_channel = j->g_per_channel;
+    s.g_stride = j->g_per_channel ? (long)j->H * j->dk : j->H;
+    s.q = j->q + bos * s.qk_stride + (long)hk * j->dk;
+    s.k = j->k + bos * s.qk_stride + (long)hk * j->dk;
     s.v = j->v + bos * s.v_stride + (long)h * j->dv;
-    s.g = j->g + bos * j->H + h;
+    s.g = j->g + bos * s.g_stride + (long)h * (j->g_per_channel ? j->dk : 1);
     s.beta = j->beta + bos * j->H + h;
     s.scale = j->scale;
     s.use_l2 = j->use_l2;
@@ -404,7 +427,8 @@ static int run_job(job_t* j, int n_threads)
 {
     for (int n = 0; n < j->num_seqs; ++n)
         if (j->cu[n + 1] < j->cu[n]) return -1;
-    if (j->form == 1 && j->C <= 0) return -1;
+    if (j->form == 1 && (j->C <= 0 || j->g_per_channel)) return -1; /* the page's chunk algorithm is scalar */
+    if (j->Hk <= 0 || j->H % j->Hk != 0) return -1;
     j->next_unit = 0;
     pthread_mutex_init(&j->mu, NULL);
     if (n_threads <= 1) {
@@ -421,16 +445,20 @@ static int run_job(job_t* j, int n_threads)
 
 /*
  * form: 0 = token-by-token recurrence, 1 = chunked form with chunk size C,
- *       2 = transition product.  Returns 0, or -1 on a malformed cu_seqlens.
+ *       2 = transition product.  Hk = number of query/key heads (H a multiple of
+ *       it); g_per_channel = 1 when g is [total_T][H][dk] (not for form 1).
+ *       Returns 0, or -1 on a malformed cu_seqlens or an unsupported request.
  */
 int gdn_oracle_forward(int form, const double* q, const double* k, const double* v,
                        const double* g, const double* beta, const int32_t* cu_seqlens,
-                       int num_seqs, int H, int dk, int dv, double scale, int use_qk_l2norm,
+                       int num_seqs, int H, int Hk, int dk, int dv, int g_per_channel,
+                       double scale, int use_qk_l2norm,
                        const double* S0, double* y, double* S_final, int C, int n_threads)
 {
     job_t j;
     j.q = q; j.k = k; j.v = v; j.g = g; j.beta = beta; j.cu = cu_seqlens;
-    j.num_seqs = num_seqs; j.H = H; j.dk = dk; j.dv = dv; j.use_l2 = use_qk_l2norm;
+    j.num_seqs = num_seqs; j.H = H; j.Hk = Hk; j.dk = dk; j.dv = dv; j.use_l2 = use_qk_l2norm;
+    j.g_per_channel = g_per_channel;
     j.form = form; j.C = C; j.scale = scale; j.S0 = S0; j.y = y; j.S_final = S_final;
     return run_job(&j, n_threads);
 }
@@ -479,4 +507,49 @@ void gdn_oracle_gates_from_logits(const double* a, const double* A_log, const do
             g[i] = -exp(A_log[h]) * softplus(a[i] + bias);
             if (b && beta) beta[i] = sigmoid(b[i]);
         }
+}
+
+/* ------------------------------------------------------------------------ */
+/* causal depthwise short convolution                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [LinAttn-conv]: a depthwise Conv1d (one K-tap filter per channel, no bias)
+ * with K-1 zeros of left padding, cut back to the sequence length, then SiLU:
+ *     out[t][c] = silu( sum_{j<K} w[c][j] * xp[t + j][c] ),
+ *     xp = [K-1 history rows ; x_0 ... x_{T-1}]
+ * so tap K-1 multiplies the current token (the page's step-by-step picture).
+ * The history rows are zeros (the page's padding) or, for a sequence continued
+ * from an earlier call, its carried state, oldest first: state[c][j] =
+ * xp[j][c].  After the sequence, state_out holds the last K-1 rows of xp.
+ * x, out [total_T][channels]; w [channels][K]; state_in/out
+ * [num_seqs][channels][K-1] (either may be NULL); silu = 0 skips the SiLU.
+ * Returns -1 on a malformed cu_seqlens.
+ */
+int gdn_oracle_short_conv(const double* x, const double* w, const int32_t* cu_seqlens, int num_seqs,
+                          int channels, int K, const double* state_in, double* out,
+                          double* state_out, int silu)
+{
+    for (int n = 0; n < num_seqs; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return -1;
+    double* xp = NULL;
+    for (int n = 0; n < num_seqs; ++n) {
+        const long bos = cu_seqlens[n], T = cu_seqlens[n + 1] - cu_seqlens[n];
+        xp = (double*)realloc(xp, sizeof(double) * (size_t)(T + K - 1 > 0 ? T + K - 1 : 1));
+        for (int c = 0; c < channels; ++c) {
+            for (int j = 0; j < K - 1; ++j)
+                xp[j] = state_in ? state_in[((long)n * channels + c) * (K - 1) + j] : 0.0;
+            for (long t = 0; t < T; ++t) xp[K - 1 + t] = x[(bos + t) * channels + c];
+            for (long t = 0; t < T; ++t) {
+                double acc = 0.0;
+                for (int j = 0; j < K; ++j) acc += w[(long)c * K + j] * xp[t + j];
+                out[(bos + t) * channels + c] = silu ? acc * sigmoid(acc) : acc;
+            }
+            if (state_out)
+                for (int j = 0; j < K - 1; ++j)
+                    state_out[((long)n * channels + c) * (K - 1) + j] = xp[T + j];
+        }
+    }
+    free(xp);
+    return 0;
 }

@@ -340,16 +340,184 @@ def test_gates_from_logits():
 
 
 # --------------------------------------------------------------------------------------
+# grouped query/key heads: "5. 线性注意力" forward code, repeat_interleave of q and k
+# --------------------------------------------------------------------------------------
+
+def test_grouped_heads_equal_interleaved_repeat():
+    """With Hk query/key heads and H = r * Hk value heads, the page repeats each query/key head r
+    times in place (repeat_interleave along the head axis) before the core; the grouped call must
+    equal the core on those expanded inputs, for every form."""
+    rng = np.random.default_rng(50)
+    T, Hk, r, dk, dv = 21, 2, 3, 5, 4
+    q = rng.standard_normal((T, Hk, dk))
+    k = rng.standard_normal((T, Hk, dk))
+    v = rng.standard_normal((T, Hk * r, dv))
+    g = -rng.random((T, Hk * r))
+    beta = rng.random((T, Hk * r))
+    S0 = rng.standard_normal((1, Hk * r, dv, dk)) * 0.3
+    qe, ke = np.repeat(q, r, axis=1), np.repeat(k, r, axis=1)   # numpy repeat == repeat_interleave
+    for fn in (oracle.recurrence, lambda *a, **kw: oracle.chunked(*a, C=4, **kw),
+               oracle.transition_product):
+        y, S = fn(q, k, v, g, beta, initial_state=S0)
+        ye, Se = fn(qe, ke, v, g, beta, initial_state=S0)
+        np.testing.assert_allclose(y, ye, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(S, Se, rtol=1e-12, atol=1e-12)
+    # the interleaved order matters: tiling the heads instead gives another result
+    yt, _ = oracle.recurrence(np.tile(q, (1, r, 1)), np.tile(k, (1, r, 1)), v, g, beta, initial_state=S0)
+    assert np.abs(yt - ye).max() > 1e-3
+
+
+# --------------------------------------------------------------------------------------
+# decay per key channel: "6.6 Gated DeltaNet" 6.6.7 (alpha_t a vector over channels)
+# --------------------------------------------------------------------------------------
+
+def _pc_inputs(rng, T, H, dk, dv):
+    q, k, v, _, beta = _rand_inputs(rng, T, H, dk, dv)
+    g = -rng.random((T, H, dk)) * 0.8
+    return q, k, v, g, beta
+
+
+def test_per_channel_equal_channels_is_scalar_decay():
+    """A per-channel decay with every channel equal is the scalar decay of the head."""
+    rng = np.random.default_rng(51)
+    q, k, v, g, beta = _rand_inputs(rng, 19, 2, 6, 5)
+    S0 = rng.standard_normal((1, 2, 5, 6)) * 0.2
+    gpc = np.repeat(g[:, :, None], 6, axis=2)
+    for fn in (oracle.recurrence, oracle.transition_product):
+        y, S = fn(q, k, v, gpc, beta, initial_state=S0)
+        ys, Ss = oracle.recurrence(q, k, v, g, beta, initial_state=S0)
+        np.testing.assert_allclose(y, ys, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(S, Ss, rtol=1e-12, atol=1e-13)
+
+
+def test_per_channel_beta_zero_closed_form():
+    """beta = 0: nothing is written, so S_t = S_0 diag(prod_s alpha_s) and y_t = S_t q_t with the
+    products taken channel by channel over the key axis."""
+    rng = np.random.default_rng(52)
+    T, H, dk, dv = 13, 2, 6, 5
+    q, k, v, g, beta = _pc_inputs(rng, T, H, dk, dv)
+    beta[:] = 0.0
+    S0 = rng.standard_normal((1, H, dv, dk))
+    y, S = oracle.recurrence(q, k, v, g, beta, initial_state=S0, use_qk_l2norm=False, scale=1.0)
+    gsum = np.cumsum(g, axis=0)                      # [T, H, dk]
+    for t in range(T):
+        for h in range(H):
+            St = S0[0, h] * np.exp(gsum[t, h])[None, :]
+            np.testing.assert_allclose(y[t, h], St @ q[t, h], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S[0], S0[0] * np.exp(gsum[-1])[:, None, :], rtol=1e-12)
+
+
+def test_per_channel_unit_key_invariant():
+    """||k|| = 1, beta = 1: the write makes S_t k_t = v_t whatever the decay, so with q = k the
+    output is scale * v_t exactly."""
+    rng = np.random.default_rng(53)
+    T, H, dk, dv = 17, 2, 8, 6
+    _, k, v, g, beta = _pc_inputs(rng, T, H, dk, dv)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    beta[:] = 1.0
+    S0 = rng.standard_normal((1, H, dv, dk))
+    y, _ = oracle.recurrence(k, k, v, g, beta, initial_state=S0, use_qk_l2norm=False, scale=0.5)
+    np.testing.assert_allclose(y, 0.5 * v, rtol=1e-10, atol=1e-12)
+
+
+def test_per_channel_transition_equals_recurrence():
+    """The unrolled product form with A_t = diag(alpha_t)(I - beta k k^T) built as explicit dense
+    matrices equals the token loop."""
+    rng = np.random.default_rng(54)
+    q, k, v, g, beta = _pc_inputs(rng, 9, 2, 5, 4)
+    S0 = rng.standard_normal((1, 2, 4, 5)) * 0.5
+    y1, S1 = oracle.recurrence(q, k, v, g, beta, initial_state=S0)
+    y2, S2 = oracle.transition_product(q, k, v, g, beta, initial_state=S0)
+    np.testing.assert_allclose(y1, y2, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(S1, S2, rtol=1e-11, atol=1e-12)
+
+
+def test_per_channel_decay_not_taken_by_chunked_form():
+    rng = np.random.default_rng(55)
+    q, k, v, g, beta = _pc_inputs(rng, 8, 1, 4, 4)
+    with pytest.raises(ValueError):
+        oracle.chunked(q, k, v, g, beta, C=4)
+
+
+# --------------------------------------------------------------------------------------
+# causal depthwise short convolution: "5. 线性注意力", "因果卷积(Causal Conv1d)"
+# --------------------------------------------------------------------------------------
+
+def _silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def test_conv_identity_tap_is_silu():
+    """A filter that keeps only the current token (tap K-1 = 1, the rest 0) gives SiLU(x)."""
+    rng = np.random.default_rng(56)
+    x = rng.standard_normal((11, 7))
+    w = np.zeros((7, 4))
+    w[:, 3] = 1.0
+    y, st = oracle.short_conv(x, w)
+    np.testing.assert_allclose(y, _silu(x), rtol=1e-15, atol=1e-16)
+    y0, _ = oracle.short_conv(x, w, activation=False)
+    np.testing.assert_array_equal(y0, x)
+
+
+def test_conv_impulse_response():
+    """The page's step-by-step picture: output t sees inputs t-3..t, the current one last, so a
+    unit impulse at t = 0 reads the filter back in reverse, then zeros (SiLU(0) = 0)."""
+    w = np.array([[0.5, -1.0, 2.0, 0.25]])
+    x = np.zeros((7, 1))
+    x[0, 0] = 1.0
+    y, _ = oracle.short_conv(x, w)
+    expect = _silu(np.array([0.25, 2.0, -1.0, 0.5, 0.0, 0.0, 0.0]))
+    np.testing.assert_allclose(y[:, 0], expect, rtol=1e-15)
+
+
+def test_conv_matches_library_conv1d():
+    """One sequence from zero history equals the page's nn.Conv1d(groups=C, padding=K-1) cut back
+    to T, followed by SiLU (torch.nn.functional on the CPU, float64)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(57)
+    T, Cn, K = 23, 9, 4
+    x = rng.standard_normal((T, Cn))
+    w = rng.standard_normal((Cn, K))
+    ref = torch.nn.functional.conv1d(torch.tensor(x.T[None]), torch.tensor(w[:, None, :]),
+                                     padding=K - 1, groups=Cn)[0, :, :T]
+    ref = torch.nn.functional.silu(ref).numpy().T
+    y, _ = oracle.short_conv(x, w)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_conv_varlen_split_and_state():
+    """Packed sequences do not see each other; the final state holds the last K-1 inputs, oldest
+    first (for short sequences the older part comes from the initial state); a sequence split in
+    two with the state carried across equals the whole."""
+    rng = np.random.default_rng(58)
+    Cn, K = 5, 4
+    lens = [9, 2, 0, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    x = rng.standard_normal((cu[-1], Cn))
+    w = rng.standard_normal((Cn, K))
+    s0 = rng.standard_normal((len(lens), Cn, K - 1))
+    y, st = oracle.short_conv(x, w, cu_seqlens=cu, state=s0)
+    for n, L in enumerate(lens):
+        yn, stn = oracle.short_conv(x[cu[n]:cu[n + 1]], w, state=s0[n:n + 1])
+        np.testing.assert_array_equal(y[cu[n]:cu[n + 1]], yn)
+        hist = np.concatenate([s0[n].T, x[cu[n]:cu[n + 1]]])   # [K-1+L, Cn], oldest first
+        np.testing.assert_array_equal(st[n], hist[-(K - 1):].T)
+    xa = x[:9]
+    ya, sa = oracle.short_conv(xa, w)
+    y1, s1 = oracle.short_conv(xa[:4], w)
+    y2, s2 = oracle.short_conv(xa[4:], w, state=s1)
+    np.testing.assert_allclose(np.concatenate([y1, y2]), ya, rtol=1e-15)
+    np.testing.assert_array_equal(s2, sa)
+
+
+# --------------------------------------------------------------------------------------
 # planted mistakes: each mutation of the oracle must be caught by a pin above
 # --------------------------------------------------------------------------------------
 
 MUTATIONS = {
     # delta read from the undecayed state (decay applied after the prediction)
-    "undecayed_prediction": ("        for (int i = 0; i < dv * dk; ++i) S[i] *= alpha;\n"
-                             "        for (int r = 0; r < dv; ++r) {\n"
-                             "            double pred = 0.0;",
-                             "        for (int r = 0; r < dv; ++r) {\n"
-                             "            double pred = 0.0;"),
+    "undecayed_prediction": ("for (int j = 0; j < dk; ++j) pred += S[(long)r * dk + j] * kn[j];",
+                             "for (int j = 0; j < dk; ++j) pred += S[(long)r * dk + j] / al[j] * kn[j];"),
     # beta dropped from the write
     "dropped_beta": ("S[(long)r * dk + j] += beta * e[r] * kn[j];",
                      "S[(long)r * dk + j] += e[r] * kn[j];"),
@@ -367,6 +535,23 @@ MUTATIONS = {
                   "a = bt[i] * dot * decay[(long)i * L + j];"),
     # rms over the sum instead of the mean
     "rms_sum": ("ms /= dv;", "ms /= 1;"),
+    # grouped heads tiled (h % Hk) instead of interleaved (h / r)
+    "gva_modulo": ("const int hk = h / (j->H / j->Hk);", "const int hk = h % j->Hk;"),
+    # per-channel decay applied to the value rows of S instead of its key columns
+    "decay_on_rows": ("for (int j = 0; j < dk; ++j) S[(long)r * dk + j] *= al[j];",
+                      "for (int j = 0; j < dk; ++j) S[(long)r * dk + j] *= al[r % dk];"),
+    # transition matrix with the per-channel decay on the wrong side
+    "transition_decay_side": ("alpha * ((i == j ? 1.0 : 0.0) - beta * kn[i] * kn[j]);",
+                              "exp(s->g_per_channel ? gt[j] : gt[0]) * ((i == j ? 1.0 : 0.0) - beta * kn[i] * kn[j]);"),
+    # convolution taps in reverse order
+    "conv_taps_reversed": ("acc += w[(long)c * K + j] * xp[t + j];",
+                           "acc += w[(long)c * K + (K - 1 - j)] * xp[t + j];"),
+    # carried convolution state stored newest first
+    "conv_state_newest_first": ("state_out[((long)n * channels + c) * (K - 1) + j] = xp[T + j];",
+                                "state_out[((long)n * channels + c) * (K - 1) + j] = xp[T + K - 2 - j];"),
+    # SiLU left out of the convolution
+    "conv_no_silu": ("out[(bos + t) * channels + c] = silu ? acc * sigmoid(acc) : acc;",
+                     "out[(bos + t) * channels + c] = acc;"),
 }
 
 
@@ -396,6 +581,15 @@ PIN_TESTS = [
     test_beta_zero_is_pure_decay,
     lambda: test_chunked_equals_recurrence(65, 16),
     test_gate_rmsnorm_silu_special_cases_and_library,
+    test_grouped_heads_equal_interleaved_repeat,
+    test_per_channel_equal_channels_is_scalar_decay,
+    test_per_channel_beta_zero_closed_form,
+    test_per_channel_unit_key_invariant,
+    test_per_channel_transition_equals_recurrence,
+    test_conv_identity_tap_is_silu,
+    test_conv_impulse_response,
+    test_conv_matches_library_conv1d,
+    test_conv_varlen_split_and_state,
 ]
 
 
