@@ -17,6 +17,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libgdn.so")
 
 GDN_F32, GDN_BF16 = 0, 1
+GDN_DECAY_PER_HEAD, GDN_DECAY_PER_KEY_CHANNEL = 0, 1
+GDN_CONV_KERNEL = 4
 STATUS = {0: "GDN_OK", -1: "GDN_ERR_ARG", -2: "GDN_ERR_DTYPE", -3: "GDN_ERR_CU_SEQLENS",
           -4: "GDN_ERR_WORKSPACE", -5: "GDN_ERR_LAUNCH", -6: "GDN_ERR_TIMEOUT",
           -7: "GDN_ERR_UNSUPPORTED", -8: "GDN_ERR_CUDA"}
@@ -28,17 +30,17 @@ _vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
 _i, _f, _sz, _l = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
 
 SIGNATURES = {
-    "gdn_chunk_fwd": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
-                           _fp, _fp, _f, _vp, _i, _vp, _sz, _vp]),
+    "gdn_chunk_fwd": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                           _fp, _fp, _fp, _fp, _fp, _fp, _fp, _f, _vp, _i, _vp, _sz, _vp]),
     "gdn_chunk_fwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
-    "gdn_recurrent_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
-                                _f, _vp, _i, _vp]),
-    "gdn_recurrent_multi_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _ip, _i, _i, _i, _i, _i, _i, _f,
-                                      _i, _fp, _fp, _f, _vp, _i, _vp]),
+    "gdn_recurrent_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                                _fp, _fp, _fp, _fp, _fp, _f, _vp, _i, _vp]),
+    "gdn_recurrent_multi_step": (_i, [_vp, _vp, _vp, _fp, _fp, _fp, _i, _ip, _i, _i, _i, _i, _i, _i, _i,
+                                      _i, _f, _i, _fp, _fp, _fp, _fp, _fp, _f, _vp, _i, _vp]),
     "gdn_gate_rmsnorm_silu": (_i, [_vp, _i, _fp, _fp, _f, _vp, _i, _l, _i, _vp]),
     "gdn_decay_from_logits": (_i, [_fp, _fp, _fp, _fp, _fp, _fp, _l, _i, _vp]),
-    "gdn_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _f, _i, _fp, _fp,
-                                   _fp, _fp, _f, _vp, _i, _vp]),
+    "gdn_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _fp, _fp, _ip, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                                   _fp, _fp, _fp, _fp, _fp, _fp, _fp, _f, _vp, _i, _vp]),
     "gdn_get_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "gdn_status_string": (ctypes.c_char_p, [_i]),
 }
@@ -110,15 +112,30 @@ def _check(fn, rc):
         raise GdnError(fn, rc)
 
 
+def _decay_mode(g, per_head_dims):
+    """GDN_DECAY_PER_HEAD when g has the per-head shape, else one decay per key channel."""
+    return GDN_DECAY_PER_HEAD if g.dim() == per_head_dims else GDN_DECAY_PER_KEY_CHANNEL
+
+
+def _conv_f32(conv_weight, conv_state, conv_state_out):
+    for name, t in (("conv_weight", conv_weight), ("conv_state", conv_state),
+                    ("conv_state_out", conv_state_out)):
+        _f32(t, name)
+
+
 def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0, use_qk_l2norm=True,
-                  initial_state=None, final_state=None, output_final_state=True, gate_z=None,
-                  norm_weight=None, norm_eps=1e-6, out=None, out_dtype=None, workspace=None,
-                  stream=None):
-    """Chunked prefill.  q, k [total_T, H, d_k]; v [total_T, H, d_v]; g, beta [total_T, H] fp32;
+                  initial_state=None, final_state=None, output_final_state=True, conv_weight=None,
+                  conv_state=None, conv_state_out=None, gate_z=None, norm_weight=None, norm_eps=1e-6,
+                  out=None, out_dtype=None, workspace=None, stream=None):
+    """Chunked prefill.  q, k [total_T, H_k, d_k]; v [total_T, H, d_v] (H a multiple of H_k);
+    beta [total_T, H] fp32; g [total_T, H] fp32, or [total_T, H, d_k] for a decay per key channel;
     cu_seqlens int32 [num_seqs+1] (device) or None with num_seqs equal sequences (default 1).
+    conv_weight [2 H_k d_k + H d_v, 4] fuses the short convolution (conv_state: carried input
+    history [num_seqs, conv_dim, 3] or None; conv_state_out: filled with the final history if
+    given, may be conv_state itself).
     Returns (out, final_state); final_state is allocated unless given or not requested."""
-    total_T, H, d_k = q.shape
-    d_v = v.shape[-1]
+    total_T, H_k, d_k = q.shape
+    H, d_v = v.shape[1], v.shape[-1]
     if cu_seqlens is not None:
         if cu_seqlens.dtype != torch.int32:
             raise TypeError("cu_seqlens must be int32")
@@ -138,26 +155,29 @@ def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0, u
     for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state),
                     ("final_state", final_state), ("gate_z", gate_z), ("norm_weight", norm_weight)):
         _f32(t, name)
+    _conv_f32(conv_weight, conv_state, conv_state_out)
     L = lib()
     ws_need = L.gdn_chunk_fwd_workspace_size(num_seqs, total_T, H, d_k, d_v, dt)
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     rc = L.gdn_chunk_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs, total_T,
-                         H, d_k, d_v, dt, float(scale), int(bool(use_qk_l2norm)), _p(initial_state),
-                         _p(final_state), _p(gate_z), _p(norm_weight), float(norm_eps), _p(out), odt,
-                         _p(workspace), workspace.numel() if workspace is not None else 0,
-                         _stream(stream))
+                         H, H_k, d_k, d_v, dt, _decay_mode(g, 2), float(scale),
+                         int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state),
+                         _p(conv_state_out), _p(initial_state), _p(final_state), _p(gate_z),
+                         _p(norm_weight), float(norm_eps), _p(out), odt, _p(workspace),
+                         workspace.numel() if workspace is not None else 0, _stream(stream))
     _check("gdn_chunk_fwd", rc)
     return out, final_state
 
 
 def gdn_chunk_fwd_noalloc(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0,
-                          use_qk_l2norm=True, initial_state=None, final_state=None, gate_z=None,
-                          norm_weight=None, norm_eps=1e-6, out=None, stream=None):
+                          use_qk_l2norm=True, initial_state=None, final_state=None, conv_weight=None,
+                          conv_state=None, conv_state_out=None, gate_z=None, norm_weight=None,
+                          norm_eps=1e-6, out=None, stream=None):
     """gdn_chunk_fwd with the library's fixed scratch array instead of a workspace; `out` and
     `final_state` must be passed in (this call allocates nothing, here or in the library)."""
-    total_T, H, d_k = q.shape
-    d_v = v.shape[-1]
+    total_T, H_k, d_k = q.shape
+    H, d_v = v.shape[1], v.shape[-1]
     if out is None:
         raise ValueError("gdn_chunk_fwd_noalloc needs a preallocated `out`")
     if cu_seqlens is not None:
@@ -170,20 +190,26 @@ def gdn_chunk_fwd_noalloc(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scal
     for name, t in (("g", g), ("beta", beta), ("initial_state", initial_state),
                     ("final_state", final_state), ("gate_z", gate_z), ("norm_weight", norm_weight)):
         _f32(t, name)
+    _conv_f32(conv_weight, conv_state, conv_state_out)
     rc = lib().gdn_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs,
-                                     total_T, H, d_k, d_v, dt, float(scale), int(bool(use_qk_l2norm)),
-                                     _p(initial_state), _p(final_state), _p(gate_z), _p(norm_weight),
-                                     float(norm_eps), _p(out), _dt(out), _stream(stream))
+                                     total_T, H, H_k, d_k, d_v, dt, _decay_mode(g, 2), float(scale),
+                                     int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state),
+                                     _p(conv_state_out), _p(initial_state), _p(final_state),
+                                     _p(gate_z), _p(norm_weight), float(norm_eps), _p(out), _dt(out),
+                                     _stream(stream))
     _check("gdn_chunk_fwd_noalloc", rc)
     return out, final_state
 
 
-def gdn_recurrent_step(q, k, v, g, beta, state, scale=0.0, use_qk_l2norm=True, gate_z=None,
-                       norm_weight=None, norm_eps=1e-6, out=None, out_dtype=None, stream=None):
-    """One decode token: q, k [N, H, d_k]; v [N, H, d_v]; g, beta [N, H]; state [N, H, d_v, d_k]
-    fp32 updated in place.  Returns out [N, H, d_v]."""
-    N, H, d_k = q.shape
-    d_v = v.shape[-1]
+def gdn_recurrent_step(q, k, v, g, beta, state, scale=0.0, use_qk_l2norm=True, conv_weight=None,
+                       conv_state=None, conv_state_out=None, gate_z=None, norm_weight=None,
+                       norm_eps=1e-6, out=None, out_dtype=None, stream=None):
+    """One decode token: q, k [N, H_k, d_k]; v [N, H, d_v]; beta [N, H]; g [N, H] or [N, H, d_k];
+    state [N, H, d_v, d_k] fp32 updated in place.  conv_weight [conv_dim, 4] fuses the short
+    convolution with history conv_state [N, conv_dim, 3] (None: zeros) and the new history written
+    to conv_state_out (may be conv_state when H_k == H).  Returns out [N, H, d_v]."""
+    N, H_k, d_k = q.shape
+    H, d_v = v.shape[1], v.shape[-1]
     dt = _dt(q)
     odt = dt if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
     if out is None:
@@ -193,21 +219,25 @@ def gdn_recurrent_step(q, k, v, g, beta, state, scale=0.0, use_qk_l2norm=True, g
     for name, t in (("g", g), ("beta", beta), ("state", state), ("gate_z", gate_z),
                     ("norm_weight", norm_weight)):
         _f32(t, name)
-    rc = lib().gdn_recurrent_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state), N, H, d_k, d_v,
-                                  dt, float(scale), int(bool(use_qk_l2norm)), _p(gate_z),
+    _conv_f32(conv_weight, conv_state, conv_state_out)
+    rc = lib().gdn_recurrent_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state), N, H, H_k, d_k,
+                                  d_v, dt, _decay_mode(g, 2), float(scale), int(bool(use_qk_l2norm)),
+                                  _p(conv_weight), _p(conv_state), _p(conv_state_out), _p(gate_z),
                                   _p(norm_weight), float(norm_eps), _p(out), odt, _stream(stream))
     _check("gdn_recurrent_step", rc)
     return out
 
 
 def gdn_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices=None, scale=0.0,
-                             use_qk_l2norm=True, gate_z=None, norm_weight=None, norm_eps=1e-6,
+                             use_qk_l2norm=True, conv_weight=None, conv_state=None,
+                             conv_state_out=None, gate_z=None, norm_weight=None, norm_eps=1e-6,
                              out=None, out_dtype=None, stream=None):
-    """T decode tokens per sequence on pooled states: q, k [N, T, H, d_k]; v [N, T, H, d_v];
-    g, beta [N, T, H]; state_pool [slots, H, d_v, d_k] fp32 updated in place; state_indices int32
-    [N] (negative = skip) or None.  Returns out [N, T, H, d_v]."""
-    N, T, H, d_k = q.shape
-    d_v = v.shape[-1]
+    """T decode tokens per sequence on pooled states: q, k [N, T, H_k, d_k]; v [N, T, H, d_v];
+    beta [N, T, H]; g [N, T, H] or [N, T, H, d_k]; state_pool [slots, H, d_v, d_k] fp32 updated in
+    place; state_indices int32 [N] (negative = skip) or None; conv_state / conv_state_out
+    [slots, conv_dim, 3] indexed like the pool.  Returns out [N, T, H, d_v]."""
+    N, T, H_k, d_k = q.shape
+    H, d_v = v.shape[2], v.shape[-1]
     dt = _dt(q)
     odt = dt if out_dtype is None else _dt(torch.empty(0, dtype=out_dtype))
     if out is None:
@@ -219,11 +249,13 @@ def gdn_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices=None, s
     for name, t in (("g", g), ("beta", beta), ("state_pool", state_pool), ("gate_z", gate_z),
                     ("norm_weight", norm_weight)):
         _f32(t, name)
+    _conv_f32(conv_weight, conv_state, conv_state_out)
     rc = lib().gdn_recurrent_multi_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool),
-                                        state_pool.shape[0], _p(state_indices), N, T, H, d_k, d_v,
-                                        dt, float(scale), int(bool(use_qk_l2norm)), _p(gate_z),
-                                        _p(norm_weight), float(norm_eps), _p(out), odt,
-                                        _stream(stream))
+                                        state_pool.shape[0], _p(state_indices), N, T, H, H_k, d_k,
+                                        d_v, dt, _decay_mode(g, 3), float(scale),
+                                        int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state),
+                                        _p(conv_state_out), _p(gate_z), _p(norm_weight),
+                                        float(norm_eps), _p(out), odt, _stream(stream))
     _check("gdn_recurrent_multi_step", rc)
     return out
 

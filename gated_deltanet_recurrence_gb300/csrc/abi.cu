@@ -30,6 +30,21 @@ int* device_error_ptr() {
 bool valid_dtype(int d) { return d == GDN_F32 || d == GDN_BF16; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool head_size_ok(int d_k, int d_v) { return d_k == d_v && (d_k == 64 || d_k == 128); }
+bool heads_ok(int H, int H_k) { return H > 0 && H_k >= 1 && H_k <= H && H % H_k == 0; }
+bool valid_decay(int d) { return d == GDN_DECAY_PER_HEAD || d == GDN_DECAY_PER_KEY_CHANNEL; }
+
+// Checks the short-convolution arguments and fills c; `rows` is the number of state rows (sequences
+// or pool slots).  Decode updates may be in place only without grouped heads.
+int conv_args(const float* w, const float* st_in, float* st_out, int H, int H_k, int d, long rows,
+              bool decode, gdn::ConvArgs& c) {
+    c = gdn::ConvArgs{};
+    if (!w) return (st_in || st_out) ? GDN_ERR_ARG : GDN_OK;
+    const long long dim = 2LL * H_k * d + (long long)H * d;
+    if (dim > 0x7fffffffLL / 4 || (long long)rows * dim * 3 > (1LL << 40)) return GDN_ERR_ARG;
+    if (decode && st_in && st_in == st_out && H_k != H) return GDN_ERR_ARG;
+    c.w = w; c.state_in = st_in; c.state_out = st_out; c.dim = (int)dim;
+    return GDN_OK;
+}
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH; }
 
@@ -67,9 +82,9 @@ int gdn_get_device_error(void* stream, int* device_status) {
     return GDN_OK;
 }
 
-// The tensor-core path (bf16, d = 128) keeps per-chunk intermediates (W, U^T, the decayed Q K^T
-// and per-token factors, about 41 KB per chunk and head) in the caller's workspace; the fp32
-// CUDA-core path needs none.
+// The tensor-core path (bf16, d = 128, one decay per head) keeps per-chunk intermediates (W, U^T,
+// the decayed Q K^T and per-token factors, about 41 KB per chunk and head) in the caller's
+// workspace; the fp32 CUDA-core path needs none.
 static bool uses_tc_path(int num_seqs, int total_T, int H, int d_k, int d_v, int qkv_dtype) {
     return qkv_dtype == GDN_BF16 && d_k == 128 && d_v == 128 && total_T > 0 && num_seqs > 0 && H > 0;
 }
@@ -81,30 +96,36 @@ size_t gdn_chunk_fwd_workspace_size(int num_seqs, int total_T, int H, int d_k, i
 }
 
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int d_k, int d_v,
-                  gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
-                  const float* initial_state, float* final_state,
+                  const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int H_k,
+                  int d_k, int d_v, gdn_dtype qkv_dtype, gdn_decay decay, float scale,
+                  int use_qk_l2norm, const float* conv_weight, const float* conv_state_in,
+                  float* conv_state_out, const float* initial_state, float* final_state,
                   const float* gate_z, const float* norm_weight, float norm_eps,
                   void* out, gdn_dtype out_dtype,
                   void* workspace, size_t workspace_bytes, void* stream) {
     if (!valid_dtype(qkv_dtype) || !valid_dtype(out_dtype)) return GDN_ERR_DTYPE;
-    if (num_seqs <= 0 || total_T < 0 || H <= 0) return GDN_ERR_ARG;
+    if (num_seqs <= 0 || total_T < 0 || !heads_ok(H, H_k) || !valid_decay(decay)) return GDN_ERR_ARG;
     if (!head_size_ok(d_k, d_v)) return GDN_ERR_UNSUPPORTED;
     if ((long long)num_seqs * H > 0x7fffffffLL) return GDN_ERR_ARG;
     if (!cu_seqlens && total_T % num_seqs != 0) return GDN_ERR_ARG;
     if (total_T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;
     if (!(norm_eps >= 0.0f) || (gate_z == nullptr && norm_weight != nullptr)) return GDN_ERR_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, initial_state, final_state, gate_z, norm_weight, out};
+    const void* ptrs[] = {q, k, v, g, beta, initial_state, final_state, gate_z, norm_weight, out,
+                          conv_weight, conv_state_in, conv_state_out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_ARG;
+    gdn::ConvArgs conv;
+    const int crc = conv_args(conv_weight, conv_state_in, conv_state_out, H, H_k, d_k, num_seqs, false, conv);
+    if (crc != GDN_OK) return crc;
     const size_t need = gdn_chunk_fwd_workspace_size(num_seqs, total_T, H, d_k, d_v, qkv_dtype);
     if (need > 0 && (!workspace || workspace_bytes < need)) return GDN_ERR_WORKSPACE;
-    if (total_T == 0 && !final_state) return GDN_OK;
+    if (total_T == 0 && !final_state && !conv_state_out) return GDN_OK;
 
     gdn::PrefillArgs a{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
-    a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs; a.total_T = total_T; a.H = H; a.d = d_k;
-    a.qkv_dtype = qkv_dtype;
+    a.cu_seqlens = cu_seqlens; a.num_seqs = num_seqs; a.total_T = total_T; a.H = H; a.Hk = H_k;
+    a.d = d_k; a.qkv_dtype = qkv_dtype; a.g_per_channel = decay == GDN_DECAY_PER_KEY_CHANNEL;
+    a.conv = conv;
     a.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)d_k);
     a.use_l2 = use_qk_l2norm ? 1 : 0;
     a.initial_state = initial_state; a.final_state = final_state;
@@ -113,61 +134,75 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
     a.err = device_error_ptr();
     if (!a.err) return GDN_ERR_CUDA;
     if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_WORKSPACE;
-    if (uses_tc_path(num_seqs, total_T, H, d_k, d_v, qkv_dtype) && gdn::prefill_tc_supported(a))
-        return launch_status(gdn::launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
-    return launch_status(gdn::launch_prefill_simt(a, static_cast<cudaStream_t>(stream)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (total_T > 0 || final_state) {
+        if (uses_tc_path(num_seqs, total_T, H, d_k, d_v, qkv_dtype) && !a.g_per_channel &&
+            gdn::prefill_tc_supported(a))
+            e = gdn::launch_prefill_tc(a, st);
+        else
+            e = gdn::launch_prefill_simt(a, st);
+    }
+    // the final convolution state is written after every kernel that reads the input state
+    if (e == cudaSuccess && conv.state_out) e = gdn::launch_conv_state(a, st);
+    return launch_status(e);
 }
 
-int gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
-                       const float* beta, float* state, int N, int H, int d_k, int d_v,
-                       gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
-                       const float* gate_z, const float* norm_weight, float norm_eps,
-                       void* out, gdn_dtype out_dtype, void* stream) {
+static int decode_entry(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float* state, int num_slots, const int32_t* idx, int N,
+                        int T, int H, int H_k, int d_k, int d_v, gdn_dtype qkv_dtype,
+                        gdn_decay decay, float scale, int use_qk_l2norm, const float* conv_weight,
+                        const float* conv_state_in, float* conv_state_out, const float* gate_z,
+                        const float* norm_weight, float norm_eps, void* out, gdn_dtype out_dtype,
+                        void* stream) {
     if (!valid_dtype(qkv_dtype) || !valid_dtype(out_dtype)) return GDN_ERR_DTYPE;
-    if (N < 0 || H <= 0) return GDN_ERR_ARG;
+    if (N < 0 || T <= 0 || !heads_ok(H, H_k) || num_slots <= 0 || !valid_decay(decay)) return GDN_ERR_ARG;
     if (!head_size_ok(d_k, d_v)) return GDN_ERR_UNSUPPORTED;
-    if ((long long)N * H > 0x7fffffffLL) return GDN_ERR_ARG;
+    if ((long long)N * H > 0x7fffffffLL || (long long)N * T * H * d_k > (1LL << 40)) return GDN_ERR_ARG;
+    if (!idx && num_slots < N) return GDN_ERR_ARG;
     if (N == 0) return GDN_OK;
     if (!q || !k || !v || !g || !beta || !state || !out) return GDN_ERR_ARG;
     if (!(norm_eps >= 0.0f) || (gate_z == nullptr && norm_weight != nullptr)) return GDN_ERR_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, state, gate_z, norm_weight, out};
+    const void* ptrs[] = {q, k, v, g, beta, state, gate_z, norm_weight, out, conv_weight,
+                          conv_state_in, conv_state_out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return GDN_ERR_ARG;
     gdn::DecodeArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state;
-    a.N = N; a.H = H; a.d = d_k; a.qkv_dtype = qkv_dtype;
-    a.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)d_k);
-    a.use_l2 = use_qk_l2norm ? 1 : 0;
-    a.z = gate_z; a.w = norm_weight; a.eps = norm_eps; a.out = out; a.out_dtype = out_dtype;
-    return launch_status(gdn::launch_decode(a, static_cast<cudaStream_t>(stream)));
-}
-
-int gdn_recurrent_multi_step(const void* q, const void* k, const void* v, const float* g,
-                             const float* beta, float* state_pool, int num_slots,
-                             const int32_t* state_indices, int N, int T, int H, int d_k, int d_v,
-                             gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
-                             const float* gate_z, const float* norm_weight, float norm_eps,
-                             void* out, gdn_dtype out_dtype, void* stream) {
-    if (!valid_dtype(qkv_dtype) || !valid_dtype(out_dtype)) return GDN_ERR_DTYPE;
-    if (N < 0 || T <= 0 || H <= 0 || num_slots <= 0) return GDN_ERR_ARG;
-    if (!head_size_ok(d_k, d_v)) return GDN_ERR_UNSUPPORTED;
-    if ((long long)N * H > 0x7fffffffLL || (long long)N * T * H * d_k > (1LL << 40)) return GDN_ERR_ARG;
-    if (!state_indices && num_slots < N) return GDN_ERR_ARG;
-    if (N == 0) return GDN_OK;
-    if (!q || !k || !v || !g || !beta || !state_pool || !out) return GDN_ERR_ARG;
-    if (!(norm_eps >= 0.0f) || (gate_z == nullptr && norm_weight != nullptr)) return GDN_ERR_ARG;
-    const void* ptrs[] = {q, k, v, g, beta, state_pool, gate_z, norm_weight, out};
-    for (const void* p : ptrs)
-        if (p && !aligned16(p)) return GDN_ERR_ARG;
-    gdn::DecodeMultiArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state_pool; a.num_slots = num_slots;
-    a.idx = state_indices; a.N = N; a.T = T; a.H = H; a.d = d_k; a.qkv_dtype = qkv_dtype;
+    const int crc = conv_args(conv_weight, conv_state_in, conv_state_out, H, H_k, d_k, num_slots, true, a.conv);
+    if (crc != GDN_OK) return crc;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.state = state; a.num_slots = num_slots;
+    a.idx = idx; a.N = N; a.T = T; a.H = H; a.Hk = H_k; a.d = d_k; a.qkv_dtype = qkv_dtype;
+    a.g_per_channel = decay == GDN_DECAY_PER_KEY_CHANNEL;
     a.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)d_k);
     a.use_l2 = use_qk_l2norm ? 1 : 0;
     a.z = gate_z; a.w = norm_weight; a.eps = norm_eps; a.out = out; a.out_dtype = out_dtype;
     a.err = device_error_ptr();
     if (!a.err) return GDN_ERR_CUDA;
-    return launch_status(gdn::launch_decode_multi(a, static_cast<cudaStream_t>(stream)));
+    return launch_status(gdn::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
+                       const float* beta, float* state, int N, int H, int H_k, int d_k, int d_v,
+                       gdn_dtype qkv_dtype, gdn_decay decay, float scale, int use_qk_l2norm,
+                       const float* conv_weight, const float* conv_state_in, float* conv_state_out,
+                       const float* gate_z, const float* norm_weight, float norm_eps,
+                       void* out, gdn_dtype out_dtype, void* stream) {
+    return decode_entry(q, k, v, g, beta, state, N > 0 ? N : 1, nullptr, N, 1, H, H_k, d_k, d_v,
+                        qkv_dtype, decay, scale, use_qk_l2norm, conv_weight, conv_state_in,
+                        conv_state_out, gate_z, norm_weight, norm_eps, out, out_dtype, stream);
+}
+
+int gdn_recurrent_multi_step(const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, float* state_pool, int num_slots,
+                             const int32_t* state_indices, int N, int T, int H, int H_k, int d_k,
+                             int d_v, gdn_dtype qkv_dtype, gdn_decay decay, float scale,
+                             int use_qk_l2norm, const float* conv_weight,
+                             const float* conv_state_in, float* conv_state_out,
+                             const float* gate_z, const float* norm_weight, float norm_eps,
+                             void* out, gdn_dtype out_dtype, void* stream) {
+    return decode_entry(q, k, v, g, beta, state_pool, num_slots, state_indices, N, T, H, H_k, d_k,
+                        d_v, qkv_dtype, decay, scale, use_qk_l2norm, conv_weight, conv_state_in,
+                        conv_state_out, gate_z, norm_weight, norm_eps, out, out_dtype, stream);
 }
 
 int gdn_gate_rmsnorm_silu(const void* y, gdn_dtype y_dtype, const float* z,

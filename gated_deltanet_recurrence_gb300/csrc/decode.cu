@@ -1,21 +1,22 @@
-// decode.cu -- one-token gated delta rule step on a kept fp32 state (gdn_recurrent_step).
+// decode.cu -- gated delta rule decode on kept fp32 states (gdn_recurrent_step and
+// gdn_recurrent_multi_step, which is the same kernel with T tokens and a state pool).
 //
 // "6.6 Gated DeltaNet" 6.6.8 and "[LLM Algorithms-2] Gated DeltaNet" section 4: per (sequence,
-// head) and per state row r (d_k contiguous),
-//     sk_r = s_r . k,  sq_r = s_r . q,
-//     delta_r = beta (v_r - alpha sk_r),
-//     s_r'  = alpha s_r + delta_r k,
-//     y_r   = s_r' . q = alpha sq_r + delta_r (k . q),
+// head) and per state row r (d_k contiguous), with alpha one value or one per key channel,
+//     sk_r = s_r . (alpha k),  sq_r = s_r . (alpha q),
+//     delta_r = beta (v_r - sk_r),
+//     s_r'  = alpha . s_r + delta_r k,
+//     y_r   = s_r' . q = sq_r + delta_r (k . q),
 // which is the decay / predict / write / read sequence of the recurrence with the read folded
 // into the same pass, so the state is read once and written once.
 //
 // HBM-bound: per (sequence, head) the kernel moves 2 * d_v * d_k * 4 bytes of state plus a few
-// hundred bytes of q, k, v, y.  Layout of the work: one CTA per (sequence, head); warp w owns 16
-// consecutive state rows; lane l holds d_k/32 consecutive columns of each row, so every row is
-// one fully coalesced 128-bit (d_k = 128) or 64-bit (d_k = 64) access per lane.  All 16 rows are
-// loaded before any arithmetic (16 x 16 B in flight per lane).  The 32 dot products of a warp
-// (16 rows x {k, q}) are reduced with a transposing butterfly: 31 shuffles leave dot product j
-// on lane j, instead of 5 shuffles per dot product.
+// hundred bytes of q, k, v, y per token.  Layout of the work: one CTA per (sequence, head); warp
+// w owns 16 consecutive state rows; lane l holds d_k/32 consecutive columns of each row, so every
+// row is one fully coalesced 128-bit (d_k = 128) or 64-bit (d_k = 64) access per lane.  All 16
+// rows are loaded before any arithmetic (16 x 16 B in flight per lane).  The 32 dot products of
+// a warp (16 rows x {k, q}) are reduced with a transposing butterfly: 31 shuffles leave dot
+// product j on lane j, instead of 5 shuffles per dot product.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -61,97 +62,23 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
     return x[0];
 }
 
-template <int D, typename TIn, bool GATE>
+// One CTA per (sequence, value head).  The state comes from slot idx[n] of the pool (slot n when
+// idx is null), stays in registers for the T tokens, and is written back once.  Per token:
+//     x' = silu(conv(x)) for x in q, k, v        (optional short convolution)
+//     q, k normalised, q scaled;  qa = alpha . q, ka = alpha . k  (alpha per key channel or one
+//     value for the head; alpha s . k = s . (alpha k))
+//     sk_r = s_r . ka,  sq_r = s_r . qa,  delta_r = beta (v_r - sk_r)
+//     s_r <- alpha . s_r + delta_r k,     y_r = sq_r + delta_r (k . q)
+template <int D, typename TIn, bool GATE, bool CONV>
 __global__ void __launch_bounds__(D * 2) decode_kernel(DecodeArgs a) {
     constexpr int EPT = D / 32;
     static_assert(D / kRowsPerWarp * 32 == D * 2, "one warp per 16 rows");
-    __shared__ float ys[GATE ? D : 1];
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const long unit = blockIdx.x;  // n * H + h
-    const TIn* q = static_cast<const TIn*>(a.q) + unit * D;
-    const TIn* k = static_cast<const TIn*>(a.k) + unit * D;
-    const TIn* v = static_cast<const TIn*>(a.v) + unit * D;
-    const int r0 = warp * kRowsPerWarp;
-    float* S = a.state + unit * D * D + (long)r0 * D + lane * EPT;
-
-    // state rows first: they are the bytes that matter
-    float s[kRowsPerWarp][EPT];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::load(S + (long)i * D, s[i]);
-
-    float qv[EPT], kv[EPT];
-    load_vec<EPT>(q + lane * EPT, qv);
-    load_vec<EPT>(k + lane * EPT, kv);
-    const float vr = lane < kRowsPerWarp ? to_f32(v[r0 + lane]) : 0.0f;
-    const float alpha = expf(a.g[unit]);
-    const float beta = a.beta[unit];
-
-    float ssq = 0.f, ssk = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) { ssq += qv[e] * qv[e]; ssk += kv[e] * kv[e]; }
-    ssq = warp_sum(ssq);
-    ssk = warp_sum(ssk);
-    const float qf = a.use_l2 ? a.scale * rsqrtf(ssq + kL2Eps) : a.scale;
-    const float kf = a.use_l2 ? rsqrtf(ssk + kL2Eps) : 1.0f;
-    float kq = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) { qv[e] *= qf; kv[e] *= kf; kq += kv[e] * qv[e]; }
-    kq = warp_sum(kq);
-
-    float x[32];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-        float dk = 0.f, dq = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) { dk += s[i][e] * kv[e]; dq += s[i][e] * qv[e]; }
-        x[i] = dk;
-        x[kRowsPerWarp + i] = dq;
-    }
-    const float t = transpose_reduce32(x, lane);  // lane<16: s_r.k of row r0+lane; else s_r.q
-    const float delta = beta * (vr - alpha * t);   // meaningful on lanes < 16
-    const float dsh = __shfl_sync(0xffffffffu, delta, lane & (kRowsPerWarp - 1));
-    const float y = alpha * t + dsh * kq;          // meaningful on lanes >= 16
-
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-        const float di = __shfl_sync(0xffffffffu, delta, i);
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) s[i][e] = alpha * s[i][e] + di * kv[e];
-        StateVec<EPT>::store(S + (long)i * D, s[i]);
-    }
-
-    if constexpr (!GATE) {
-        if (lane >= kRowsPerWarp) store_out(a.out, unit * D + r0 + lane - kRowsPerWarp, a.out_dtype, y);
-    } else {
-        if (lane >= kRowsPerWarp) ys[r0 + lane - kRowsPerWarp] = y;
-        __syncthreads();
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) { float t2 = ys[lane * EPT + e]; ss += t2 * t2; }
-        ss = warp_sum(ss);
-        const float rinv = rsqrtf(ss / D + a.eps);
-        if (threadIdx.x < D) {
-            const int r = threadIdx.x;
-            const float z = a.z[unit * D + r];
-            const float w = a.w ? a.w[r] : 1.0f;
-            store_out(a.out, unit * D + r, a.out_dtype, w * ys[r] * rinv * z * sigmoidf_(z));
-        }
-    }
-}
-
-// T tokens per sequence on a state taken from a pool by index ("6.6 Gated DeltaNet" 6.6.8 applied T
-// times): the state rows stay in registers across the tokens and are written back once.  The
-// per-token arithmetic is the single-step kernel's.
-template <int D, typename TIn, bool GATE>
-__global__ void __launch_bounds__(D * 2) decode_multi_kernel(DecodeMultiArgs a) {
-    constexpr int EPT = D / 32;
     __shared__ float ys[GATE ? D : 1];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int unit = blockIdx.x;  // n * H + h
     const int n = unit / a.H, h = unit % a.H;
+    const int grp = a.H / a.Hk, hk = h / grp;   // value head h reads query/key head h / grp
     const int slot = a.idx ? a.idx[n] : n;
     if (slot < 0) return;                       // padding entry: nothing to do
     if (slot >= a.num_slots) {                  // checked before any state access
@@ -159,22 +86,71 @@ __global__ void __launch_bounds__(D * 2) decode_multi_kernel(DecodeMultiArgs a) 
         return;
     }
     const int r0 = warp * kRowsPerWarp;
+    const int vrow = r0 + (lane & (kRowsPerWarp - 1));
     float* S = a.state + ((long)slot * a.H + h) * D * D + (long)r0 * D + lane * EPT;
+
+    // state rows first: they are the bytes that matter
     float s[kRowsPerWarp][EPT];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::load(S + (long)i * D, s[i]);
 
+    // short convolution: taps and the three previous raw inputs of this lane's channels
+    const int cq = hk * D + lane * EPT, ck = a.Hk * D + cq, cv = 2 * a.Hk * D + h * D + vrow;
+    float4 wq[CONV ? EPT : 1], wk[CONV ? EPT : 1], wv;
+    float hq[CONV ? EPT : 1][3], hkk[CONV ? EPT : 1][3], hv[3];
+    if constexpr (CONV) {
+        const float4* w4 = reinterpret_cast<const float4*>(a.conv.w);
+        const float* si = a.conv.state_in ? a.conv.state_in + (long)slot * a.conv.dim * 3 : nullptr;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            wq[e] = __ldg(w4 + cq + e);
+            wk[e] = __ldg(w4 + ck + e);
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                hq[e][j] = si ? si[(long)(cq + e) * 3 + j] : 0.f;
+                hkk[e][j] = si ? si[(long)(ck + e) * 3 + j] : 0.f;
+            }
+        }
+        wv = __ldg(w4 + cv);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) hv[j] = si ? si[(long)cv * 3 + j] : 0.f;
+    }
+
     for (int t = 0; t < a.T; ++t) {
-        const long tok = ((long)n * a.T + t) * a.H + h;   // [N, T, H] token index
-        const TIn* q = static_cast<const TIn*>(a.q) + tok * D;
-        const TIn* k = static_cast<const TIn*>(a.k) + tok * D;
-        const TIn* v = static_cast<const TIn*>(a.v) + tok * D;
-        float qv[EPT], kv[EPT];
+        const long tok = (long)n * a.T + t;
+        const long vt = tok * a.H + h;          // [.., H] row of this value head
+        const long qt = tok * a.Hk + hk;        // [.., Hk] row of its query/key head
+        const TIn* q = static_cast<const TIn*>(a.q) + qt * D;
+        const TIn* k = static_cast<const TIn*>(a.k) + qt * D;
+        float qv[EPT], kv[EPT], alpha[EPT];
         load_vec<EPT>(q + lane * EPT, qv);
         load_vec<EPT>(k + lane * EPT, kv);
-        const float vr = lane < kRowsPerWarp ? to_f32(v[r0 + lane]) : 0.0f;
-        const float alpha = expf(a.g[tok]);
-        const float beta = a.beta[tok];
+        float vr = to_f32(static_cast<const TIn*>(a.v)[vt * D + vrow]);
+        if constexpr (CONV) {
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                const float xq = qv[e], xk = kv[e];
+                qv[e] = round_to<TIn>(conv4_silu(wq[e], hq[e][0], hq[e][1], hq[e][2], xq));
+                kv[e] = round_to<TIn>(conv4_silu(wk[e], hkk[e][0], hkk[e][1], hkk[e][2], xk));
+                hq[e][0] = hq[e][1]; hq[e][1] = hq[e][2]; hq[e][2] = xq;
+                hkk[e][0] = hkk[e][1]; hkk[e][1] = hkk[e][2]; hkk[e][2] = xk;
+            }
+            const float xv = vr;
+            vr = round_to<TIn>(conv4_silu(wv, hv[0], hv[1], hv[2], xv));
+            hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
+        }
+        if (a.g_per_channel) {
+            float gv[EPT];
+            load_vec<EPT>(a.g + vt * D + lane * EPT, gv);
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) alpha[e] = expf(gv[e]);
+        } else {
+            const float a0 = expf(a.g[vt]);
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) alpha[e] = a0;
+        }
+        const float beta = a.beta[vt];
+
         float ssq = 0.f, ssk = 0.f;
 #pragma unroll
         for (int e = 0; e < EPT; ++e) { ssq += qv[e] * qv[e]; ssk += kv[e] * kv[e]; }
@@ -182,33 +158,41 @@ __global__ void __launch_bounds__(D * 2) decode_multi_kernel(DecodeMultiArgs a) 
         ssk = warp_sum(ssk);
         const float qf = a.use_l2 ? a.scale * rsqrtf(ssq + kL2Eps) : a.scale;
         const float kf = a.use_l2 ? rsqrtf(ssk + kL2Eps) : 1.0f;
-        float kq = 0.f;
+        float kq = 0.f, qa[EPT], ka[EPT];
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) { qv[e] *= qf; kv[e] *= kf; kq += kv[e] * qv[e]; }
+        for (int e = 0; e < EPT; ++e) {
+            qv[e] *= qf;
+            kv[e] *= kf;
+            kq += kv[e] * qv[e];
+            qa[e] = alpha[e] * qv[e];
+            ka[e] = alpha[e] * kv[e];
+        }
         kq = warp_sum(kq);
+
         float x[32];
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
             float dk = 0.f, dq = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) { dk += s[i][e] * kv[e]; dq += s[i][e] * qv[e]; }
+            for (int e = 0; e < EPT; ++e) { dk += s[i][e] * ka[e]; dq += s[i][e] * qa[e]; }
             x[i] = dk;
             x[kRowsPerWarp + i] = dq;
         }
-        const float tt = transpose_reduce32(x, lane);
-        const float delta = beta * (vr - alpha * tt);
+        const float tt = transpose_reduce32(x, lane);  // lane < 16: s_r . ka of row r0 + lane; else s_r . qa
+        const float delta = beta * (vr - tt);           // meaningful on lanes < 16
         const float dsh = __shfl_sync(0xffffffffu, delta, lane & (kRowsPerWarp - 1));
-        const float y = alpha * tt + dsh * kq;
+        const float y = tt + dsh * kq;                  // meaningful on lanes >= 16
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
             const float di = __shfl_sync(0xffffffffu, delta, i);
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) s[i][e] = alpha * s[i][e] + di * kv[e];
+            for (int e = 0; e < EPT; ++e) s[i][e] = alpha[e] * s[i][e] + di * kv[e];
         }
+
         if constexpr (!GATE) {
-            if (lane >= kRowsPerWarp) store_out(a.out, tok * D + r0 + lane - kRowsPerWarp, a.out_dtype, y);
+            if (lane >= kRowsPerWarp) store_out(a.out, vt * D + vrow, a.out_dtype, y);
         } else {
-            if (lane >= kRowsPerWarp) ys[r0 + lane - kRowsPerWarp] = y;
+            if (lane >= kRowsPerWarp) ys[vrow] = y;
             __syncthreads();
             float ss = 0.f;
 #pragma unroll
@@ -217,40 +201,50 @@ __global__ void __launch_bounds__(D * 2) decode_multi_kernel(DecodeMultiArgs a) 
             const float rinv = rsqrtf(ss / D + a.eps);
             if (threadIdx.x < D) {
                 const int r = threadIdx.x;
-                const float z = a.z[tok * D + r];
+                const float z = a.z[vt * D + r];
                 const float w = a.w ? a.w[r] : 1.0f;
-                store_out(a.out, tok * D + r, a.out_dtype, w * ys[r] * rinv * z * sigmoidf_(z));
+                store_out(a.out, vt * D + r, a.out_dtype, w * ys[r] * rinv * z * sigmoidf_(z));
             }
             __syncthreads();  // ys is rewritten by the next token
         }
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::store(S + (long)i * D, s[i]);
-}
 
-template <int D, typename TIn>
-cudaError_t launch_multi_d(const DecodeMultiArgs& a, cudaStream_t s) {
-    dim3 grid((unsigned)((long)a.N * a.H)), block(D * 2);
-    if (a.z) decode_multi_kernel<D, TIn, true><<<grid, block, 0, s>>>(a);
-    else decode_multi_kernel<D, TIn, false><<<grid, block, 0, s>>>(a);
-    return cudaGetLastError();
+    if constexpr (CONV) {
+        if (a.conv.state_out) {
+            float* so = a.conv.state_out + (long)slot * a.conv.dim * 3;
+            __syncthreads();  // every warp has read its input history (the update may be in place)
+            if (warp == 0 && h % grp == 0) {  // one writer per query/key head
+#pragma unroll
+                for (int e = 0; e < EPT; ++e)
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) {
+                        so[(long)(cq + e) * 3 + j] = hq[e][j];
+                        so[(long)(ck + e) * 3 + j] = hkk[e][j];
+                    }
+            }
+            if (lane < kRowsPerWarp)
+#pragma unroll
+                for (int j = 0; j < 3; ++j) so[(long)cv * 3 + j] = hv[j];
+        }
+    }
 }
 
 template <int D, typename TIn>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)((long)a.N * a.H)), block(D * 2);
-    if (a.z) decode_kernel<D, TIn, true><<<grid, block, 0, s>>>(a);
-    else decode_kernel<D, TIn, false><<<grid, block, 0, s>>>(a);
+    if (a.conv.w) {
+        if (a.z) decode_kernel<D, TIn, true, true><<<grid, block, 0, s>>>(a);
+        else decode_kernel<D, TIn, false, true><<<grid, block, 0, s>>>(a);
+    } else {
+        if (a.z) decode_kernel<D, TIn, true, false><<<grid, block, 0, s>>>(a);
+        else decode_kernel<D, TIn, false, false><<<grid, block, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
 }  // namespace
-
-cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t s) {
-    if (a.d == 128)
-        return a.qkv_dtype == GDN_BF16 ? launch_multi_d<128, __nv_bfloat16>(a, s) : launch_multi_d<128, float>(a, s);
-    return a.qkv_dtype == GDN_BF16 ? launch_multi_d<64, __nv_bfloat16>(a, s) : launch_multi_d<64, float>(a, s);
-}
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     if (a.d == 128) return a.qkv_dtype == GDN_BF16 ? launch_d<128, __nv_bfloat16>(a, s) : launch_d<128, float>(a, s);

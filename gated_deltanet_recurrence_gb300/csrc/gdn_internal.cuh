@@ -63,6 +63,19 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// A value rounded to the element type T (the convolution output is an activation of the q/k/v
+// type: rounded once, after the SiLU, before the core uses it).
+template <typename T>
+__device__ __forceinline__ float round_to(float x) { return x; }
+template <>
+__device__ __forceinline__ float round_to<__nv_bfloat16>(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Short convolution of one channel: taps w[0..3] over (h0, h1, h2, x), oldest first, then SiLU.
+__device__ __forceinline__ float conv4_silu(float4 w, float h0, float h1, float h2, float x) {
+    const float c = fmaf(w.w, x, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
+    return c * sigmoidf_(c);
+}
+
 // Record a device-side status in the library's error word (first writer wins).
 __device__ __forceinline__ void record_error(int* err, int status) {
     if (err) atomicCAS(err, 0, status);
@@ -70,20 +83,23 @@ __device__ __forceinline__ void record_error(int* err, int status) {
 
 // ---- launchers (one translation unit each; called from abi.cu after argument checks) --------
 
+// The fused short convolution ("因果卷积"): weight [dim, 4]; states [rows, dim, 3], oldest first.
+struct ConvArgs {
+    const float* w;         // null: no convolution
+    const float* state_in;  // null: zero history
+    float* state_out;       // null: not written
+    int dim;                // 2 * Hk * d + H * d
+};
+
+// One or more decode tokens per sequence; the single-token call is T = 1 with slot n for
+// sequence n.  q, k are [N, T, Hk, d]; v, z, out [N, T, H, d]; g [N, T, H] or [N, T, H, d].
 struct DecodeArgs {
     const void* q; const void* k; const void* v; const float* g; const float* beta;
-    float* state; int N, H, d; gdn_dtype qkv_dtype; float scale; int use_l2;
-    const float* z; const float* w; float eps; void* out; gdn_dtype out_dtype;
+    float* state; int num_slots; const int32_t* idx; int N, T, H, Hk, d; gdn_dtype qkv_dtype;
+    int g_per_channel; float scale; int use_l2; ConvArgs conv;
+    const float* z; const float* w; float eps; void* out; gdn_dtype out_dtype; int* err;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-
-struct DecodeMultiArgs {
-    const void* q; const void* k; const void* v; const float* g; const float* beta;
-    float* state; int num_slots; const int32_t* idx; int N, T, H, d; gdn_dtype qkv_dtype;
-    float scale; int use_l2; const float* z; const float* w; float eps; void* out; gdn_dtype out_dtype;
-    int* err;
-};
-cudaError_t launch_decode_multi(const DecodeMultiArgs& a, cudaStream_t s);
 
 struct GateArgs {
     const void* y; gdn_dtype y_dtype; const float* z; const float* w; float eps;
@@ -99,12 +115,16 @@ cudaError_t launch_gate_prep(const GatePrepArgs& a, cudaStream_t s);
 
 struct PrefillArgs {
     const void* q; const void* k; const void* v; const float* g; const float* beta;
-    const int32_t* cu_seqlens; int num_seqs, total_T, H, d; gdn_dtype qkv_dtype;
-    float scale; int use_l2; const float* initial_state; float* final_state;
+    const int32_t* cu_seqlens; int num_seqs, total_T, H, Hk, d; gdn_dtype qkv_dtype;
+    int g_per_channel; float scale; int use_l2; ConvArgs conv;
+    const float* initial_state; float* final_state;
     const float* z; const float* w; float eps; void* out; gdn_dtype out_dtype;
     void* workspace; size_t workspace_bytes; int* err;
 };
 cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t s);
+
+// Final short-convolution state of every sequence (after the prefill kernels, same stream).
+cudaError_t launch_conv_state(const PrefillArgs& a, cudaStream_t s);
 
 // tensor-core prefill (bf16 q/k/v, d_k = d_v = 128): workspace size, availability, launch
 size_t prefill_tc_workspace_bytes(int num_seqs, int total_T, int H);

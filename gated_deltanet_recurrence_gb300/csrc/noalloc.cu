@@ -49,8 +49,10 @@ void* scratch_ptr() {
 
 extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
                                      const float* beta, const int32_t* cu_seqlens, int num_seqs,
-                                     int total_T, int H, int d_k, int d_v, gdn_dtype qkv_dtype,
-                                     float scale, int use_qk_l2norm, const float* initial_state,
+                                     int total_T, int H, int H_k, int d_k, int d_v, gdn_dtype qkv_dtype,
+                                     gdn_decay decay, float scale, int use_qk_l2norm,
+                                     const float* conv_weight, const float* conv_state_in,
+                                     float* conv_state_out, const float* initial_state,
                                      float* final_state, const float* gate_z, const float* norm_weight,
                                      float norm_eps, void* out, gdn_dtype out_dtype, void* stream) {
     if (num_seqs <= 0 || total_T < 0 || H <= 0) return GDN_ERR_ARG;
@@ -61,7 +63,8 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
         ws = scratch_ptr();
         if (!ws) return GDN_ERR_CUDA;
     }
-    return gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, num_seqs, total_T, H, d_k, d_v, qkv_dtype, scale,
-                         use_qk_l2norm, initial_state, final_state, gate_z, norm_weight, norm_eps, out,
-                         out_dtype, ws, need > 0 ? (size_t)GDN_NOALLOC_SCRATCH_BYTES : 0, stream);
+    return gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, num_seqs, total_T, H, H_k, d_k, d_v, qkv_dtype,
+                         decay, scale, use_qk_l2norm, conv_weight, conv_state_in, conv_state_out,
+                         initial_state, final_state, gate_z, norm_weight, norm_eps, out, out_dtype, ws,
+                         need > 0 ? (size_t)GDN_NOALLOC_SCRATCH_BYTES : 0, stream);
 }

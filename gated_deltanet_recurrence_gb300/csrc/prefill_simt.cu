@@ -19,6 +19,19 @@
 //
 // This path keeps every product in fp32 (it is the one used for fp32 inputs, where the required
 // accuracy is a relative L2 error of 1e-4); bf16 inputs are upcast exactly on load.
+//
+// Options handled here:
+//   - grouped query/key heads: value head h reads query/key head h / (H / Hk);
+//   - the short convolution ("因果卷积"): each loaded element is silu(w . (x_{t-3}, .., x_t)),
+//     rounded once to the input element type, the history taken from the sequence itself or,
+//     before its first token, from the input state;
+//   - a decay per key channel ("6.6 Gated DeltaNet" 6.6.7), template PC: gc becomes a C x d_k
+//     tile (per-channel inclusive sums), and the decays enter per element:
+//       A_ij  = beta_i sum_x k_ix k_jx e^(gc_ix - gc_jx),   (Q K^T * D)_ij likewise,
+//       W     = T diag(beta) (K . e^gc),   O_inter = (Q . e^gc) S^T,
+//       S    <- S diag(e^gc_last) + V_new^T (K . e^(gc_last - gc)),
+//     where "." scales each column x by its own factor.  Every exponent used is <= 0 (the clamp
+//     only touches entries above the diagonal, which are masked), so nothing overflows.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -37,11 +50,31 @@ struct SimtLayout {
     static constexpr int oQ = 0, oK = kTile, oW = 2 * kTile, oU = 3 * kTile, oVN = 4 * kTile;
     static constexpr int oT = 5 * kTile, oAq = oT + kSq;
     static constexpr int oG = oAq + kSq;  // gc, e^gc, e^(glast-gc), beta
-    static constexpr int kWords = oG + 4 * kC;
+    static constexpr int oEL = oG + 4 * kC;  // per-channel e^(gc_last) (decay per key channel)
+    static constexpr int kWords = oEL + D;
     static constexpr size_t kBytes = sizeof(float) * kWords;
 };
 
-template <int D, typename TIn>
+// One raw element of q, k or v at token t (absolute index) and column x, or the carried
+// convolution history when t is before the sequence start bos.
+template <typename TIn>
+__device__ __forceinline__ float conv_tap(const TIn* base, long stride, long t, long bos, int x,
+                                          const float* hist, int c) {
+    if (t >= bos) return to_f32(base[t * stride + x]);
+    return hist ? hist[(long)c * 3 + 3 + (t - bos)] : 0.f;
+}
+
+template <typename TIn>
+__device__ __forceinline__ float load_conv(const TIn* base, long stride, long t, long bos, int x,
+                                           const float* w, const float* hist, int c) {
+    const float4 wc = *reinterpret_cast<const float4*>(w + (long)c * 4);
+    return round_to<TIn>(conv4_silu(wc, conv_tap(base, stride, t - 3, bos, x, hist, c),
+                                    conv_tap(base, stride, t - 2, bos, x, hist, c),
+                                    conv_tap(base, stride, t - 1, bos, x, hist, c),
+                                    to_f32(base[t * stride + x])));
+}
+
+template <int D, typename TIn, bool PC>
 __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a) {
     using Lay = SimtLayout<D>;
     constexpr int LD = Lay::LD, LC = Lay::LC;
@@ -62,6 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
     float* egc = gcs + kC;
     float* ekl = gcs + 2 * kC;
     float* bts = gcs + 3 * kC;
+    float* elast = sm + Lay::oEL;
+    float* G = Ws;  // per-channel gc (PC only), alive until the W step overwrites it
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x;
@@ -79,10 +114,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
         bos = (long)n * T;
         eos = bos + T;
     }
-    const long tok_stride = (long)a.H * D;   // elements between consecutive tokens
-    const TIn* qg = static_cast<const TIn*>(a.q) + (long)h * D;
-    const TIn* kg = static_cast<const TIn*>(a.k) + (long)h * D;
+    const long tok_stride = (long)a.H * D;   // elements between consecutive tokens of v, z, out
+    const long qk_stride = (long)a.Hk * D;   // ... of q and k
+    const int hk = h / (a.H / a.Hk);
+    const TIn* qg = static_cast<const TIn*>(a.q) + (long)hk * D;
+    const TIn* kg = static_cast<const TIn*>(a.k) + (long)hk * D;
     const TIn* vg = static_cast<const TIn*>(a.v) + (long)h * D;
+    const float* chist = a.conv.state_in ? a.conv.state_in + (long)n * a.conv.dim * 3 : nullptr;
+    const int cq0 = hk * D, ck0 = a.Hk * D + hk * D, cv0 = 2 * a.Hk * D + h * D;
 
     // state row r, columns x_e = p + TPR * e
     const int r = tid / TPR, p = tid % TPR;
@@ -100,10 +139,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
             const int i = idx / D, x = idx % D;
             float qv = 0.f, kv = 0.f, vv = 0.f;
             if (i < L) {
-                const long off = (c0 + i) * tok_stride + x;
-                qv = to_f32(qg[off]);
-                kv = to_f32(kg[off]);
-                vv = to_f32(vg[off]);
+                const long t = c0 + i;
+                if (a.conv.w) {
+                    qv = load_conv(qg, qk_stride, t, bos, x, a.conv.w, chist, cq0 + x);
+                    kv = load_conv(kg, qk_stride, t, bos, x, a.conv.w, chist, ck0 + x);
+                    vv = load_conv(vg, tok_stride, t, bos, x, a.conv.w, chist, cv0 + x);
+                } else {
+                    qv = to_f32(qg[t * qk_stride + x]);
+                    kv = to_f32(kg[t * qk_stride + x]);
+                    vv = to_f32(vg[t * tok_stride + x]);
+                }
             }
             Qs[i * LD + x] = qv;
             Ks[i * LD + x] = kv;
@@ -111,8 +156,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
         }
         if (tid < kC) {
             const bool in = tid < L;
-            gcs[tid] = in ? a.g[(c0 + tid) * a.H + h] : 0.f;
+            gcs[tid] = (in && !PC) ? a.g[(c0 + tid) * a.H + h] : 0.f;
             bts[tid] = in ? a.beta[(c0 + tid) * a.H + h] : 0.f;
+        }
+        if constexpr (PC) {  // per-channel inclusive sums down the chunk, one column per thread
+            for (int x = tid; x < D; x += kThreads) {
+                const float* gx = a.g + (c0 * a.H + h) * (long)D + x;
+                float acc = 0.f;
+                for (int i = 0; i < kC; ++i) {
+                    acc += i < L ? gx[(long)i * a.H * D] : 0.f;
+                    G[i * LD + x] = acc;
+                }
+                elast[x] = expf(acc);
+            }
         }
         __syncthreads();
 
@@ -160,18 +216,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
             for (int m = 0; m < 16; ++m) { kk[m] = 0.f; qk[m] = 0.f; }
             for (int x = 0; x < D; ++x) {
                 const float ki = Ks[i * LD + x], qi = Qs[i * LD + x];
+                if constexpr (PC) {
+                    const float gix = G[i * LD + x];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float kj = Ks[(jp + 4 * m) * LD + x];
-                    kk[m] += ki * kj;
-                    qk[m] += qi * kj;
+                    for (int m = 0; m < 16; ++m) {
+                        const int j = jp + 4 * m;
+                        const float kj = Ks[j * LD + x] * __expf(fminf(gix - G[j * LD + x], 0.f));
+                        kk[m] += ki * kj;
+                        qk[m] += qi * kj;
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const float kj = Ks[(jp + 4 * m) * LD + x];
+                        kk[m] += ki * kj;
+                        qk[m] += qi * kj;
+                    }
                 }
             }
             const float gi = gcs[i], bi = bts[i];
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int j = jp + 4 * m;
-                const float dec = j <= i ? expf(gi - gcs[j]) : 0.f;
+                const float dec = j <= i ? (PC ? 1.f : expf(gi - gcs[j])) : 0.f;
                 VN[i * LC + j] = j < i ? bi * kk[m] * dec : 0.f;
                 Aq[i * LC + j] = qk[m] * dec;
                 Ts[i * LC + j] = i == j ? 1.f : 0.f;
@@ -198,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
 #pragma unroll
             for (int u = 0; u < RPG; ++u) { wacc[u] = 0.f; uacc[u] = 0.f; }
             for (int j = 0; j < kC; ++j) {
-                const float kb = bts[j] * egc[j] * Ks[j * LD + x];
+                const float kb = bts[j] * (PC ? __expf(G[j * LD + x]) : egc[j]) * Ks[j * LD + x];
                 const float vb = bts[j] * Us[j * LD + x];
 #pragma unroll
                 for (int u = 0; u < RPG; ++u) {
@@ -208,6 +275,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
                 }
             }
             __syncthreads();
+            if constexpr (PC) {
+                // fold the per-channel decays into Q (output) and K (state update) before G,
+                // which lives in the W tile, is overwritten
+                for (int idx = tid; idx < kC * D; idx += kThreads) {
+                    const int i = idx / D, xx = idx % D;
+                    const float gc = G[i * LD + xx], gl = G[(kC - 1) * LD + xx];
+                    Qs[i * LD + xx] *= __expf(gc);
+                    Ks[i * LD + xx] *= __expf(gl - gc);
+                }
+                __syncthreads();
+            }
 #pragma unroll
             for (int u = 0; u < RPG; ++u) {
                 Ws[(rg * RPG + u) * LD + x] = wacc[u];
@@ -232,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
 #pragma unroll
             for (int e = 0; e < EPT; ++e) inter += Qs[i * LD + p + TPR * e] * S[e];
             for (int j = p; j <= i; j += TPR) intra += Aq[i * LC + j] * VN[j * LD + r];
-            float o = egc[i] * inter + intra;
+            float o = (PC ? 1.f : egc[i]) * inter + intra;
 #pragma unroll
             for (int s = 1; s < TPR; s <<= 1) o += __shfl_xor_sync(0xffffffffu, o, s);
             if (p == 0) Us[i * LD + r] = o;
@@ -241,9 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
         {
             const float gamma = expf(gcs[kC - 1]);
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) S[e] *= gamma;
+            for (int e = 0; e < EPT; ++e) S[e] *= PC ? elast[p + TPR * e] : gamma;
             for (int j = 0; j < L; ++j) {
-                const float vj = VN[j * LD + r] * ekl[j];
+                const float vj = VN[j * LD + r] * (PC ? 1.f : ekl[j]);
 #pragma unroll
                 for (int e = 0; e < EPT; ++e) S[e] += vj * Ks[j * LD + p + TPR * e];
             }
@@ -280,15 +358,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(PrefillArgs a
     }
 }
 
-template <int D, typename TIn>
-cudaError_t launch_simt_d(const PrefillArgs& a, cudaStream_t s) {
+template <int D, typename TIn, bool PC>
+cudaError_t launch_simt_pc(const PrefillArgs& a, cudaStream_t s) {
     const size_t smem = SimtLayout<D>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, TIn>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<D, TIn, PC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((long)a.num_seqs * a.H);
-    prefill_simt_kernel<D, TIn><<<grid, kThreads, smem, s>>>(a);
+    prefill_simt_kernel<D, TIn, PC><<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+template <int D, typename TIn>
+cudaError_t launch_simt_d(const PrefillArgs& a, cudaStream_t s) {
+    return a.g_per_channel ? launch_simt_pc<D, TIn, true>(a, s) : launch_simt_pc<D, TIn, false>(a, s);
 }
 
 }  // namespace

@@ -76,7 +76,11 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
 
 struct TcArgs {
     const int32_t* cu;   // may be null: fixed length
-    int num_seqs, total_T, H;
+    int num_seqs, total_T, H, Hk;
+    const __nv_bfloat16* q;  // raw q, k [total_T, Hk, 128] and v [total_T, H, 128]: convolution history
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    ConvArgs conv;
     const float* g;
     const float* beta;
     float scale;
@@ -184,6 +188,28 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
     p.z = pack_bf16x2(v[4], v[5]);
     p.w = pack_bf16x2(v[6], v[7]);
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, chunk * 8)) = p;
+}
+
+// Short convolution + SiLU ("因果卷积") of one channel of a loaded 128B-swizzled operand tile, in
+// place, rows 0..L-1 of the chunk starting at token t0.  The three inputs before t0 come from the
+// sequence (t >= bos) or from the carried state.  `src` points at the channel's column of the raw
+// tensor (row stride `stride` elements); c is the channel's index in the mixed q|k|v layout.
+__device__ __forceinline__ void conv_column(uint8_t* tile, int col, const __nv_bfloat16* src, long stride,
+                                            const TcArgs& a, int n, int c, long bos, long t0, int L) {
+    const float4 w = __ldg(reinterpret_cast<const float4*>(a.conv.w) + c);
+    const float* hist = a.conv.state_in ? a.conv.state_in + ((long)n * a.conv.dim + c) * 3 : nullptr;
+    float hq[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const long t = t0 - 3 + j;
+        hq[j] = t >= bos ? __bfloat162float(src[t * stride]) : (hist ? hist[3 + (t - bos)] : 0.f);
+    }
+    for (int i = 0; i < L; ++i) {
+        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(tile + sw128_offset(i, col));
+        const float x = __bfloat162float(*e);
+        *e = __float2bfloat16_rn(conv4_silu(w, hq[0], hq[1], hq[2], x));
+        hq[0] = hq[1]; hq[1] = hq[2]; hq[2] = x;
+    }
 }
 
 __device__ __forceinline__ void ld_sw128_chunk(const uint8_t* tile, int row, int chunk, float* v) {
@@ -310,6 +336,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long gh = blockIdx.x;  // chunk * H + head
     const int chunk = (int)(gh / a.H), h = (int)(gh % a.H);
+    const int hk = h / (a.H / a.Hk);  // query/key head read by value head h
     if (chunk >= a.n_chunks[0]) return;
     const int n = a.chunk_seq[chunk];
     long bos, eos;
@@ -341,8 +368,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     if (tid == 0) {
         mbar_arrive_expect_tx(&bars[0], 49152);
         for (int c = 0; c < 2; ++c) {
-            tma_load_3d(sm + oKQ + c * 16384, &mK, &bars[0], c * 64, h, (int)t0);
-            tma_load_3d(sm + oKQ + c * 16384 + 8192, &mQ, &bars[0], c * 64, h, (int)t0);
+            tma_load_3d(sm + oKQ + c * 16384, &mK, &bars[0], c * 64, hk, (int)t0);
+            tma_load_3d(sm + oKQ + c * 16384 + 8192, &mQ, &bars[0], c * 64, hk, (int)t0);
             tma_load_3d(sm + oV + c * 8192, &mV, &bars[0], c * 64, h, (int)t0);
         }
     }
@@ -359,6 +386,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         gcs[2 * lane + 1] = s;
     }
     bool ok = mbar_wait(&bars[0], 0, kPolls);
+    if (ok && a.conv.w) {  // fused short convolution of the loaded rows: thread = channel
+        const int x = tid, half = x >> 6, col = x & 63;
+        const long qks = (long)a.Hk * kD, vs = (long)a.H * kD;
+        const int cq = hk * kD + x;
+        conv_column(sm + oKQ + half * 16384 + 8192, col, a.q + hk * kD + x, qks, a, n, cq, bos, t0, L);
+        conv_column(sm + oKQ + half * 16384, col, a.k + hk * kD + x, qks, a, n, a.Hk * kD + cq, bos, t0, L);
+        conv_column(sm + oV + half * 8192, col, a.v + (long)h * kD + x, vs, a, n, 2 * a.Hk * kD + h * kD + x,
+                    bos, t0, L);
+    }
     if (ok && L < kC) {  // rows past the end of the sequence hold other tokens: zero them
         for (int e = tid; e < (kC - L) * 8 * 5; e += kThreads) {
             const int r = L + e / 40, part = e % 40;  // 5 tiles x 8 chunks of 16 B
@@ -372,8 +408,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 *reinterpret_cast<uint4*>(base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
             }
         }
-        fence_async_smem();
     }
+    if (ok && (a.conv.w || L < kC)) fence_async_smem();  // generic writes, read next by the MMA
     __syncthreads();
     if (!ok) {
         if (tid == 0) record_error(a.err, GDN_ERR_TIMEOUT);
@@ -1025,7 +1061,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     const WsLayout L = ws_layout(p.num_seqs, p.total_T, p.H);
     uint8_t* ws = static_cast<uint8_t*>(p.workspace);
     TcArgs a{};
-    a.cu = p.cu_seqlens; a.num_seqs = p.num_seqs; a.total_T = p.total_T; a.H = p.H;
+    a.cu = p.cu_seqlens; a.num_seqs = p.num_seqs; a.total_T = p.total_T; a.H = p.H; a.Hk = p.Hk;
+    a.q = static_cast<const __nv_bfloat16*>(p.q);
+    a.k = static_cast<const __nv_bfloat16*>(p.k);
+    a.v = static_cast<const __nv_bfloat16*>(p.v);
+    a.conv = p.conv;
     a.g = p.g; a.beta = p.beta; a.scale = p.scale; a.use_l2 = p.use_l2;
     a.chunk_seq = reinterpret_cast<int32_t*>(ws + L.off_map);
     a.chunk_first = reinterpret_cast<int32_t*>(ws + L.off_first);
@@ -1040,7 +1080,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.z = p.z; a.w = p.w; a.eps = p.eps; a.out = p.out; a.out_dtype = p.out_dtype; a.err = p.err;
 
     CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ;
-    if (!map_tokens(&mQ, p.q, p.total_T, p.H) || !map_tokens(&mK, p.k, p.total_T, p.H) ||
+    if (!map_tokens(&mQ, p.q, p.total_T, p.Hk) || !map_tokens(&mK, p.k, p.total_T, p.Hk) ||
         !map_tokens(&mV, p.v, p.total_T, p.H) || !map_rows(&mW, a.W, L.nch * kC, kD, 64) ||
         !map_rows(&mAqk, a.Aqk, L.nch * kC, kC, 64) || !map_rows(&mQt, a.Qt, L.nch * kC, kD, 64) ||
         !map_rows(&mKt, a.Kt, L.nch * kC, kD, 64))

@@ -12,10 +12,17 @@ Workloads (named by what they are):
   varlen   64 packed sequences with lengths uniform in [128, 8192], H=16, d=128, bf16;
            initial states ~ N(0, 0.02^2) per sequence; final states written.
   long     B=1, H=32, T=131072, d=128, bf16; a ~ N(-4, 1) (alpha close to 1); fused gate.
+  prefill_gva   the prefill workload with 4 query/key heads shared by the 16 value heads.
+  prefill_kda   the prefill workload with one decay per key channel (a drawn per channel).
+  prefill_conv  the prefill workload with the short convolution fused (raw q, k, v drawn; taps
+                per channel ~ U(-1/2, 1/2), the default uniform bound 1/sqrt(fan_in) of a
+                depthwise kernel of 4 taps; zero history, i.e. sequences that start here).
 Distributions common to all: q, k, v ~ N(0, 1); a ~ N(-1, 1) unless stated; A = exp(A_log) with
 A_log ~ U[0, ln 8] per head; b ~ N(0, 1) (beta = sigmoid(b)); z ~ N(0, 1).
+Options (any workload): Hk (query/key heads, default H), per_channel (a drawn [T, H, d] so that
+g = -exp(A_log) softplus(a) is per key channel), conv (taps drawn), conv_state (history ~ N(0, 1)).
 Draw order from one torch.Generator seeded with the workload's seed: lengths (varlen only),
-q, k, v, a, A_log, b, z (if gated), initial state (if any).
+q, k, v, a, A_log, b, z (if gated), initial state (if any), conv taps, conv history (if any).
 """
 from __future__ import annotations
 
@@ -34,7 +41,18 @@ WORKLOADS = {
                    dtype=torch.bfloat16, a_mean=-1.0, gate=False, init_state=True, state_std=0.02),
     "long": dict(kind="prefill", seed=4, num_seqs=1, T=131072, H=32, d=128, dtype=torch.bfloat16,
                  a_mean=-4.0, gate=True, init_state=False),
+    "prefill_gva": dict(kind="prefill", seed=5, num_seqs=2, T=4096, H=16, Hk=4, d=128,
+                        dtype=torch.bfloat16, a_mean=-1.0, gate=True, init_state=False),
+    "prefill_kda": dict(kind="prefill", seed=6, num_seqs=2, T=4096, H=16, d=128, dtype=torch.bfloat16,
+                        a_mean=-1.0, gate=True, init_state=False, per_channel=True),
+    "prefill_conv": dict(kind="prefill", seed=7, num_seqs=2, T=4096, H=16, d=128, dtype=torch.bfloat16,
+                         a_mean=-1.0, gate=True, init_state=False, conv=True),
 }
+
+
+def conv_dim(H, Hk, d):
+    """Channels of the mixed q|k|v projection the short convolution runs over."""
+    return 2 * Hk * d + H * d
 
 
 def workload(name: str, **overrides) -> dict:
@@ -73,14 +91,18 @@ def prefill_inputs(cfg, device="cpu", seed=None) -> dict:
     def randn(*shape):
         return torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
 
-    q = randn(total_T, H, d).to(dt)
-    k = randn(total_T, H, d).to(dt)
+    Hk = cfg.get("Hk", H)
+    q = randn(total_T, Hk, d).to(dt)
+    k = randn(total_T, Hk, d).to(dt)
     v = randn(total_T, H, d).to(dt)
-    a = randn(total_T, H) + cfg["a_mean"]
+    a = (randn(total_T, H, d) if cfg.get("per_channel") else randn(total_T, H)) + cfg["a_mean"]
     A_log = torch.rand(H, generator=gen, device=device, dtype=torch.float32) * math.log(8.0)
     b = randn(total_T, H)
     z = randn(total_T, H, d) if cfg.get("gate") else None
     S0 = randn(n, H, d, d) * cfg.get("state_std", 0.02) if cfg.get("init_state") else None
+    C = conv_dim(H, Hk, d)
+    conv_w = (torch.rand(C, 4, generator=gen, device=device) - 0.5) if cfg.get("conv") else None
+    conv_s = randn(n, C, 3) if cfg.get("conv_state") else None
     cu = None
     if varlen:
         offs = [0]
@@ -88,7 +110,8 @@ def prefill_inputs(cfg, device="cpu", seed=None) -> dict:
             offs.append(offs[-1] + L)
         cu = torch.tensor(offs, dtype=torch.int32, device=device)
     return dict(q=q, k=k, v=v, a=a, A_log=A_log, b=b, z=z, initial_state=S0, cu_seqlens=cu,
-                num_seqs=n, lengths=lengths, total_T=total_T, cfg=cfg)
+                num_seqs=n, lengths=lengths, total_T=total_T, conv_weight=conv_w, conv_state=conv_s,
+                cfg=cfg)
 
 
 def decode_inputs(cfg, device="cpu", seed=None) -> dict:

@@ -10,6 +10,12 @@
  *   q and k are L2-normalised (x / sqrt(sum x^2 + 1e-6)) and q is scaled by 1/sqrt(d_k).
  *   "5. 线性注意力", "门控 RMSNorm": o = w * RMSNorm(y) * SiLU(z).
  *   "5. 线性注意力", "Delta Rule 的 Chunk 实现": the chunked form used for prefill.
+ *   "5. 线性注意力", "因果卷积(Causal Conv1d)": q, k, v come out of a causal depthwise
+ *   convolution (kernel 4, no bias) followed by SiLU; the optional conv_* arguments fuse it.
+ *   "5. 线性注意力", forward code: with fewer query/key heads than value heads, each query/key
+ *   head serves H / H_k consecutive value heads (repeat_interleave along the head axis).
+ *   "6.6 Gated DeltaNet", 6.6.7: a decay per feature channel instead of one per head (read here
+ *   as one per key channel: S <- S diag(alpha_t)).
  *
  * Conventions for every call
  *   - All tensor pointers are DEVICE pointers owned by the caller, row-major and contiguous,
@@ -20,9 +26,20 @@
  *     the host before anything is launched.  Errors that only the device can see (a malformed
  *     cu_seqlens array) are recorded in a device error word: the kernels then write nothing
  *     for the affected sequence, and gdn_get_device_error() reports and clears the word.
- *   - Token tensors are packed: q, k [total_T, H, d_k]; v, out [total_T, H, d_v];
- *     gates g, beta [total_T, H] fp32; states [num_seqs, H, d_v, d_k] fp32 (d_k contiguous,
- *     the orientation of "[LLM Algorithms-2] Gated DeltaNet" section 1: y = S q).
+ *   - Token tensors are packed: q, k [total_T, H_k, d_k]; v, out [total_T, H, d_v] with H a
+ *     multiple of H_k (value head h uses query/key head h / (H / H_k)); gates beta [total_T, H]
+ *     fp32 and g [total_T, H] fp32, or g [total_T, H, d_k] with GDN_DECAY_PER_KEY_CHANNEL;
+ *     states [num_seqs, H, d_v, d_k] fp32 (d_k contiguous, the orientation of
+ *     "[LLM Algorithms-2] Gated DeltaNet" section 1: y = S q).
+ *   - Short convolution (optional; conv_weight NULL leaves q, k, v as given).  Its channels are
+ *     those of the page's mixed projection in order: the H_k * d_k query channels, the H_k * d_k
+ *     key channels, then the H * d_v value channels; conv_dim = 2 H_k d_k + H d_v.
+ *       conv_weight  [conv_dim, GDN_CONV_KERNEL] fp32; tap GDN_CONV_KERNEL - 1 multiplies the
+ *                    current token:  x'_t = silu(sum_j w[c][j] x_{t - 3 + j}).
+ *       conv state   [sequences, conv_dim, GDN_CONV_KERNEL - 1] fp32: the last three raw inputs
+ *                    of each channel, oldest first.  A NULL input state means zeros (the page's
+ *                    left padding, i.e. the start of a sequence).
+ *     The q/k normalisation and everything after it act on the convolved values.
  *   - Supported head sizes: d_k = d_v in {64, 128}.  Other sizes return GDN_ERR_UNSUPPORTED.
  */
 #ifndef GDN_H_
@@ -37,6 +54,12 @@ extern "C" {
 
 /* Element type of q, k, v and of outputs.  Gates, states and the gate input z are fp32. */
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Shape of the decay g: one log-decay per (token, head), or one per (token, head, key channel). */
+typedef enum { GDN_DECAY_PER_HEAD = 0, GDN_DECAY_PER_KEY_CHANNEL = 1 } gdn_decay;
+
+/* Taps of the short convolution ("因果卷积": kernel_size = 4). */
+#define GDN_CONV_KERNEL 4
 
 typedef enum {
     GDN_OK = 0,
@@ -55,15 +78,23 @@ typedef enum {
  * Source: "5. 线性注意力", "Delta Rule 的 Chunk 实现" (stages 1-3) for the algorithm, and
  * "[LLM Algorithms-2] Gated DeltaNet" sections 4-5 for the result it must equal.
  *
- *   q, k          [total_T, H, d_k], qkv_dtype.  Raw; normalised in-kernel when use_qk_l2norm.
+ *   q, k          [total_T, H_k, d_k], qkv_dtype.  Raw; normalised in-kernel when use_qk_l2norm.
  *   v             [total_T, H, d_v], qkv_dtype.
- *   g             [total_T, H] fp32, log-decay (g = log alpha <= 0; see gdn_decay_from_logits).
+ *   g             log-decay (g = log alpha <= 0; see gdn_decay_from_logits), fp32:
+ *                 [total_T, H] with GDN_DECAY_PER_HEAD, [total_T, H, d_k] with
+ *                 GDN_DECAY_PER_KEY_CHANNEL.
  *   beta          [total_T, H] fp32, update strength in [0, 1].
+ *   H, H_k        value heads and query/key heads; H_k >= 1 divides H.
  *   cu_seqlens    device int32 [num_seqs + 1], prefix sums of sequence lengths starting at 0
  *                 and ending at total_T; NULL means num_seqs sequences of total_T / num_seqs
  *                 tokens (total_T must then be a multiple of num_seqs).  Chunks never cross a
  *                 sequence boundary; a shorter last chunk is masked.  Empty sequences are allowed.
  *   scale         multiplies q after normalisation; scale <= 0 selects 1/sqrt(d_k).
+ *   conv_weight, conv_state_in, conv_state_out
+ *                 the fused short convolution (see the conventions above), or NULL.  The
+ *                 states are [num_seqs, conv_dim, 3]; conv_state_out receives each sequence's
+ *                 last three raw inputs (older ones from conv_state_in when the sequence is
+ *                 shorter than three tokens) and may alias conv_state_in.
  *   initial_state [num_seqs, H, d_v, d_k] fp32, or NULL for zeros.
  *   final_state   [num_seqs, H, d_v, d_k] fp32, or NULL (not written).  May alias
  *                 initial_state (each sequence's state is read before it is written).
@@ -75,14 +106,16 @@ typedef enum {
  *                 aligned; may be NULL when that size is 0.
  */
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int d_k, int d_v,
-                  gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
-                  const float* initial_state, float* final_state,
+                  const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int H_k,
+                  int d_k, int d_v, gdn_dtype qkv_dtype, gdn_decay decay, float scale,
+                  int use_qk_l2norm, const float* conv_weight, const float* conv_state_in,
+                  float* conv_state_out, const float* initial_state, float* final_state,
                   const float* gate_z, const float* norm_weight, float norm_eps,
                   void* out, gdn_dtype out_dtype,
                   void* workspace, size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace gdn_chunk_fwd needs for these sizes (0 when it needs none). */
+/* Bytes of workspace gdn_chunk_fwd needs for these sizes (0 when it needs none); enough for every
+ * choice of the arguments not listed (H_k, decay, convolution, gate). */
 size_t gdn_chunk_fwd_workspace_size(int num_seqs, int total_T, int H, int d_k, int d_v,
                                     gdn_dtype qkv_dtype);
 
@@ -91,14 +124,20 @@ size_t gdn_chunk_fwd_workspace_size(int num_seqs, int total_T, int H, int d_k, i
  * Source: "6.6 Gated DeltaNet", 6.6.8 (decode keeps only S); the update of
  * "[LLM Algorithms-2] Gated DeltaNet" section 4.  One read and one write of each state.
  *
- *   q, k   [N, H, d_k] qkv_dtype;  v [N, H, d_v] qkv_dtype;  g, beta [N, H] fp32.
+ *   q, k   [N, H_k, d_k] qkv_dtype;  v [N, H, d_v] qkv_dtype;  beta [N, H] fp32;
+ *          g [N, H] fp32 (GDN_DECAY_PER_HEAD) or [N, H, d_k] (GDN_DECAY_PER_KEY_CHANNEL).
  *   state  [N, H, d_v, d_k] fp32, read and overwritten with the new state.
+ *   conv_weight [conv_dim, 4] or NULL; conv_state_in / conv_state_out [N, conv_dim, 3]: the
+ *          three raw inputs before this token (NULL in: zeros) and after it (NULL out: not
+ *          written).  The two may be the same array only when H_k == H (with grouped heads the
+ *          query/key history is read by several CTAs, so an in-place update would race).
  *   gate_z [N, H, d_v] fp32 or NULL; norm_weight [d_v] or NULL; as in gdn_chunk_fwd.
  *   out    [N, H, d_v] of out_dtype; must not overlap state.
  */
 int gdn_recurrent_step(const void* q, const void* k, const void* v, const float* g,
-                       const float* beta, float* state, int N, int H, int d_k, int d_v,
-                       gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
+                       const float* beta, float* state, int N, int H, int H_k, int d_k, int d_v,
+                       gdn_dtype qkv_dtype, gdn_decay decay, float scale, int use_qk_l2norm,
+                       const float* conv_weight, const float* conv_state_in, float* conv_state_out,
                        const float* gate_z, const float* norm_weight, float norm_eps,
                        void* out, gdn_dtype out_dtype, void* stream);
 
@@ -109,8 +148,12 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v, const float*
  * applied T times in order (speculative / multi-token decode).  Each state is read once, kept on
  * chip for the T tokens, and written once.
  *
- *   q, k   [N, T, H, d_k] qkv_dtype;  v [N, T, H, d_v];  g, beta [N, T, H] fp32.
+ *   q, k   [N, T, H_k, d_k] qkv_dtype;  v [N, T, H, d_v];  beta [N, T, H] fp32;
+ *          g [N, T, H] fp32, or [N, T, H, d_k] with GDN_DECAY_PER_KEY_CHANNEL.
  *   state_pool     [num_slots, H, d_v, d_k] fp32, updated in place.
+ *   conv_weight    [conv_dim, 4] or NULL; conv_state_in / conv_state_out
+ *                  [num_slots, conv_dim, 3], indexed like the state pool, with the aliasing rule
+ *                  of gdn_recurrent_step.
  *   state_indices  device int32 [N] or NULL (then sequence n uses slot n; num_slots >= N).  A
  *                  negative index skips the sequence (nothing read or written).  An index
  *                  >= num_slots is caught on the device: the sequence is skipped and GDN_ERR_ARG is
@@ -119,8 +162,10 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v, const float*
  */
 int gdn_recurrent_multi_step(const void* q, const void* k, const void* v, const float* g,
                              const float* beta, float* state_pool, int num_slots,
-                             const int32_t* state_indices, int N, int T, int H, int d_k, int d_v,
-                             gdn_dtype qkv_dtype, float scale, int use_qk_l2norm,
+                             const int32_t* state_indices, int N, int T, int H, int H_k, int d_k,
+                             int d_v, gdn_dtype qkv_dtype, gdn_decay decay, float scale,
+                             int use_qk_l2norm, const float* conv_weight,
+                             const float* conv_state_in, float* conv_state_out,
                              const float* gate_z, const float* norm_weight, float norm_eps,
                              void* out, gdn_dtype out_dtype, void* stream);
 
@@ -172,8 +217,10 @@ int gdn_decay_from_logits(const float* a, const float* A_log, const float* dt_bi
 #define GDN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
                           const float* beta, const int32_t* cu_seqlens, int num_seqs, int total_T,
-                          int H, int d_k, int d_v, gdn_dtype qkv_dtype, float scale,
-                          int use_qk_l2norm, const float* initial_state, float* final_state,
+                          int H, int H_k, int d_k, int d_v, gdn_dtype qkv_dtype, gdn_decay decay,
+                          float scale, int use_qk_l2norm, const float* conv_weight,
+                          const float* conv_state_in, float* conv_state_out,
+                          const float* initial_state, float* final_state,
                           const float* gate_z, const float* norm_weight, float norm_eps,
                           void* out, gdn_dtype out_dtype, void* stream);
 

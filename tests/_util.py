@@ -53,9 +53,35 @@ def cu_list(inp):
 
 
 def oracle_gates(inp):
-    """g, beta from the drawn logits, in fp64 by the oracle, rounded once to fp32."""
-    g, beta = oracle.gates_from_logits(inp["a"], inp["A_log"], b=inp["b"])
+    """g, beta from the drawn logits, in fp64 by the oracle, rounded once to fp32.  With logits per
+    key channel (a [T, H, d]) each channel is its own column with its head's A_log."""
+    a = inp["a"]
+    if a.dim() == 3:
+        T, H, d = a.shape
+        g = oracle.gates_from_logits(a.reshape(T, H * d), inp["A_log"].repeat_interleave(d))
+        _, beta = oracle.gates_from_logits(torch.zeros(T, H), inp["A_log"], b=inp["b"])
+        return torch.from_numpy(g).float().reshape(T, H, d), torch.from_numpy(beta).float()
+    g, beta = oracle.gates_from_logits(a, inp["A_log"], b=inp["b"])
     return torch.from_numpy(g).float(), torch.from_numpy(beta).float()
+
+
+def oracle_conv_qkv(q, k, v, conv_weight, conv_state, cu):
+    """The oracle's short convolution over the mixed q|k|v channels of raw inputs.
+    Returns (q, k, v) after convolution + SiLU (float64 numpy, input shapes) and the final
+    history [num_seqs, conv_dim, 3].  The convolution output is an activation of the q/k/v type
+    (the page's module runs in the model dtype), so it is rounded once to that type here, as the
+    kernels do, before the core sees it."""
+    T, Hk, d = q.shape
+    H = v.shape[1]
+    dt = q.dtype if isinstance(q, torch.Tensor) else torch.float64
+    x = torch.cat([torch.as_tensor(q).reshape(T, Hk * d).double(), torch.as_tensor(k).reshape(T, Hk * d).double(),
+                   torch.as_tensor(v).reshape(T, H * d).double()], dim=1)
+    y, st = oracle.short_conv(x, conv_weight, cu_seqlens=np.asarray(cu, dtype=np.int32), state=conv_state)
+    y = torch.from_numpy(y).to(dt).double().numpy()
+    qc = y[:, :Hk * d].reshape(T, Hk, d)
+    kc = y[:, Hk * d:2 * Hk * d].reshape(T, Hk, d)
+    vc = y[:, 2 * Hk * d:].reshape(T, H, d)
+    return qc, kc, vc, st
 
 
 def oracle_prefill(inp, g32, b32, scale=None, use_l2=True, threads=THREADS, gate=True,
@@ -65,7 +91,11 @@ def oracle_prefill(inp, g32, b32, scale=None, use_l2=True, threads=THREADS, gate
     cu = cu_list(inp)
     q, k, v, z, S0 = inp["q"], inp["k"], inp["v"], inp["z"], inp["initial_state"]
     g, b = g32, b32
+    if inp.get("conv_weight") is not None:
+        q, k, v, _ = oracle_conv_qkv(q, k, v, inp["conv_weight"], inp.get("conv_state"), cu)
+        q, k, v = (torch.from_numpy(t) for t in (q, k, v))
     if heads is not None:
+        assert q.shape[1] == v.shape[1], "head sampling needs one query/key head per value head"
         sel = lambda t: t[:, heads] if t is not None else None  # noqa: E731
         q, k, v, z, g, b = (sel(t) for t in (q, k, v, z, g, b))
         S0 = S0[:, heads] if S0 is not None else None

@@ -44,9 +44,9 @@ def test_status_strings():
 
 
 def _chunk(**kw):
-    args = dict(q=P, k=P, v=P, g=P, beta=P, cu=NUL, num_seqs=1, total_T=64, H=2, dk=128, dv=128,
-                dt=0, scale=0.0, l2=1, S0=NUL, Sf=NUL, z=NUL, w=NUL, eps=1e-6, out=P, odt=0,
-                ws=NUL, wsb=0, stream=NUL)
+    args = dict(q=P, k=P, v=P, g=P, beta=P, cu=NUL, num_seqs=1, total_T=64, H=2, Hk=2, dk=128, dv=128,
+                dt=0, decay=0, scale=0.0, l2=1, cw=NUL, cin=NUL, cout=NUL, S0=NUL, Sf=NUL, z=NUL,
+                w=NUL, eps=1e-6, out=P, odt=0, ws=NUL, wsb=0, stream=NUL)
     args.update(kw)
     return gdn.lib().gdn_chunk_fwd(*args.values())
 
@@ -65,7 +65,14 @@ def test_chunk_fwd_rejects_bad_arguments():
     assert _chunk(k=ctypes.c_void_p(0x10004)) == -1      # misaligned
     assert _chunk(w=P) == -1                              # weight without a gate
     assert _chunk(eps=-1.0) == -1
-    assert _chunk(num_seqs=1 << 20, H=1 << 12, total_T=0) == -1  # grid too large
+    assert _chunk(num_seqs=1 << 20, H=1 << 12, Hk=1 << 12, total_T=0) == -1  # grid too large
+    assert _chunk(Hk=0) == -1
+    assert _chunk(H=6, Hk=4) == -1                        # H must be a multiple of H_k
+    assert _chunk(H=2, Hk=4) == -1
+    assert _chunk(decay=2) == -1
+    assert _chunk(cin=P) == -1                            # convolution state without weights
+    assert _chunk(cout=P) == -1
+    assert _chunk(cw=ctypes.c_void_p(0x10004)) == -1     # misaligned weights
 
 
 def test_workspace_size_is_consistent():
@@ -84,8 +91,9 @@ def test_recurrent_step_rejects_bad_arguments():
     L = gdn.lib()
 
     def step(**kw):
-        a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, N=4, H=2, dk=128, dv=128, dt=1, scale=0.0, l2=1,
-                 z=NUL, w=NUL, eps=1e-6, out=P, odt=1, stream=NUL)
+        a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, N=4, H=2, Hk=2, dk=128, dv=128, dt=1, decay=0,
+                 scale=0.0, l2=1, cw=NUL, cin=NUL, cout=NUL, z=NUL, w=NUL, eps=1e-6, out=P, odt=1,
+                 stream=NUL)
         a.update(kw)
         return L.gdn_recurrent_step(*a.values())
 
@@ -97,6 +105,11 @@ def test_recurrent_step_rejects_bad_arguments():
     assert step(S=NUL) == -1
     assert step(S=ctypes.c_void_p(0x10008)) == -1
     assert step(w=P) == -1
+    assert step(H=4, Hk=3) == -1
+    assert step(decay=5) == -1
+    assert step(cin=P, cout=NUL) == -1                    # state without weights
+    # an in-place convolution-state update races when query/key heads are shared
+    assert step(H=4, Hk=2, cw=P, cin=P, cout=P) == -1
 
 
 def test_gate_and_decay_reject_bad_arguments():
@@ -128,8 +141,9 @@ def test_recurrent_multi_step_rejects_bad_arguments():
     L = gdn.lib()
 
     def ms(**kw):
-        a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, slots=8, idx=NUL, N=4, T=2, H=2, dk=128, dv=128, dt=1,
-                 scale=0.0, l2=1, z=NUL, w=NUL, eps=1e-6, out=P, odt=1, stream=NUL)
+        a = dict(q=P, k=P, v=P, g=P, beta=P, S=P, slots=8, idx=NUL, N=4, T=2, H=2, Hk=2, dk=128, dv=128,
+                 dt=1, decay=0, scale=0.0, l2=1, cw=NUL, cin=NUL, cout=NUL, z=NUL, w=NUL, eps=1e-6,
+                 out=P, odt=1, stream=NUL)
         a.update(kw)
         return L.gdn_recurrent_multi_step(*a.values())
 
@@ -141,3 +155,5 @@ def test_recurrent_multi_step_rejects_bad_arguments():
     assert ms(dk=64, dv=128) == -7
     assert ms(S=NUL) == -1
     assert ms(w=P) == -1
+    assert ms(H=2, Hk=4) == -1
+    assert ms(H=8, Hk=2, cw=P, cin=P, cout=P) == -1

@@ -46,6 +46,6 @@ def test_noalloc_refuses_sizes_beyond_the_array():
     out = torch.zeros(1, H, 128, dtype=torch.bfloat16, device="cuda")
     L = gdn.lib()
     rc = L.gdn_chunk_fwd_noalloc(x.data_ptr(), x.data_ptr(), x.data_ptr(), gf.data_ptr(), gf.data_ptr(),
-                                 None, 1, T, H, 128, 128, gdn.GDN_BF16, 0.0, 1, None, None, None, None,
-                                 1e-6, out.data_ptr(), gdn.GDN_BF16, None)
+                                 None, 1, T, H, H, 128, 128, gdn.GDN_BF16, 0, 0.0, 1, None, None, None,
+                                 None, None, None, None, 1e-6, out.data_ptr(), gdn.GDN_BF16, None)
     assert rc == -4  # GDN_ERR_WORKSPACE, rejected before any launch
