@@ -359,6 +359,106 @@ def bench_decode(args, dev):
                 multi_bytes=multi_bytes, multi_slots=slots)
 
 
+def bench_variants(args, dev):
+    """The prefill options on the prefill workload's sizes (B=2 x T=4096, H=16, d=128, bf16, fused
+    gate): 4 query/key heads shared by 16 value heads, a decay per key channel, and the fused short
+    convolution; plus one decode step with the convolution and its history updated in place.  Each
+    timed region is one gdn_chunk_fwd (or gdn_recurrent_step) call, L2 flushed before every call."""
+    import gated_deltanet_recurrence_gb300 as gdn
+    from gated_deltanet_recurrence_gb300 import synthetic
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peaks, _ = load_peaks()
+    res = {}
+    steps = max(3, min(args.steps, 10))
+    for name in ("prefill_gva", "prefill_kda", "prefill_conv"):
+        inp = synthetic.prefill_inputs(name)
+        cfg = inp["cfg"]
+        total_T, H, d, n = inp["total_T"], cfg["H"], cfg["d"], inp["num_seqs"]
+        Hk = cfg.get("Hk", H)
+        q, k, v, z = (inp[x].to(dev) for x in ("q", "k", "v", "z"))
+        A_log, b = inp["A_log"].to(dev), inp["b"].to(dev)
+        a = inp["a"].to(dev)
+        if a.dim() == 3:  # one log-decay per key channel: each channel is a column with its head's A_log
+            g = gdn.gdn_decay_from_logits(a.reshape(total_T, H * d), A_log.repeat_interleave(d)).reshape(total_T, H, d)
+            _, beta = gdn.gdn_decay_from_logits(torch.zeros_like(b), A_log, b=b)
+        else:
+            g, beta = gdn.gdn_decay_from_logits(a, A_log, b=b)
+        cw = inp["conv_weight"].to(dev) if inp["conv_weight"] is not None else None
+        out = torch.empty(total_T, H, d, dtype=torch.bfloat16, device=dev)
+        Sf = torch.empty(n, H, d, d, device=dev)
+        ws_bytes = gdn.lib().gdn_chunk_fwd_workspace_size(n, total_T, H, d, d, gdn.GDN_BF16)
+        ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+        def call():
+            gdn.gdn_chunk_fwd(q, k, v, g, beta, num_seqs=n, conv_weight=cw, gate_z=z, out=out,
+                              final_state=Sf, workspace=ws)
+
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize()
+        assert gdn.gdn_get_device_error() == 0
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        assert gdn.gdn_get_device_error() == 0
+        ms = statistics.mean(x.elapsed_time(y) for x, y in ts)
+        per_tok_head = (2 * Hk / H + 1) * d * 2 + 4 * (d if a.dim() == 3 else 1) + 4 + d * 4 + d * 2
+        byts = total_T * H * per_tok_head + n * H * d * d * 4
+        gbs = byts / (ms / 1e3) / 1e9
+        path = "tensor-core" if (ws_bytes > 0 and a.dim() == 2) else "cuda-core"
+        res[name] = {"tokens_per_s": total_T / (ms / 1e3), "ms": ms, "path": path, "H": H, "H_k": Hk,
+                     "decay": "per key channel" if a.dim() == 3 else "per head",
+                     "conv": cw is not None, "algorithmic_bytes": byts, "hbm_gbs": gbs,
+                     "hbm_frac": gbs / peaks["hbm_gbs"]}
+        if a.dim() == 3:
+            th = total_T * H
+            res[name]["fp32_tflops"] = th * prefill_flops_per_token_head(d) / (ms / 1e3) / 1e12
+        del q, k, v, z, g, beta, out, Sf, ws
+
+    # decode with the fused convolution, history updated in place
+    inp = synthetic.decode_inputs("decode")
+    cfg = inp["cfg"]
+    N, H, d = cfg["N"], cfg["H"], cfg["d"]
+    q, k, v, a, A_log, b = (inp[x].to(dev) for x in ("q", "k", "v", "a", "A_log", "b"))
+    state = inp["state"].to(dev)
+    g, beta = gdn.gdn_decay_from_logits(a, A_log, b=b)
+    C = synthetic.conv_dim(H, H, d)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    cw = torch.rand(C, 4, generator=gen, device=dev) - 0.5
+    cs = torch.randn(N, C, 3, generator=gen, device=dev)
+    out = torch.empty(N, H, d, dtype=torch.bfloat16, device=dev)
+
+    def dcall():
+        gdn.gdn_recurrent_step(q, k, v, g, beta, state, conv_weight=cw, conv_state=cs, conv_state_out=cs, out=out)
+
+    for _ in range(3):
+        dcall()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(args.steps, 20)):
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        dcall()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    assert gdn.gdn_get_device_error() == 0
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ts)
+    byts = decode_bytes(N, H, d) + N * C * 3 * 4 * 2 + C * 16
+    res["decode_conv"] = {"tokens_per_s": N / (ms / 1e3), "ms": ms, "algorithmic_bytes": byts,
+                          "hbm_gbs": byts / (ms / 1e3) / 1e9,
+                          "hbm_frac": byts / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    return res
+
+
 def run_gdn(args):
     dev = torch.device("cuda", args.local)
     torch.cuda.set_device(dev)
@@ -375,6 +475,7 @@ def run_gdn(args):
                               "e2e_ms": pf["e2e_ms"]}), flush=True)
         return
     dc = bench_decode(args, dev)
+    variants = bench_variants(args, dev) if not args.no_variants else None
     world = args.world
     ms = max_over_ranks(pf["ms"], world)
     e2e_ms = max_over_ranks(pf["e2e_ms"], world)
@@ -423,6 +524,7 @@ def run_gdn(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "decode": decode,
+        "variants": variants,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": pf["h2d"],
                 "d2h_bytes_per_step": pf["d2h"], "ms_per_step": e2e_ms},
         "gpu_launches": pf["launches"],
@@ -472,6 +574,8 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="budget of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the grouped-head / per-channel-decay / convolution measurements")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time only one workload (profiling runs); the driver uses the default")
     args = ap.parse_args()
