@@ -70,7 +70,7 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 //     sk_r = s_r . ka,  sq_r = s_r . qa,  delta_r = beta (v_r - sk_r)
 //     s_r <- alpha . s_r + delta_r k,     y_r = sq_r + delta_r (k . q)
 template <int D, typename TIn, bool GATE, bool CONV>
-__global__ void __launch_bounds__(D * 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
     constexpr int EPT = D / 32;
     static_assert(D / kRowsPerWarp * 32 == D * 2, "one warp per 16 rows");
     __shared__ float ys[GATE ? D : 1];
@@ -96,22 +96,17 @@ __global__ void __launch_bounds__(D * 2) decode_kernel(DecodeArgs a) {
 
     // short convolution: taps and the three previous raw inputs of this lane's channels
     const int cq = hk * D + lane * EPT, ck = a.Hk * D + cq, cv = 2 * a.Hk * D + h * D + vrow;
-    float4 wq[CONV ? EPT : 1], wk[CONV ? EPT : 1], wv;
+    const float4* w4 = reinterpret_cast<const float4*>(a.conv.w);
     float hq[CONV ? EPT : 1][3], hkk[CONV ? EPT : 1][3], hv[3];
     if constexpr (CONV) {
-        const float4* w4 = reinterpret_cast<const float4*>(a.conv.w);
         const float* si = a.conv.state_in ? a.conv.state_in + (long)slot * a.conv.dim * 3 : nullptr;
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-            wq[e] = __ldg(w4 + cq + e);
-            wk[e] = __ldg(w4 + ck + e);
+        for (int e = 0; e < EPT; ++e)
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
                 hq[e][j] = si ? si[(long)(cq + e) * 3 + j] : 0.f;
                 hkk[e][j] = si ? si[(long)(ck + e) * 3 + j] : 0.f;
             }
-        }
-        wv = __ldg(w4 + cv);
 #pragma unroll
         for (int j = 0; j < 3; ++j) hv[j] = si ? si[(long)cv * 3 + j] : 0.f;
     }
@@ -128,15 +123,15 @@ __global__ void __launch_bounds__(D * 2) decode_kernel(DecodeArgs a) {
         float vr = to_f32(static_cast<const TIn*>(a.v)[vt * D + vrow]);
         if constexpr (CONV) {
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) {
+            for (int e = 0; e < EPT; ++e) {  // taps read here (L1) rather than held across the tokens
                 const float xq = qv[e], xk = kv[e];
-                qv[e] = round_to<TIn>(conv4_silu(wq[e], hq[e][0], hq[e][1], hq[e][2], xq));
-                kv[e] = round_to<TIn>(conv4_silu(wk[e], hkk[e][0], hkk[e][1], hkk[e][2], xk));
+                qv[e] = round_to<TIn>(conv4_silu(__ldg(w4 + cq + e), hq[e][0], hq[e][1], hq[e][2], xq));
+                kv[e] = round_to<TIn>(conv4_silu(__ldg(w4 + ck + e), hkk[e][0], hkk[e][1], hkk[e][2], xk));
                 hq[e][0] = hq[e][1]; hq[e][1] = hq[e][2]; hq[e][2] = xq;
                 hkk[e][0] = hkk[e][1]; hkk[e][1] = hkk[e][2]; hkk[e][2] = xk;
             }
             const float xv = vr;
-            vr = round_to<TIn>(conv4_silu(wv, hv[0], hv[1], hv[2], xv));
+            vr = round_to<TIn>(conv4_silu(__ldg(w4 + cv), hv[0], hv[1], hv[2], xv));
             hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
         }
         if (a.g_per_channel) {

@@ -190,28 +190,6 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, chunk * 8)) = p;
 }
 
-// Short convolution + SiLU ("因果卷积") of one channel of a loaded 128B-swizzled operand tile, in
-// place, rows 0..L-1 of the chunk starting at token t0.  The three inputs before t0 come from the
-// sequence (t >= bos) or from the carried state.  `src` points at the channel's column of the raw
-// tensor (row stride `stride` elements); c is the channel's index in the mixed q|k|v layout.
-__device__ __forceinline__ void conv_column(uint8_t* tile, int col, const __nv_bfloat16* src, long stride,
-                                            const TcArgs& a, int n, int c, long bos, long t0, int L) {
-    const float4 w = __ldg(reinterpret_cast<const float4*>(a.conv.w) + c);
-    const float* hist = a.conv.state_in ? a.conv.state_in + ((long)n * a.conv.dim + c) * 3 : nullptr;
-    float hq[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        const long t = t0 - 3 + j;
-        hq[j] = t >= bos ? __bfloat162float(src[t * stride]) : (hist ? hist[3 + (t - bos)] : 0.f);
-    }
-    for (int i = 0; i < L; ++i) {
-        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(tile + sw128_offset(i, col));
-        const float x = __bfloat162float(*e);
-        *e = __float2bfloat16_rn(conv4_silu(w, hq[0], hq[1], hq[2], x));
-        hq[0] = hq[1]; hq[1] = hq[2]; hq[2] = x;
-    }
-}
-
 __device__ __forceinline__ void ld_sw128_chunk(const uint8_t* tile, int row, int chunk, float* v) {
     uint4 p = *reinterpret_cast<const uint4*>(tile + sw128_offset(row, chunk * 8));
     const uint32_t w[4] = {p.x, p.y, p.z, p.w};
@@ -316,6 +294,100 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
     }
 }
 
+// silu(c) = c sigmoid(c) = (c/2)(1 + tanh(c/2)), with the hardware tanh approximation (relative
+// error near 2^-11; the result is rounded to bf16, 2^-9, next).
+__device__ __forceinline__ float silu_tanh(float c) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * c));
+    return fmaf(0.5f * c, t, 0.5f * c);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 p, float* f) {
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        f[2 * e] = t.x;
+        f[2 * e + 1] = t.y;
+    }
+}
+
+// Short convolution + SiLU ("因果卷积") of the loaded Q, K, V tiles (128B-swizzled bf16), in place,
+// rows 0..L-1 of the chunk starting at token t0.  Thread tid owns 8 consecutive channels (one
+// 16-byte chunk: c8 = tid % 8 of column half (tid / 8) % 2) and 8 rows (segment tid / 16) of each
+// tile, so a quarter-warp reads or writes one whole 128-byte row.  Every thread first captures the
+// three raw rows before its segment (from the tile, or, for the first segment, from the sequence
+// in global memory or the carried state); after a barrier it reads its 8 raw rows, convolves
+// them and writes them back, so no thread reads a row that another one has overwritten.
+__device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, int h, int hk, long bos,
+                                           long t0, int L, int tid) {
+    using namespace prep;
+    const int c8 = tid & 7, half = (tid >> 3) & 1, r0 = (tid >> 4) * 8;
+    const int x0 = half * 64 + c8 * 8;
+    uint8_t* tiles[3] = {sm + oKQ + half * 16384 + 8192, sm + oKQ + half * 16384, sm + oV + half * 8192};
+    const __nv_bfloat16* srcs[3] = {a.q + hk * kD + x0, a.k + hk * kD + x0, a.v + (long)h * kD + x0};
+    const long strides[3] = {(long)a.Hk * kD, (long)a.Hk * kD, (long)a.H * kD};
+    const int chans[3] = {hk * kD + x0, a.Hk * kD + hk * kD + x0, 2 * a.Hk * kD + h * kD + x0};
+    const bool live = r0 < L;
+    float hist[3][3][8];
+#pragma unroll
+    for (int ten = 0; ten < 3; ++ten)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int r = r0 - 3 + j;
+            float* f = hist[ten][j];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            if (!live) continue;
+            if (r >= 0) {
+                unpack_bf16x8(*reinterpret_cast<const uint4*>(tiles[ten] + sw128_offset(r, c8 * 8)), f);
+            } else {
+                const long t = t0 + r;
+                if (t >= bos) {
+                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(srcs[ten] + t * strides[ten])), f);
+                } else if (a.conv.state_in) {
+                    const float* st = a.conv.state_in + ((long)n * a.conv.dim + chans[ten]) * 3 + 3 + (t - bos);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = st[e * 3];
+                }
+            }
+        }
+    __syncthreads();
+    if (!live) return;
+#pragma unroll
+    for (int ten = 0; ten < 3; ++ten) {
+        uint4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            raw[i] = r0 + i < L ? *reinterpret_cast<const uint4*>(tiles[ten] + sw128_offset(r0 + i, c8 * 8))
+                                : make_uint4(0, 0, 0, 0);
+        float4 w[8];
+        const float4* w4 = reinterpret_cast<const float4*>(a.conv.w) + chans[ten];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = __ldg(w4 + e);
+        float* h0 = hist[ten][0];
+        float* h1 = hist[ten][1];
+        float* h2 = hist[ten][2];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float x[8];
+            unpack_bf16x8(raw[i], x);
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const float y0 = silu_tanh(fmaf(w[e].w, x[e], fmaf(w[e].z, h2[e], fmaf(w[e].y, h1[e], w[e].x * h0[e]))));
+                const float y1 = silu_tanh(fmaf(w[e + 1].w, x[e + 1],
+                                                fmaf(w[e + 1].z, h2[e + 1], fmaf(w[e + 1].y, h1[e + 1], w[e + 1].x * h0[e + 1]))));
+                o[e / 2] = pack_bf16x2(y0, y1);
+            }
+            if (r0 + i < L)
+                *reinterpret_cast<uint4*>(tiles[ten] + sw128_offset(r0 + i, c8 * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { h0[e] = h1[e]; h1[e] = h2[e]; h2[e] = x[e]; }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(prep::kThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, TcArgs a) {
@@ -386,14 +458,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         gcs[2 * lane + 1] = s;
     }
     bool ok = mbar_wait(&bars[0], 0, kPolls);
-    if (ok && a.conv.w) {  // fused short convolution of the loaded rows: thread = channel
-        const int x = tid, half = x >> 6, col = x & 63;
-        const long qks = (long)a.Hk * kD, vs = (long)a.H * kD;
-        const int cq = hk * kD + x;
-        conv_column(sm + oKQ + half * 16384 + 8192, col, a.q + hk * kD + x, qks, a, n, cq, bos, t0, L);
-        conv_column(sm + oKQ + half * 16384, col, a.k + hk * kD + x, qks, a, n, a.Hk * kD + cq, bos, t0, L);
-        conv_column(sm + oV + half * 8192, col, a.v + (long)h * kD + x, vs, a, n, 2 * a.Hk * kD + h * kD + x,
-                    bos, t0, L);
+    if (a.conv.w) {  // fused short convolution of the loaded rows (block-uniform: has a barrier)
+        if (!__syncthreads_or(!ok)) conv_tiles(sm, a, n, h, hk, bos, t0, L, tid);
     }
     if (ok && L < kC) {  // rows past the end of the sequence hold other tokens: zero them
         for (int e = tid; e < (kC - L) * 8 * 5; e += kThreads) {
