@@ -82,9 +82,9 @@ int gdn_get_device_error(void* stream, int* device_status) {
     return GDN_OK;
 }
 
-// The tensor-core path (bf16, d = 128, one decay per head) keeps per-chunk intermediates (W, U^T,
-// the decayed Q K^T and per-token factors, about 41 KB per chunk and head) in the caller's
-// workspace; the fp32 CUDA-core path needs none.
+// The tensor-core path (bf16, d = 128) keeps per-chunk intermediates (W, U^T, the decayed Q K^T,
+// Q~, K~ and decay factors, about 42 KB per chunk and head) in the caller's workspace; the fp32
+// CUDA-core path needs none.
 static bool uses_tc_path(int num_seqs, int total_T, int H, int d_k, int d_v, int qkv_dtype) {
     return qkv_dtype == GDN_BF16 && d_k == 128 && d_v == 128 && total_T > 0 && num_seqs > 0 && H > 0;
 }
@@ -137,8 +137,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if (total_T > 0 || final_state) {
-        if (uses_tc_path(num_seqs, total_T, H, d_k, d_v, qkv_dtype) && !a.g_per_channel &&
-            gdn::prefill_tc_supported(a))
+        if (uses_tc_path(num_seqs, total_T, H, d_k, d_v, qkv_dtype) && gdn::prefill_tc_supported(a))
             e = gdn::launch_prefill_tc(a, st);
         else
             e = gdn::launch_prefill_simt(a, st);

@@ -50,7 +50,7 @@ constexpr uint64_t kPolls = 2000000000ull;  // bound on any single mbarrier wait
 
 struct WsLayout {
     long nch;          // chunk-head slots = max_chunks * H
-    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, total;
+    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, off_gam, total;
 };
 
 __host__ __device__ inline long max_chunks(int num_seqs, int total_T) { return (long)total_T / kC + num_seqs; }
@@ -70,6 +70,7 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
     w.off_scal = o;  o = al(o + sizeof(float) * w.nch * 4 * kC);
     w.off_Qt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^gc qs) Q
     w.off_Kt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^(glast-gc) kinv) K
+    w.off_gam = o;   o = al(o + sizeof(float) * w.nch * kD);                // per-channel e^(gc_last)
     w.total = o;
     return w;
 }
@@ -94,6 +95,7 @@ struct TcArgs {
     float* scal;
     __nv_bfloat16* Qt;
     __nv_bfloat16* Kt;
+    float* gam;          // decay per key channel: e^(gc_last) per chunk and channel [nch][128]
     const float* initial_state;
     float* final_state;
     const float* z;
@@ -154,8 +156,8 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
 
 // ---- shared helpers --------------------------------------------------------------------------------
 
-// SiLU for the output gate, from sigma(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh
-// approximation (relative error near 5e-4, below the bf16 rounding of the output that follows):
+// SiLU from sigma(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation (relative error
+// near 5e-4, below the bf16 rounding that follows wherever it is used):
 // x sigma(x) = h + h tanh(h) with h = x / 2.
 __device__ __forceinline__ float fast_silu(float x) {
     const float hx = 0.5f * x;
@@ -294,14 +296,6 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
     }
 }
 
-// silu(c) = c sigmoid(c) = (c/2)(1 + tanh(c/2)), with the hardware tanh approximation (relative
-// error near 2^-11; the result is rounded to bf16, 2^-9, next).
-__device__ __forceinline__ float silu_tanh(float c) {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * c));
-    return fmaf(0.5f * c, t, 0.5f * c);
-}
-
 __device__ __forceinline__ void unpack_bf16x8(uint4 p, float* f) {
     const uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
@@ -375,8 +369,8 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
             uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const float y0 = silu_tanh(fmaf(w[e].w, x[e], fmaf(w[e].z, h2[e], fmaf(w[e].y, h1[e], w[e].x * h0[e]))));
-                const float y1 = silu_tanh(fmaf(w[e + 1].w, x[e + 1],
+                const float y0 = fast_silu(fmaf(w[e].w, x[e], fmaf(w[e].z, h2[e], fmaf(w[e].y, h1[e], w[e].x * h0[e]))));
+                const float y1 = fast_silu(fmaf(w[e + 1].w, x[e + 1],
                                                 fmaf(w[e + 1].z, h2[e + 1], fmaf(w[e + 1].y, h1[e + 1], w[e + 1].x * h0[e + 1]))));
                 o[e / 2] = pack_bf16x2(y0, y1);
             }
@@ -388,6 +382,218 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
     }
 }
 
+
+// ---- decay per key channel ("6.6 Gated DeltaNet" 6.6.7): the products on the CUDA cores ------------
+//
+// With g a vector per token, the in-chunk decays enter the contraction over the key channels:
+//     A_ij   = beta_i kinv_i kinv_j  sum_c k_ic k_jc e^(G_ic - G_jc)     (j < i)
+//     Aqk_ij = qs_i kinv_j           sum_c q_ic k_jc e^(G_ic - G_jc)     (j <= i)
+// with G the per-channel inclusive sums of g down the chunk.  Each thread owns a 4 x 4 block of the
+// strictly lower triangle (120 blocks for threads 0-119) and takes its first row r as reference:
+// e^(G_i - G_j) = e^(G_i - G_r) e^(G_r - G_j), both factors <= 1 (G does not increase down the
+// chunk and j < r <= i), so 8 exponentials per channel serve 16 pairs and nothing overflows.  The
+// 16 diagonal 4 x 4 blocks take their 6 exponentials per channel directly; all 128 threads share
+// them, 8 channels each, and add their partial sums with shuffles.  The channels are processed in
+// two halves of 64 so that the transposed copies fit in the T', T'' and A tiles, which are not yet
+// in use.  The same pass writes the state pass's operand rows Q~ = qs diag(e^G) Q and
+// K~ = kinv diag(e^(G_last - G)) K, the per-channel e^(G_last), and overwrites the K tile with
+// K . e^G, the operand of W = T diag(beta kinv) (K . e^G).
+namespace pcx {
+constexpr int LDG = 68;                      // G^T row stride (floats): [channel][row], 16-byte rows
+constexpr int LDK = 68;                      // K^T, Q^T row stride (bf16): 136 bytes
+constexpr uint32_t oGT = prep::oTP;
+constexpr uint32_t oKT = oGT + 64 * LDG * 4;
+constexpr uint32_t oQT = oKT + 64 * LDK * 2;
+constexpr uint32_t kEnd = oQT + 64 * LDK * 2;
+static_assert(kEnd <= prep::oSc, "per-channel scratch must end before the per-token scalars");
+}  // namespace pcx
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void bf16x4(uint2 w, float* f) {
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+
+__device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t0, int L, int tid,
+                            const float* kinv, const float* qsv, const float* bts, float* Af, float* Tf) {
+    using namespace prep;
+    float* GT = reinterpret_cast<float*>(sm + pcx::oGT);
+    __nv_bfloat16* KT = reinterpret_cast<__nv_bfloat16*>(sm + pcx::oKT);
+    __nv_bfloat16* QT = reinterpret_cast<__nv_bfloat16*>(sm + pcx::oQT);
+    constexpr int LG = pcx::LDG, LK = pcx::LDK;
+    constexpr float kLog2e = 1.4426950408889634f;
+
+    const bool off = tid < 120;                  // strictly lower block (I, J), J < I, row by row
+    int I = 1, J = tid;
+    while (J >= I) { J -= I; ++I; }
+    const int i0 = 4 * I, j0 = 4 * J;
+    const int dr = 4 * (tid >> 3), cg = tid & 7; // diagonal block at row dr; channels e * 8 + cg
+
+    float accA[16], accQ[16], dA[6], dQ[10];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) { accA[e] = 0.f; accQ[e] = 0.f; }
+#pragma unroll
+    for (int e = 0; e < 6; ++e) dA[e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 10; ++e) dQ[e] = 0.f;
+
+    for (int hf = 0; hf < 2; ++hf) {
+        // (a) per-channel inclusive sums, in log2 units; e^(G_last) for the state pass
+        if (tid < 64) {
+            const float* gp = a.g + (t0 * a.H + h) * (long)kD + hf * 64 + tid;
+            const long gs = (long)a.H * kD;
+            float acc = 0.f;
+#pragma unroll 16
+            for (int i = 0; i < kC; ++i) {
+                acc += i < L ? __ldg(gp + i * gs) : 0.f;
+                GT[tid * LG + i] = acc * kLog2e;
+            }
+            a.gam[gh * kD + hf * 64 + tid] = ex2_approx(acc * kLog2e);
+        }
+        __syncthreads();
+        // (b) raw transposed copies; Q~, K~ rows to the workspace; K . e^G in the K tile
+        {
+            const int i = tid & 63, hc = tid >> 6;
+            uint8_t* ktile = sm + oKQ + hf * 16384;
+            const uint8_t* qtile = ktile + 8192;
+            const float fq = qsv[i], fk = kinv[i];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c8 = hc * 4 + cc;
+                const uint4 kr = *reinterpret_cast<const uint4*>(ktile + sw128_offset(i, c8 * 8));
+                const uint4 qr = *reinterpret_cast<const uint4*>(qtile + sw128_offset(i, c8 * 8));
+                float kf[8], qf[8], qo[8], ko[8], ke[8];
+                unpack_bf16x8(kr, kf);
+                unpack_bf16x8(qr, qf);
+                const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int cl = c8 * 8 + e;
+                    KT[cl * LK + i] = kb[e];
+                    QT[cl * LK + i] = qb[e];
+                    const float G = GT[cl * LG + i], Gl = GT[cl * LG + kC - 1];
+                    const float eg = ex2_approx(G), el = ex2_approx(Gl - G);
+                    qo[e] = qf[e] * eg * fq;
+                    ko[e] = kf[e] * el * fk;
+                    ke[e] = kf[e] * eg;
+                }
+                *reinterpret_cast<uint4*>(ktile + sw128_offset(i, c8 * 8)) = pack_bf16x8(ke);
+                const long ro = gh * kC * kD + (long)i * kD + hf * 64 + c8 * 8;
+                *reinterpret_cast<uint4*>(a.Qt + ro) = pack_bf16x8(qo);
+                *reinterpret_cast<uint4*>(a.Kt + ro) = pack_bf16x8(ko);
+            }
+        }
+        __syncthreads();
+        // (c) products over this half's 64 channels
+        if (off) {
+#pragma unroll 2
+            for (int cl = 0; cl < 64; ++cl) {
+                const float4 Gi = *reinterpret_cast<const float4*>(GT + cl * LG + i0);
+                const float4 Gj = *reinterpret_cast<const float4*>(GT + cl * LG + j0);
+                float ki[4], qi[4], kj[4];
+                bf16x4(*reinterpret_cast<const uint2*>(KT + cl * LK + i0), ki);
+                bf16x4(*reinterpret_cast<const uint2*>(QT + cl * LK + i0), qi);
+                bf16x4(*reinterpret_cast<const uint2*>(KT + cl * LK + j0), kj);
+                const float ei[4] = {1.f, ex2_approx(Gi.y - Gi.x), ex2_approx(Gi.z - Gi.x), ex2_approx(Gi.w - Gi.x)};
+                const float ej[4] = {ex2_approx(Gi.x - Gj.x), ex2_approx(Gi.x - Gj.y), ex2_approx(Gi.x - Gj.z),
+                                     ex2_approx(Gi.x - Gj.w)};
+                float kje[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) kje[b] = kj[b] * ej[b];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float kie = ki[r] * ei[r], qie = qi[r] * ei[r];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        accA[r * 4 + b] = fmaf(kie, kje[b], accA[r * 4 + b]);
+                        accQ[r * 4 + b] = fmaf(qie, kje[b], accQ[r * 4 + b]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int cl = e * 8 + cg;
+            const float4 G = *reinterpret_cast<const float4*>(GT + cl * LG + dr);
+            float k[4], q[4];
+            bf16x4(*reinterpret_cast<const uint2*>(KT + cl * LK + dr), k);
+            bf16x4(*reinterpret_cast<const uint2*>(QT + cl * LK + dr), q);
+            const float e10 = ex2_approx(G.y - G.x), e20 = ex2_approx(G.z - G.x), e30 = ex2_approx(G.w - G.x);
+            const float e21 = ex2_approx(G.z - G.y), e31 = ex2_approx(G.w - G.y), e32 = ex2_approx(G.w - G.z);
+            const float k10 = k[0] * e10, k20 = k[0] * e20, k30 = k[0] * e30;
+            const float k21 = k[1] * e21, k31 = k[1] * e31, k32 = k[2] * e32;
+            dA[0] = fmaf(k[1], k10, dA[0]); dA[1] = fmaf(k[2], k20, dA[1]); dA[2] = fmaf(k[3], k30, dA[2]);
+            dA[3] = fmaf(k[2], k21, dA[3]); dA[4] = fmaf(k[3], k31, dA[4]); dA[5] = fmaf(k[3], k32, dA[5]);
+            dQ[0] = fmaf(q[0], k[0], dQ[0]); dQ[1] = fmaf(q[1], k10, dQ[1]); dQ[2] = fmaf(q[1], k[1], dQ[2]);
+            dQ[3] = fmaf(q[2], k20, dQ[3]); dQ[4] = fmaf(q[2], k21, dQ[4]); dQ[5] = fmaf(q[2], k[2], dQ[5]);
+            dQ[6] = fmaf(q[3], k30, dQ[6]); dQ[7] = fmaf(q[3], k31, dQ[7]); dQ[8] = fmaf(q[3], k32, dQ[8]);
+            dQ[9] = fmaf(q[3], k[3], dQ[9]);
+        }
+        __syncthreads();
+    }
+    // diagonal blocks: sum the 8 channel groups (lanes 8m .. 8m + 7 of one warp)
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 6; ++e) dA[e] += __shfl_xor_sync(0xffffffffu, dA[e], o);
+#pragma unroll
+        for (int e = 0; e < 10; ++e) dQ[e] += __shfl_xor_sync(0xffffffffu, dQ[e], o);
+    }
+    // A (fp32) into Af; the decayed Q K^T (fp32) staged in Tf
+    if (off) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const int i = i0 + r, j = j0 + b;
+                Af[i * LDA + j] = bts[i] * kinv[i] * kinv[j] * accA[r * 4 + b];
+                Tf[i * LD + j] = qsv[i] * kinv[j] * accQ[r * 4 + b];
+            }
+    }
+    if (cg == 0) {
+        const int ia[6] = {1, 2, 3, 2, 3, 3}, ja[6] = {0, 0, 0, 1, 1, 2};
+        const int iq[10] = {0, 1, 1, 2, 2, 2, 3, 3, 3, 3}, jq[10] = {0, 0, 1, 0, 1, 2, 0, 1, 2, 3};
+#pragma unroll
+        for (int e = 0; e < 6; ++e) {
+            const int i = dr + ia[e], j = dr + ja[e];
+            Af[i * LDA + j] = bts[i] * kinv[i] * kinv[j] * dA[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 10; ++e) {
+            const int i = dr + iq[e], j = dr + jq[e];
+            Tf[i * LD + j] = qsv[i] * kinv[j] * dQ[e];
+        }
+    }
+    __syncthreads();
+    if (tid >= kC) {  // decayed Q K^T rows to the workspace, zero above the diagonal
+        const int i = tid - kC;
+        uint4* dst = reinterpret_cast<uint4*>(a.Aqk + gh * kC * kC + (long)i * kC);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = c8 * 8 + e;
+                v[e] = j <= i ? Tf[i * LD + j] : 0.f;
+            }
+            dst[c8] = pack_bf16x8(v);
+        }
+    }
+}
+
+template <bool PC>
 __global__ void __launch_bounds__(prep::kThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, TcArgs a) {
@@ -430,7 +636,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     }
     if (tid < kC) {
         const bool in = tid < L;
-        gcs[tid] = in ? a.g[(t0 + tid) * a.H + h] : 0.f;
+        gcs[tid] = (in && !PC) ? a.g[(t0 + tid) * a.H + h] : 0.f;  // per channel: zero here
         bts[tid] = in ? a.beta[(t0 + tid) * a.H + h] : 0.f;
     }
     tc_fence_before();
@@ -525,6 +731,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         }
         tc_fence_before();
         __syncthreads();
+        if constexpr (PC) {
+            pc_products(sm, a, gh, h, t0, L, tid, kinv, qsv, bts, Af, Tf);
+        } else {
         if (tid < kC) {
             const int i = tid;
             const float gi = gcs[i], f = bts[i] * kinv[i];
@@ -571,6 +780,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                                       pack_bf16x2(v[6], v[7]));
             }
         }
+        }  // per-head decay
+        fence_async_smem();  // the K tile may have been rewritten (K . e^G) for the W product
         __syncthreads();
         // ---- T = (I + A)^-1 (the 16 x 48 fp32 scratch of the block steps lives in the T' tile,
         //      which is written only after the inverse is complete) ----
@@ -674,8 +885,10 @@ constexpr uint32_t kStage = 57344;          // multiple of 1024
 constexpr uint32_t oZ = oStage + 2 * kStage;     // gate input z, two buffers of 4 boxes of
                                                  // [64 tokens][32 fp32] SW128 = 2 x 32 KB
 constexpr uint32_t oBar = oZ + 2 * 32768;
-constexpr uint32_t kBytes = oBar + 256;
+constexpr uint32_t oGam = oBar + 256;       // decay per key channel: next chunk's e^(gc_last), 2 x 128 fp32
+constexpr uint32_t kBytes = oGam + 1024;
 constexpr uint32_t kSmem = kBytes + 1024;
+static_assert(kSmem <= 232448, "state kernel shared memory exceeds the per-block limit");
 constexpr uint32_t kStageTx = 32768 + 16384 + 8192;
 // barriers
 enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF, DA1, A12, SFULL, DO_0, DO_1, DOE_0, DOE_1, ZFULL0, ZFULL1, NBAR };
@@ -684,6 +897,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns of the state CTA: S [0,128); S W^T (M=128, 64 columns) x 2 buffers [128,256);
 // O = Q~ S^T + Aqk V_new (M=64, rows = tokens, 128 columns) x 2 buffers [256,512).
+template <bool PC>
 __global__ void __launch_bounds__(st::kThreads, 1)
 chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constant__ CUtensorMap mKt,
                    const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mAqk,
@@ -827,8 +1041,20 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(Sb + (blk >> 1) * 16384, r, (blk & 1) * 4 + c8, f + 8 * c8);
                 uint32_t v[32];
+                if constexpr (PC) {  // first chunk's decay, one factor per key channel (column)
+                    const float4* gv = reinterpret_cast<const float4*>(a.gam + ((long)first * a.H + h) * kD + blk * 32);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(g0 * f[j]);
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 t = __ldg(gv + j / 4);
+                        v[j] = __float_as_uint(t.x * f[j]);
+                        v[j + 1] = __float_as_uint(t.y * f[j + 1]);
+                        v[j + 2] = __float_as_uint(t.z * f[j + 2]);
+                        v[j + 3] = __float_as_uint(t.w * f[j + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(g0 * f[j]);
+                }
                 tmem_st32(tS + lrow + blk * 32, v);
             }
             if (nck > 0) {
@@ -854,7 +1080,9 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             uint4 up[8];
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) up[c8] = up_next[c8];
-            const float gnext = last ? 1.0f : __ldg(a.scal + (gh + a.H) * 4 * kC + 3 * kC);
+            const float gnext = (last || PC) ? 1.0f : __ldg(a.scal + (gh + a.H) * 4 * kC + 3 * kC);
+            float* gvec = reinterpret_cast<float*>(sm + oGam) + ((c + 1) & 1) * kD;
+            if (PC && !last) gvec[r] = __ldg(a.gam + (gh + a.H) * kD + r);  // read after the next group barrier
             if (!last) {
                 const uint4* src = reinterpret_cast<const uint4*>(a.Ut + (gh + a.H) * kD * kC + (long)r * kC);
 #pragma unroll
@@ -916,8 +1144,16 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8)
                             st_sw128_chunk(Sb + (blk >> 1) * 16384, r, (blk & 1) * 4 + c8, f + 8 * c8);
+                        if constexpr (PC) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) f[j] *= gnext;
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 t = *reinterpret_cast<const float4*>(gvec + blk * 32 + j);
+                                f[j] *= t.x; f[j + 1] *= t.y; f[j + 2] *= t.z; f[j + 3] *= t.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) f[j] *= gnext;
+                        }
                         tmem_st32(tS + lrow + blk * 32, v[blk]);
                     }
                 }
@@ -1142,6 +1378,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.scal = reinterpret_cast<float*>(ws + L.off_scal);
     a.Qt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Qt);
     a.Kt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Kt);
+    a.gam = reinterpret_cast<float*>(ws + L.off_gam);
     a.initial_state = p.initial_state; a.final_state = p.final_state;
     a.z = p.z; a.w = p.w; a.eps = p.eps; a.out = p.out; a.out_dtype = p.out_dtype; a.err = p.err;
 
@@ -1160,14 +1397,16 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     chunk_map_kernel<<<1, 1024, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep::kSmem);
+    auto prep_fn = p.g_per_channel ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+    auto state_fn = p.g_per_channel ? chunk_state_kernel<true> : chunk_state_kernel<false>;
+    e = cudaFuncSetAttribute(prep_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep::kSmem);
     if (e != cudaSuccess) return e;
-    chunk_prep_kernel<<<(unsigned)L.nch, prep::kThreads, prep::kSmem, s>>>(mQ, mK, mV, a);
+    prep_fn<<<(unsigned)L.nch, prep::kThreads, prep::kSmem, s>>>(mQ, mK, mV, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmem);
+    e = cudaFuncSetAttribute(state_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmem);
     if (e != cudaSuccess) return e;
-    chunk_state_kernel<<<(unsigned)((long)p.num_seqs * p.H), st::kThreads, st::kSmem, s>>>(mQt, mKt, mW, mAqk, mZ, a);
+    state_fn<<<(unsigned)((long)p.num_seqs * p.H), st::kThreads, st::kSmem, s>>>(mQt, mKt, mW, mAqk, mZ, a);
     return cudaGetLastError();
 }
 
