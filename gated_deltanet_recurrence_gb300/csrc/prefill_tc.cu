@@ -30,6 +30,7 @@
 // Every mbarrier wait is bounded; on a timeout the kernel records GDN_ERR_TIMEOUT and its roles
 // stop issuing work, wait (bounded) for what they issued, free TMEM and return.
 #include <cuda.h>
+#include <stdlib.h>
 #include <cudaTypedefs.h>
 
 #include <cuda_fp16.h>
@@ -50,7 +51,7 @@ constexpr uint64_t kPolls = 2000000000ull;  // bound on any single mbarrier wait
 
 struct WsLayout {
     long nch;          // chunk-head slots = max_chunks * H
-    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, off_gam, total;
+    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, off_gam, off_ready, total;
 };
 
 __host__ __device__ inline long max_chunks(int num_seqs, int total_T) { return (long)total_T / kC + num_seqs; }
@@ -71,6 +72,7 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
     w.off_Qt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^gc qs) Q
     w.off_Kt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^(glast-gc) kinv) K
     w.off_gam = o;   o = al(o + sizeof(float) * w.nch * kD);                // per-channel e^(gc_last)
+    w.off_ready = o; o = al(o + sizeof(int32_t) * w.nch);                  // fused kernel: chunk ready flags
     w.total = o;
     return w;
 }
@@ -96,6 +98,8 @@ struct TcArgs {
     __nv_bfloat16* Qt;
     __nv_bfloat16* Kt;
     float* gam;          // decay per key channel: e^(gc_last) per chunk and channel [nch][128]
+    int32_t* ready;      // fused kernel only: per chunk-head slot, 1 once its entries are written
+    long nch;            // chunk-head slots of the workspace
     const float* initial_state;
     float* final_state;
     const float* z;
@@ -122,18 +126,28 @@ __device__ __forceinline__ bool seq_bounds(const TcArgs& a, int n, long& bos, lo
 
 __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
     __shared__ int32_t part[1024];
+    __shared__ int32_t longest;
     const int tid = threadIdx.x;
+    if (tid == 0) longest = 0;
+    if (a.ready)  // fused kernel: no chunk is ready yet
+        for (long i = tid; i < a.nch; i += 1024) a.ready[i] = 0;
     // per-thread contiguous block of sequences
     const int per = (a.num_seqs + 1023) / 1024;
     const int s0 = tid * per, s1 = min(a.num_seqs, s0 + per);
-    int32_t cnt = 0;
+    int32_t cnt = 0, mx = 0;
     for (int n = s0; n < s1; ++n) {
         long bos, eos;
-        if (seq_bounds(a, n, bos, eos)) cnt += (int32_t)((eos - bos + kC - 1) / kC);
-        else record_error(a.err, GDN_ERR_CU_SEQLENS);
+        if (seq_bounds(a, n, bos, eos)) {
+            const int32_t c = (int32_t)((eos - bos + kC - 1) / kC);
+            cnt += c;
+            mx = max(mx, c);
+        } else {
+            record_error(a.err, GDN_ERR_CU_SEQLENS);
+        }
     }
     part[tid] = cnt;
     __syncthreads();
+    atomicMax(&longest, mx);
     for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan
         int32_t t = tid >= o ? part[tid - o] : 0;
         __syncthreads();
@@ -151,6 +165,8 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
     if (tid == 1023) {
         a.chunk_first[a.num_seqs] = part[1023];
         a.n_chunks[0] = part[1023];
+        a.n_chunks[1] = longest;  // chunks of the longest sequence
+        a.n_chunks[2] = 0;        // fused kernel: work counter of the preparing CTAs
     }
 }
 
@@ -244,7 +260,29 @@ __device__ __forceinline__ void warp_mm16(const float* P, const float* Q, float 
 // substitution (one warp per block, one lane per column); then block rows 1..3 in order,
 // T_bj = -T_bb sum_{k=j}^{b-1} A_bk T_kj, one warp per block (b, j) with the 16x16 products held
 // in registers; X is a per-warp 16 x LD scratch (warps 0-2 only: 3 x 16 x 68 x 4 B = 13 KB).
-__device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid) {
+// Bounded wait (2 s at the top SM clock) for another CTA of the fused kernel to publish a chunk's
+// workspace entries; false when the bound runs out.
+__device__ __forceinline__ bool wait_ready(const int32_t* flag) {
+    if (ld_acquire_gpu(flag)) return true;
+    const long long limit = static_cast<long long>(kPolls) * 21 / 10;
+    const long long t0 = clock64();
+    while (!ld_acquire_gpu(flag)) {
+        __nanosleep(128);
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+// The barrier over the 128 threads that process one chunk: named barrier `id` (and id + 1 inside
+// the triangular solve).  In chunk_prep_kernel these are all the CTA's threads; in the fused kernel
+// one warpgroup, so that two chunks proceed independently in one CTA.
+struct GroupBar {
+    uint32_t id;
+    __device__ __forceinline__ void sync() const { bar_sync(id, 128); }
+    __device__ __forceinline__ bool sync_or(bool p) const { return bar_sync_or(id, 128, p); }
+};
+
+__device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid, GroupBar gb) {
     constexpr int LD = prep::LD, LDA = prep::LDA;
     const int warp = tid >> 5, lane = tid & 31;
     {   // diagonal blocks
@@ -271,7 +309,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
             if (j >= b0 + 16) Tf[(b0 + ii) * LD + j] = 0.f;
         }
     }
-    bar_sync(2, prep::kThreads);
+    bar_sync(gb.id + 1, prep::kThreads);
     float* Xw = X + warp * 16 * LD;
     const int ii = lane >> 1, c0 = (lane & 1) * 8;
     for (int b = 1; b < 4; ++b) {
@@ -292,7 +330,7 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
             for (int e = 0; e < 8; ++e) Tf[(b * 16 + ii) * LD + j * 16 + c0 + e] = -c[e];
             __syncwarp();
         }
-        bar_sync(2, prep::kThreads);
+        bar_sync(gb.id + 1, prep::kThreads);
     }
 }
 
@@ -314,7 +352,7 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 p, float* f) {
 // in global memory or the carried state); after a barrier it reads its 8 raw rows, convolves
 // them and writes them back, so no thread reads a row that another one has overwritten.
 __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, int h, int hk, long bos,
-                                           long t0, int L, int tid) {
+                                           long t0, int L, int tid, GroupBar gb) {
     using namespace prep;
     const int c8 = tid & 7, half = (tid >> 3) & 1, r0 = (tid >> 4) * 8;
     const int x0 = half * 64 + c8 * 8;
@@ -346,7 +384,7 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
                 }
             }
         }
-    __syncthreads();
+    gb.sync();
     if (!live) return;
 #pragma unroll
     for (int ten = 0; ten < 3; ++ten) {
@@ -426,7 +464,8 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
 }
 
 __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t0, int L, int tid,
-                            const float* kinv, const float* qsv, const float* bts, float* Af, float* Tf) {
+                            const float* kinv, const float* qsv, const float* bts, float* Af, float* Tf,
+                            GroupBar gb) {
     using namespace prep;
     float* GT = reinterpret_cast<float*>(sm + pcx::oGT);
     __nv_bfloat16* KT = reinterpret_cast<__nv_bfloat16*>(sm + pcx::oKT);
@@ -461,7 +500,7 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
             }
             a.gam[gh * kD + hf * 64 + tid] = ex2_approx(acc * kLog2e);
         }
-        __syncthreads();
+        gb.sync();
         // (b) raw transposed copies; Q~, K~ rows to the workspace; K . e^G in the K tile
         {
             const int i = tid & 63, hc = tid >> 6;
@@ -495,7 +534,7 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
                 *reinterpret_cast<uint4*>(a.Kt + ro) = pack_bf16x8(ko);
             }
         }
-        __syncthreads();
+        gb.sync();
         // (c) products over this half's 64 channels
         if (off) {
 #pragma unroll 2
@@ -541,7 +580,7 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
             dQ[6] = fmaf(q[3], k30, dQ[6]); dQ[7] = fmaf(q[3], k31, dQ[7]); dQ[8] = fmaf(q[3], k32, dQ[8]);
             dQ[9] = fmaf(q[3], k[3], dQ[9]);
         }
-        __syncthreads();
+        gb.sync();
     }
     // diagonal blocks: sum the 8 channel groups (lanes 8m .. 8m + 7 of one warp)
 #pragma unroll
@@ -576,7 +615,7 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
             Tf[i * LD + j] = qsv[i] * kinv[j] * dQ[e];
         }
     }
-    __syncthreads();
+    gb.sync();
     if (tid >= kC) {  // decayed Q K^T rows to the workspace, zero above the diagonal
         const int i = tid - kC;
         uint4* dst = reinterpret_cast<uint4*>(a.Aqk + gh * kC * kC + (long)i * kC);
@@ -593,62 +632,43 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
     }
 }
 
+// One chunk of one head: everything the state pass needs from it, written to the workspace.  The
+// 128 threads (tid 0..127) synchronise with `gb`; `sm` is this chunk's 1024-aligned shared region,
+// `tm` its 256 TMEM columns, `bars` its two mbarriers, the TMA barrier expected at `tma_parity`.
 template <bool PC>
-__global__ void __launch_bounds__(prep::kThreads, 2)
-chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                  const __grid_constant__ CUtensorMap mV, TcArgs a) {
+__device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* bars, uint32_t tma_parity,
+                                           GroupBar gb, int tid, long gh, const CUtensorMap* mQ,
+                                           const CUtensorMap* mK, const CUtensorMap* mV, const TcArgs& a) {
     using namespace prep;
-    extern __shared__ uint8_t smraw[];
-    // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
-    // keeps the shared address space (plain shared loads and stores, not generic ones)
-    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     float* Af = reinterpret_cast<float*>(sm + oAf);
     float* Tf = reinterpret_cast<float*>(sm + oTf);
     float* gcs = reinterpret_cast<float*>(sm + oSc);
     float* bts = gcs + kC;
     float* kinv = gcs + 2 * kC;
     float* qsv = gcs + 3 * kC;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 16);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long gh = blockIdx.x;  // chunk * H + head
-    const int chunk = (int)(gh / a.H), h = (int)(gh % a.H);
+    const int warp = tid >> 5, lane = tid & 31;
+    const int chunk = (int)(gh / a.H), h = (int)(gh % a.H);  // gh = chunk * H + head
     const int hk = h / (a.H / a.Hk);  // query/key head read by value head h
-    if (chunk >= a.n_chunks[0]) return;
     const int n = a.chunk_seq[chunk];
     long bos, eos;
     seq_bounds(a, n, bos, eos);
     const long t0 = bos + (long)(chunk - a.chunk_first[n]) * kC;
     const int L = (eos - t0 < kC) ? (int)(eos - t0) : kC;
 
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        fence_mbar_init();
-        prefetch_tmap(&mQ);
-        prefetch_tmap(&mK);
-        prefetch_tmap(&mV);
-    }
-    if (warp == 0) {
-        tmem_alloc(tbase, kTmemCols);
-        tmem_relinquish();
-    }
     if (tid < kC) {
         const bool in = tid < L;
         gcs[tid] = (in && !PC) ? a.g[(t0 + tid) * a.H + h] : 0.f;  // per channel: zero here
         bts[tid] = in ? a.beta[(t0 + tid) * a.H + h] : 0.f;
     }
     tc_fence_before();
-    __syncthreads();
+    gb.sync();
     tc_fence_after();
-    const uint32_t tm = *tbase;
     if (tid == 0) {
         mbar_arrive_expect_tx(&bars[0], 49152);
         for (int c = 0; c < 2; ++c) {
-            tma_load_3d(sm + oKQ + c * 16384, &mK, &bars[0], c * 64, hk, (int)t0);
-            tma_load_3d(sm + oKQ + c * 16384 + 8192, &mQ, &bars[0], c * 64, hk, (int)t0);
-            tma_load_3d(sm + oV + c * 8192, &mV, &bars[0], c * 64, h, (int)t0);
+            tma_load_3d(sm + oKQ + c * 16384, mK, &bars[0], c * 64, hk, (int)t0);
+            tma_load_3d(sm + oKQ + c * 16384 + 8192, mQ, &bars[0], c * 64, hk, (int)t0);
+            tma_load_3d(sm + oV + c * 8192, mV, &bars[0], c * 64, h, (int)t0);
         }
     }
     if (warp == 0) {  // inclusive scan of g, two per lane
@@ -663,9 +683,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         gcs[2 * lane] = s - g1;
         gcs[2 * lane + 1] = s;
     }
-    bool ok = mbar_wait(&bars[0], 0, kPolls);
-    if (a.conv.w) {  // fused short convolution of the loaded rows (block-uniform: has a barrier)
-        if (!__syncthreads_or(!ok)) conv_tiles(sm, a, n, h, hk, bos, t0, L, tid);
+    bool ok = mbar_wait(&bars[0], tma_parity, kPolls);
+    if (a.conv.w) {  // fused short convolution of the loaded rows (group-uniform: has a barrier)
+        if (!gb.sync_or(!ok)) conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb);
     }
     if (ok && L < kC) {  // rows past the end of the sequence hold other tokens: zero them
         for (int e = tid; e < (kC - L) * 8 * 5; e += kThreads) {
@@ -682,7 +702,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         }
     }
     if (ok && (a.conv.w || L < kC)) fence_async_smem();  // generic writes, read next by the MMA
-    __syncthreads();
+    gb.sync();
     if (!ok) {
         if (tid == 0) record_error(a.err, GDN_ERR_TIMEOUT);
     } else if (tid == 0) {
@@ -730,9 +750,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             qsv[ii] = a.scale * (a.use_l2 ? rsqrtf(diag + kL2Eps) : 1.0f);
         }
         tc_fence_before();
-        __syncthreads();
+        gb.sync();
         if constexpr (PC) {
-            pc_products(sm, a, gh, h, t0, L, tid, kinv, qsv, bts, Af, Tf);
+            pc_products(sm, a, gh, h, t0, L, tid, kinv, qsv, bts, Af, Tf, gb);
         } else {
         if (tid < kC) {
             const int i = tid;
@@ -747,10 +767,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
             sc[kC + i] = __expf(glast - gi) * kinv[i];
             sc[2 * kC + i] = gi;
             if (i == 0) sc[3 * kC] = __expf(glast);
-        } else {
+        } else {  // decayed Q K^T row, bf16, staged (in the T tile, free until the solve)
             const int i = tid - kC;
             const float gi = gcs[i], f = qsv[i];
-            uint4* dst = reinterpret_cast<uint4*>(a.Aqk + gh * kC * kC + (long)i * kC);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Tf) + i * 128);
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
                 float v[8];
@@ -759,36 +779,45 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                     const int j = c8 * 8 + e;
                     v[e] = j <= i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
                 }
-                dst[c8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                     pack_bf16x2(v[6], v[7]));
+                dst[c8 ^ (i & 7)] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
             }
         }
-        // ---- scaled operand rows for the state pass: K~ = diag(e^(glast-gc) kinv) K (thread i < 64),
-        //      Q~ = diag(e^gc qs) Q (thread 64 + i); one 256-byte row per thread ----
+        // ---- scaled operand rows for the state pass: K~ = diag(e^(glast-gc) kinv) K,
+        //      Q~ = diag(e^gc qs) Q; per-row factors first, then every warp writes whole rows ----
+        float* rowf = Tf + 2048;  // [K~ factors 64 | Q~ factors 64], after the 8 KB staged rows
         {
-            const int i = tid & 63, isq = tid >> 6;
-            const float f = isq ? __expf(gcs[i]) * qsv[i] : __expf(gcs[kC - 1] - gcs[i]) * kinv[i];
-            const uint8_t* src = sm + oKQ + (isq ? 8192 : 0);
-            uint4* dst = reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)i * kD);
+            const int i = tid & 63;
+            rowf[tid] = tid >= kC ? __expf(gcs[i]) * qsv[i] : __expf(gcs[kC - 1] - gcs[i]) * kinv[i];
+        }
+        gb.sync();
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {  // 2 tensors x 64 rows x 16 chunks of 16 B; a warp: 2 rows
+            const int flat = it * kThreads + tid, isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
+            const float f = rowf[isq * kC + r];
+            float v[8];
+            ld_sw128_chunk(sm + oKQ + (isq ? 8192 : 0) + (c16 >> 3) * 16384, r, c16 & 7, v);
 #pragma unroll
-            for (int c16 = 0; c16 < 16; ++c16) {
-                float v[8];
-                ld_sw128_chunk(src + (c16 >> 3) * 16384, i, c16 & 7, v);
+            for (int e = 0; e < 8; ++e) v[e] *= f;
+            *reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)r * kD + c16 * 8) =
+                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                           pack_bf16x2(v[6], v[7]));
+        }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= f;
-                dst[c16] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                      pack_bf16x2(v[6], v[7]));
-            }
+        for (int it = 0; it < 4; ++it) {   // the staged Q K^T rows: 64 rows x 8 chunks; a warp: 4 rows
+            const int flat = it * kThreads + tid, r = flat >> 3, c8 = flat & 7;
+            reinterpret_cast<uint4*>(a.Aqk + gh * kC * kC + (long)r * kC)[c8] =
+                reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(Tf) + r * 128)[c8 ^ (r & 7)];
         }
         }  // per-head decay
         fence_async_smem();  // the K tile may have been rewritten (K . e^G) for the W product
-        __syncthreads();
+        gb.sync();
         // ---- T = (I + A)^-1 (the 16 x 48 fp32 scratch of the block steps lives in the T' tile,
         //      which is written only after the inverse is complete) ----
-        unit_lower_inverse(Af, Tf, reinterpret_cast<float*>(sm + oTP), tid);  // scratch: T' / T'' tiles
+        unit_lower_inverse(Af, Tf, reinterpret_cast<float*>(sm + oTP), tid, gb);  // scratch: T' / T'' tiles
         // ---- T' = T diag(beta e^gc kinv) and T'' = T diag(beta) as bf16 SW128 operand tiles ----
         if (tid < kC) qsv[tid] = bts[tid] * __expf(gcs[tid]) * kinv[tid];  // q factors no longer needed
-        __syncthreads();
+        gb.sync();
         {
             const int i = tid & 63, which = tid >> 6;
             uint8_t* dst = sm + (which ? oTPP : oTP);
@@ -803,7 +832,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        gb.sync();
         if (tid == 0) {
             tc_fence_after();
             const uint32_t kq = smem_u32(sm + oKQ), vv = smem_u32(sm + oV);
@@ -840,25 +869,67 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
                 tmem_ld32(lane_addr + 64, r0);
                 tmem_ld32(lane_addr + 96, r1);
                 tmem_wait_ld();
-                uint4* dst = reinterpret_cast<uint4*>(a.Ut + gh * kD * kC + (long)tid * kC);
+                // U^T row tid (128 B), staged in the T tile (free once T' and T'' are built)
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Tf) + tid * 128);
+                const int sw = tid & 7;
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {
-                    dst[c8] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c8]), __uint_as_float(r0[8 * c8 + 1])),
-                                         pack_bf16x2(__uint_as_float(r0[8 * c8 + 2]), __uint_as_float(r0[8 * c8 + 3])),
-                                         pack_bf16x2(__uint_as_float(r0[8 * c8 + 4]), __uint_as_float(r0[8 * c8 + 5])),
-                                         pack_bf16x2(__uint_as_float(r0[8 * c8 + 6]), __uint_as_float(r0[8 * c8 + 7])));
-                    dst[4 + c8] = make_uint4(pack_bf16x2(__uint_as_float(r1[8 * c8]), __uint_as_float(r1[8 * c8 + 1])),
-                                             pack_bf16x2(__uint_as_float(r1[8 * c8 + 2]), __uint_as_float(r1[8 * c8 + 3])),
-                                             pack_bf16x2(__uint_as_float(r1[8 * c8 + 4]), __uint_as_float(r1[8 * c8 + 5])),
-                                             pack_bf16x2(__uint_as_float(r1[8 * c8 + 6]), __uint_as_float(r1[8 * c8 + 7])));
+                    dst[c8 ^ sw] = make_uint4(pack_bf16x2(__uint_as_float(r0[8 * c8]), __uint_as_float(r0[8 * c8 + 1])),
+                                              pack_bf16x2(__uint_as_float(r0[8 * c8 + 2]), __uint_as_float(r0[8 * c8 + 3])),
+                                              pack_bf16x2(__uint_as_float(r0[8 * c8 + 4]), __uint_as_float(r0[8 * c8 + 5])),
+                                              pack_bf16x2(__uint_as_float(r0[8 * c8 + 6]), __uint_as_float(r0[8 * c8 + 7])));
+                    dst[(4 + c8) ^ sw] = make_uint4(pack_bf16x2(__uint_as_float(r1[8 * c8]), __uint_as_float(r1[8 * c8 + 1])),
+                                                    pack_bf16x2(__uint_as_float(r1[8 * c8 + 2]), __uint_as_float(r1[8 * c8 + 3])),
+                                                    pack_bf16x2(__uint_as_float(r1[8 * c8 + 4]), __uint_as_float(r1[8 * c8 + 5])),
+                                                    pack_bf16x2(__uint_as_float(r1[8 * c8 + 6]), __uint_as_float(r1[8 * c8 + 7])));
                 }
             }
-            __syncthreads();
+            gb.sync();
             const uint4* src = reinterpret_cast<const uint4*>(Wst);
             uint4* dst = reinterpret_cast<uint4*>(a.W + gh * kC * kD);
             for (int e = tid; e < kC * kD / 8; e += kThreads) dst[e] = src[e];
+            const uint4* usrc = reinterpret_cast<const uint4*>(Tf);
+            uint4* udst = reinterpret_cast<uint4*>(a.Ut + gh * kD * kC);
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {  // 128 rows x 8 chunks; a warp writes 4 whole rows
+                const int e = it * kThreads + tid, r = e >> 3;
+                udst[e] = usrc[(r << 3) + ((e & 7) ^ (r & 7))];
+            }
         }
     }
+}
+
+template <bool PC>
+__global__ void __launch_bounds__(prep::kThreads, 2)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                  const __grid_constant__ CUtensorMap mV, TcArgs a) {
+    using namespace prep;
+    extern __shared__ uint8_t smraw[];
+    // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
+    // keeps the shared address space (plain shared loads and stores, not generic ones)
+    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 16);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const long gh = blockIdx.x;  // chunk * H + head
+    if (gh / a.H >= a.n_chunks[0]) return;
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        prefetch_tmap(&mQ);
+        prefetch_tmap(&mK);
+        prefetch_tmap(&mV);
+    }
+    if (warp == 0) {
+        tmem_alloc(tbase, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tbase;
+    prep_chunk<PC>(sm, tm, bars, 0, GroupBar{1}, tid, gh, &mQ, &mK, &mV, a);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -897,22 +968,22 @@ constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns of the state CTA: S [0,128); S W^T (M=128, 64 columns) x 2 buffers [128,256);
 // O = Q~ S^T + Aqk V_new (M=64, rows = tokens, 128 columns) x 2 buffers [256,512).
+// The serial pass of one (sequence, head) unit by the whole CTA (384 threads).  When a.ready is set
+// (fused kernel) the chunks' workspace entries are produced concurrently by other CTAs: the TMA
+// producer and the state epilogue wait for a chunk's ready flag before they read its entries.  The
+// epilogue's read-only-path loads (__ldg) of those entries stay correct there: every entry is
+// first touched after its flag is acquired, each chunk's entries fill whole aligned slots (no
+// cache line holds two chunks), and the SM runs no other CTA, so no stale line can be cached.
 template <bool PC>
-__global__ void __launch_bounds__(st::kThreads, 1)
-chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constant__ CUtensorMap mKt,
-                   const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mAqk,
-                   const __grid_constant__ CUtensorMap mZ, TcArgs a) {
+__device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensorMap* mQt, const CUtensorMap* mKt,
+                                           const CUtensorMap* mW, const CUtensorMap* mAqk,
+                                           const CUtensorMap* mZ, const TcArgs& a) {
     using namespace st;
-    extern __shared__ uint8_t smraw[];
-    // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
-    // keeps the shared address space (plain shared loads and stores, not generic ones)
-    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 8 * NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oBar + 8 * NBAR + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int unit = blockIdx.x;
     const int n = unit / a.H, h = unit % a.H;
     long bos, eos;
     if (!seq_bounds(a, n, bos, eos)) return;  // reported by the chunk map kernel
@@ -949,15 +1020,20 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
                 const int s = c & 1;
                 if (c >= 2 && !mbar_wait(&bars[EMPTY0 + s], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
                 if (*abort_flag) break;
+                const long ghc = (long)(first + c) * a.H + h;
+                if (a.ready) {
+                    if (!wait_ready(a.ready + ghc)) { fail(); break; }
+                    fence_proxy_async_global();  // the entries were written by generic stores
+                }
                 uint8_t* sp = stage_ptr(s);
-                const int row = (int)(((long)(first + c) * a.H + h) * kC);
+                const int row = (int)(ghc * kC);
                 mbar_arrive_expect_tx(&bars[FULL0 + s], kStageTx);
                 for (int ac = 0; ac < 2; ++ac) {
-                    tma_load_2d(sp + sWQ + ac * 16384, &mW, &bars[FULL0 + s], ac * 64, row);
-                    tma_load_2d(sp + sWQ + ac * 16384 + 8192, &mQt, &bars[FULL0 + s], ac * 64, row);
-                    tma_load_2d(sp + sK + ac * 8192, &mKt, &bars[FULL0 + s], ac * 64, row);
+                    tma_load_2d(sp + sWQ + ac * 16384, mW, &bars[FULL0 + s], ac * 64, row);
+                    tma_load_2d(sp + sWQ + ac * 16384 + 8192, mQt, &bars[FULL0 + s], ac * 64, row);
+                    tma_load_2d(sp + sK + ac * 8192, mKt, &bars[FULL0 + s], ac * 64, row);
                 }
-                tma_load_2d(sp + sAqk, &mAqk, &bars[FULL0 + s], 0, row);
+                tma_load_2d(sp + sAqk, mAqk, &bars[FULL0 + s], 0, row);
             }
             // drain: wait until the last issued stages have landed before the CTA may exit
             for (int c = max(0, nck - 2); c < nck; ++c) mbar_wait(&bars[FULL0 + (c & 1)], (c >> 1) & 1, kPolls);
@@ -1022,7 +1098,10 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
         {
             const float* src = a.initial_state ? a.initial_state + ((long)unit * kD + r) * kD : nullptr;
             float* dst = (nck == 0 && a.final_state) ? a.final_state + ((long)unit * kD + r) * kD : nullptr;
-            const float g0 = nck > 0 ? __ldg(a.scal + ((long)first * a.H + h) * 4 * kC + 3 * kC) : 0.f;
+            bool ready0 = true;
+            if (nck > 0 && a.ready) ready0 = wait_ready(a.ready + (long)first * a.H + h);
+            if (!ready0) fail();
+            const float g0 = (nck > 0 && ready0) ? __ldg(a.scal + ((long)first * a.H + h) * 4 * kC + 3 * kC) : 0.f;
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
                 float f[32];
@@ -1045,7 +1124,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
                     const float4* gv = reinterpret_cast<const float4*>(a.gam + ((long)first * a.H + h) * kD + blk * 32);
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        const float4 t = __ldg(gv + j / 4);
+                        const float4 t = ready0 ? __ldg(gv + j / 4) : make_float4(0.f, 0.f, 0.f, 0.f);
                         v[j] = __float_as_uint(t.x * f[j]);
                         v[j + 1] = __float_as_uint(t.y * f[j + 1]);
                         v[j + 2] = __float_as_uint(t.z * f[j + 2]);
@@ -1066,7 +1145,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             }
         }
         uint4 up_next[8];
-        if (nck > 0) {
+        if (nck > 0 && !*abort_flag) {
             const uint4* src = reinterpret_cast<const uint4*>(a.Ut + ((long)first * a.H + h) * kD * kC + (long)r * kC);
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) up_next[c8] = __ldg(src + c8);
@@ -1080,10 +1159,13 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             uint4 up[8];
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) up[c8] = up_next[c8];
-            const float gnext = (last || PC) ? 1.0f : __ldg(a.scal + (gh + a.H) * 4 * kC + 3 * kC);
+            // the next chunk's entries (a failed wait skips them; the group leaves at its next barrier)
+            const bool nready = !last && (!a.ready || wait_ready(a.ready + gh + a.H));
+            if (!last && !nready) fail();
+            const float gnext = (!nready || PC) ? 1.0f : __ldg(a.scal + (gh + a.H) * 4 * kC + 3 * kC);
             float* gvec = reinterpret_cast<float*>(sm + oGam) + ((c + 1) & 1) * kD;
-            if (PC && !last) gvec[r] = __ldg(a.gam + (gh + a.H) * kD + r);  // read after the next group barrier
-            if (!last) {
+            if (PC && nready) gvec[r] = __ldg(a.gam + (gh + a.H) * kD + r);  // read after the next group barrier
+            if (nready) {
                 const uint4* src = reinterpret_cast<const uint4*>(a.Ut + (gh + a.H) * kD * kC + (long)r * kC);
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) up_next[c8] = __ldg(src + c8);
@@ -1187,7 +1269,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
             uint64_t* zb = &bars[ZFULL0 + (cz & 1)];
             mbar_arrive_expect_tx(zb, 32768);
             for (int cb = 0; cb < 4; ++cb)
-                tma_load_3d(sm + oZ + (cz & 1) * 32768 + cb * 8192, &mZ, zb, cb * 32, h, t0z);
+                tma_load_3d(sm + oZ + (cz & 1) * 32768 + cb * 8192, mZ, zb, cb * 32, h, t0z);
         };
         if (a.z && leader) {
             if (nck > 0) issue_z(0);
@@ -1303,6 +1385,116 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
     }
 }
 
+template <bool PC>
+__global__ void __launch_bounds__(st::kThreads, 1)
+chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constant__ CUtensorMap mKt,
+                   const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mAqk,
+                   const __grid_constant__ CUtensorMap mZ, TcArgs a) {
+    extern __shared__ uint8_t smraw[];
+    // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
+    // keeps the shared address space (plain shared loads and stores, not generic ones)
+    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, a);
+}
+
+
+// ---- 4. fused preparation + serial pass (few units) ----------------------------------------------
+//
+// With few (sequence, head) units the serial pass occupies few SMs, yet it can only start after the
+// whole preparation kernel.  The fused kernel runs both in one cooperative launch (one CTA per SM,
+// all resident at once): CTAs 0 .. n_units-1 each run the serial pass of one unit; every other CTA
+// prepares two chunks at a time (one per warpgroup, each with its own shared region, 256 TMEM
+// columns and named barriers), taking chunks from a global counter position by position (the
+// first chunk of every unit, then the second, ...), so the serial passes find their next chunk
+// ready.  A prepared chunk is published by a release store of its flag, which the serial pass
+// acquires (bounded) before reading the chunk's entries.  Preparing CTAs never wait for serial ones.
+namespace fz {
+constexpr uint32_t kPrepStride = (prep::kBytes + 1023u) & ~1023u;
+constexpr uint32_t oTmemBase = 2 * kPrepStride;   // prep role: TMEM base address
+constexpr uint32_t oItem = oTmemBase + 16;        // prep role: work item of each warpgroup
+constexpr uint32_t kPrepBytes = oItem + 16;
+constexpr uint32_t kSmem = st::kSmem > kPrepBytes + 1024 ? st::kSmem : kPrepBytes + 1024;
+static_assert(kSmem <= 232448, "fused kernel shared memory exceeds the per-block limit");
+// register split of the prep role (launched at 168 per thread, 384 x 168 = 64512):
+// two preparing warpgroups at 232 and the third at 40: 2 x 128 x 232 + 128 x 40 = 64512
+constexpr int kRegsPrep = 232, kRegsIdle = 40;
+static_assert(2 * 128 * kRegsPrep + 128 * kRegsIdle <= 384 * 168, "register split above the launch total");
+}  // namespace fz
+
+template <bool PC>
+__global__ void __launch_bounds__(st::kThreads, 1)
+chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                   const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mQt,
+                   const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mW,
+                   const __grid_constant__ CUtensorMap mAqk, const __grid_constant__ CUtensorMap mZ,
+                   TcArgs a, int n_units) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    if ((int)blockIdx.x < n_units) {
+        state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, a);
+        return;
+    }
+    using namespace fz;
+    const int tid = threadIdx.x, warp = tid >> 5, wg = tid >> 7, ltid = tid & 127;
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oTmemBase);
+    volatile long* item_slot = reinterpret_cast<volatile long*>(sm + oItem);
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            uint64_t* b = reinterpret_cast<uint64_t*>(sm + i * kPrepStride + prep::oBar);
+            mbar_init(&b[0], 1);
+            mbar_init(&b[1], 1);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&mQ);
+        prefetch_tmap(&mK);
+        prefetch_tmap(&mV);
+    }
+    if (warp == 0) {
+        tmem_alloc(tbase, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tbase;
+    if (wg < 2) {
+        reg_alloc<kRegsPrep>();
+        uint8_t* smi = sm + wg * kPrepStride;
+        uint64_t* bars = reinterpret_cast<uint64_t*>(smi + prep::oBar);
+        const GroupBar gb{1u + 2u * (uint32_t)wg};
+        const long n_items = (long)a.n_chunks[1] * n_units;
+        uint32_t parity = 0;
+        for (;;) {
+            if (ltid == 0) item_slot[wg] = atomicAdd(&a.n_chunks[2], 1);
+            gb.sync();
+            const long item = item_slot[wg];
+            gb.sync();  // the slot is rewritten only after every thread has read it
+            if (item >= n_items) break;
+            const int pos = (int)(item / n_units), unit = (int)(item % n_units);
+            const int nn = unit / a.H, hh = unit % a.H;
+            const int first = a.chunk_first[nn];
+            if (pos >= a.chunk_first[nn + 1] - first) continue;  // this sequence is shorter
+            const long gh = (long)(first + pos) * a.H + hh;
+            prep_chunk<PC>(smi, tm + (uint32_t)wg * 256u, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a);
+            parity ^= 1u;
+            __threadfence();
+            gb.sync();
+            if (ltid == 0) {
+                fence_proxy_async_global();
+                st_release_gpu(a.ready + gh, 1);
+            }
+        }
+    } else {
+        reg_dealloc<kRegsIdle>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
+}
+
 // ---- host side -----------------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -1394,9 +1586,34 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
         mZ = mQ;  // never dereferenced without a gate
     }
 
-    chunk_map_kernel<<<1, 1024, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    // the fused cooperative kernel serves calls with few (sequence, head) units: at most half the SMs
+    // run serial passes, the rest prepare chunks; GDN_PREFILL_FUSED=0 in the environment turns it off
+    int units = p.num_seqs * p.H, sms = 0, coop = 0, dev = 0, resident = 0;
+    auto fused_fn = p.g_per_channel ? chunk_fused_kernel<true> : chunk_fused_kernel<false>;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
+    const char* env = getenv("GDN_PREFILL_FUSED");
+    bool fused = coop && units <= sms / 2 && !(env && env[0] == '0');
+    if (fused) {
+        e = cudaFuncSetAttribute(fused_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fz::kSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, fused_fn, st::kThreads, fz::kSmem);
+        if (e != cudaSuccess) return e;
+        fused = resident >= 1;
+    }
+    a.nch = L.nch;
+    a.ready = fused ? reinterpret_cast<int32_t*>(ws + L.off_ready) : nullptr;
+
+    chunk_map_kernel<<<1, 1024, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (fused) {  // one CTA per SM, all resident (cooperative launch)
+        void* args[] = {&mQ, &mK, &mV, &mQt, &mKt, &mW, &mAqk, &mZ, &a, &units};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_fn), dim3((unsigned)sms),
+                                           dim3(st::kThreads), args, fz::kSmem, s);
+    }
     auto prep_fn = p.g_per_channel ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
     auto state_fn = p.g_per_channel ? chunk_state_kernel<true> : chunk_state_kernel<false>;
     e = cudaFuncSetAttribute(prep_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep::kSmem);

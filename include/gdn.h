@@ -104,6 +104,10 @@ typedef enum {
  *   out           [total_T, H, d_v], element type out_dtype.
  *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte
  *                 aligned; may be NULL when that size is 0.
+ * With bf16 q/k/v and d = 128, calls with at most (number of SMs) / 2 (sequence, head) pairs run the
+ * chunk preparation and the serial pass as one cooperative launch that occupies every SM; setting
+ * the environment variable GDN_PREFILL_FUSED=0 selects the two-kernel form (same results, bit for
+ * bit).
  */
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int H_k,

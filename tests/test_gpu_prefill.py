@@ -193,3 +193,29 @@ def test_gate_prep_then_prefill_end_to_end():
     o_ref = oracle.gate_rmsnorm_silu(y_ref, inp["z"])
     assert rel_l2_tokens(out.float().cpu(), o_ref, [0, 512, 1024]) <= TOL_BF16
     assert rel_l2_states(Sf.cpu(), S_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("name,kw", [("prefill", {}), ("prefill_kda", {}), ("prefill_conv", {}),
+                                     ("varlen", dict(lengths=[300, 64, 0, 1000, 65], num_seqs=5, H=4))])
+def test_fused_and_two_kernel_paths_agree_bitwise(name, kw, monkeypatch):
+    """Few (sequence, head) units run the fused cooperative kernel (preparation and serial pass at
+    once); GDN_PREFILL_FUSED=0 selects the two-kernel path.  Both run the same arithmetic in the
+    same order, so outputs and final states must be identical bit for bit."""
+    cfg = synthetic.workload(name if name != "varlen" else "varlen", **kw) if kw else synthetic.workload(name)
+    inp = synthetic.prefill_inputs(cfg)
+    g32, b32 = oracle_gates(inp)
+    dev = "cuda"
+    args = [inp[x].to(dev) for x in ("q", "k", "v")] + [g32.to(dev), b32.to(dev)]
+    kwargs = dict(cu_seqlens=inp["cu_seqlens"].to(dev) if inp["cu_seqlens"] is not None else None,
+                  num_seqs=inp["num_seqs"],
+                  initial_state=inp["initial_state"].to(dev) if inp["initial_state"] is not None else None,
+                  conv_weight=inp["conv_weight"].to(dev) if inp.get("conv_weight") is not None else None,
+                  gate_z=inp["z"].to(dev) if inp["z"] is not None else None)
+    outs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("GDN_PREFILL_FUSED", mode)
+        out, Sf = gdn.gdn_chunk_fwd(*args, **kwargs)
+        assert gdn.gdn_get_device_error() == 0
+        outs[mode] = (out.cpu(), Sf.cpu())
+    assert torch.equal(outs["1"][0], outs["0"][0])
+    assert torch.equal(outs["1"][1], outs["0"][1])
