@@ -977,7 +977,7 @@ constexpr uint32_t kTmemCols = 512;
 template <bool PC>
 __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensorMap* mQt, const CUtensorMap* mKt,
                                            const CUtensorMap* mW, const CUtensorMap* mAqk,
-                                           const CUtensorMap* mZ, const TcArgs& a) {
+                                           const CUtensorMap* mZ, const CUtensorMap* mOut, const TcArgs& a) {
     using namespace st;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 8 * NBAR);
@@ -1317,10 +1317,16 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 ok = mbar_wait(&bars[ZFULL0 + (c & 1)], (c >> 1) & 1, kPolls);
                 if (!ok) fail();
                 const float rinv = rsqrtf(ss / kD + a.eps);
+                float4 zz[16];  // all of this lane's z first (independent loads), then the math
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const int col = 64 * half + 4 * c4, cb = col >> 5, ch = (col & 31) >> 2;
+                    zz[c4] = *reinterpret_cast<const float4*>(zt + cb * 8192 + i * 128 + ((ch ^ (i & 7)) << 4));
+                }
 #pragma unroll
                 for (int c4 = 0; c4 < 16; ++c4) {        // columns 64 half + 4 c4 .. + 3
-                    const int col = 64 * half + 4 * c4, cb = col >> 5, ch = (col & 31) >> 2;
-                    const float4 z = *reinterpret_cast<const float4*>(zt + cb * 8192 + i * 128 + ((ch ^ (i & 7)) << 4));
+                    const int col = 64 * half + 4 * c4;
+                    const float4 z = zz[c4];
                     float4 w = make_float4(rinv, rinv, rinv, rinv);
                     if (a.w) {
                         const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w + col));
@@ -1333,11 +1339,29 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                     o[4 * c4 + 3] *= w.w * s23.y;
                 }
             }
-            if (bf16_out) {
-                // stage this half row (128 B) in the chunk's own z buffer, then one warp store per row.
-                // The staged rows overlap z rows of other warps: with a gate, the whole group must
-                // have read its z first; without one the buffer holds no z and each warp only
-                // touches its own staged rows.
+            if (bf16_out && L == kC) {
+                // a full chunk: stage the bf16 rows as two 128-byte-swizzled [64 x 64] boxes in the
+                // chunk's own z buffer (after every row has read its z) and let one thread store
+                // them with the tensor map of the output
+                if (a.z) bar_sync(4, 128);
+                uint8_t* box = zt + half * 8192 + i * 128;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    *reinterpret_cast<uint4*>(box + ((c8 ^ (i & 7)) << 4)) =
+                        make_uint4(pack_bf16x2(o[8 * c8], o[8 * c8 + 1]), pack_bf16x2(o[8 * c8 + 2], o[8 * c8 + 3]),
+                                   pack_bf16x2(o[8 * c8 + 4], o[8 * c8 + 5]), pack_bf16x2(o[8 * c8 + 6], o[8 * c8 + 7]));
+                fence_async_smem();
+                bar_sync(4, 128);
+                if (leader && ok) {
+                    tma_store_3d(mOut, zt, 0, h, (int)t0);
+                    tma_store_3d(mOut, zt + 8192, 64, h, (int)t0);
+                    bulk_commit();
+                }
+            } else if (bf16_out) {
+                // a partial chunk (last of its sequence): stage this half row (128 B) in the chunk's
+                // own z buffer, then one warp store per row inside the sequence.  The staged rows
+                // overlap z rows of other warps: with a gate, the whole group must have read its z
+                // first; without one the buffer holds no z and each warp only touches its own rows.
                 if (a.z) bar_sync(4, 128);
                 else __syncwarp();
                 uint4* dst = reinterpret_cast<uint4*>(zt + i * kStageRow + half * 128);
@@ -1362,13 +1386,20 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 for (int c4 = 0; c4 < 16; ++c4) dst[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
             }
             if (a.z) {
-                // every row has read its z and written its output: the buffer may be refilled
+                // every row has read its z and written its output: the buffer may be refilled once
+                // the tensor store issued from it has read it
                 if (bar_sync_or(4, 128, *abort_flag != 0)) break;
-                if (leader && c + 2 < nck) issue_z(c + 2);
+                if (leader && c + 2 < nck) {
+                    bulk_wait_read();
+                    issue_z(c + 2);
+                }
             } else {
-                __syncwarp();                       // the staged rows are reused two chunks later
+                // the staged rows are reused two chunks later
+                if (bar_sync_or(4, 128, *abort_flag != 0)) break;
+                if (leader) bulk_wait_read();
             }
         }
+        if (leader) bulk_wait_all();  // output tensor stores complete before the CTA exits
         // a z tile still in flight (only after a timeout) must land before the CTA exits; its
         // completion is the one phase nobody waited for, so any completion state will do
         if (a.z && leader && *abort_flag) {
@@ -1389,12 +1420,12 @@ template <bool PC>
 __global__ void __launch_bounds__(st::kThreads, 1)
 chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constant__ CUtensorMap mKt,
                    const __grid_constant__ CUtensorMap mW, const __grid_constant__ CUtensorMap mAqk,
-                   const __grid_constant__ CUtensorMap mZ, TcArgs a) {
+                   const __grid_constant__ CUtensorMap mZ, const __grid_constant__ CUtensorMap mOut, TcArgs a) {
     extern __shared__ uint8_t smraw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
     // keeps the shared address space (plain shared loads and stores, not generic ones)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
-    state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, a);
+    state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, a);
 }
 
 
@@ -1427,11 +1458,11 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mQt,
                    const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mW,
                    const __grid_constant__ CUtensorMap mAqk, const __grid_constant__ CUtensorMap mZ,
-                   TcArgs a, int n_units) {
+                   const __grid_constant__ CUtensorMap mOut, TcArgs a, int n_units) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     if ((int)blockIdx.x < n_units) {
-        state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, a);
+        state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, a);
         return;
     }
     using namespace fz;
@@ -1574,7 +1605,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.initial_state = p.initial_state; a.final_state = p.final_state;
     a.z = p.z; a.w = p.w; a.eps = p.eps; a.out = p.out; a.out_dtype = p.out_dtype; a.err = p.err;
 
-    CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ;
+    CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ, mOut;
     if (!map_tokens(&mQ, p.q, p.total_T, p.Hk) || !map_tokens(&mK, p.k, p.total_T, p.Hk) ||
         !map_tokens(&mV, p.v, p.total_T, p.H) || !map_rows(&mW, a.W, L.nch * kC, kD, 64) ||
         !map_rows(&mAqk, a.Aqk, L.nch * kC, kC, 64) || !map_rows(&mQt, a.Qt, L.nch * kC, kD, 64) ||
@@ -1584,6 +1615,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
         if (!map_z(&mZ, p.z, p.total_T, p.H)) return cudaErrorInvalidValue;
     } else {
         mZ = mQ;  // never dereferenced without a gate
+    }
+    if (p.out_dtype == GDN_BF16) {
+        if (!map_tokens(&mOut, p.out, p.total_T, p.H)) return cudaErrorInvalidValue;
+    } else {
+        mOut = mQ;  // never dereferenced with an fp32 output
     }
 
     // the fused cooperative kernel serves calls with few (sequence, head) units: at most half the SMs
@@ -1610,7 +1646,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (fused) {  // one CTA per SM, all resident (cooperative launch)
-        void* args[] = {&mQ, &mK, &mV, &mQt, &mKt, &mW, &mAqk, &mZ, &a, &units};
+        void* args[] = {&mQ, &mK, &mV, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &a, &units};
         return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_fn), dim3((unsigned)sms),
                                            dim3(st::kThreads), args, fz::kSmem, s);
     }
@@ -1623,7 +1659,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(state_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmem);
     if (e != cudaSuccess) return e;
-    state_fn<<<(unsigned)((long)p.num_seqs * p.H), st::kThreads, st::kSmem, s>>>(mQt, mKt, mW, mAqk, mZ, a);
+    state_fn<<<(unsigned)((long)p.num_seqs * p.H), st::kThreads, st::kSmem, s>>>(mQt, mKt, mW, mAqk, mZ, mOut, a);
     return cudaGetLastError();
 }
 
