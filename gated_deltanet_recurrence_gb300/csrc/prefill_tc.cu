@@ -941,10 +941,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
 // ---- 3. serial state pass ------------------------------------------------------------------------
 
 namespace st {
-constexpr int kThreads = 384;               // 12 warps = 3 warpgroups
-// register split: launched at 168 per thread (384 x 168 = 64512); the producer / MMA warpgroup
-// gives back down to 80 and the two epilogue warpgroups rise to 208: 128 x 80 + 256 x 208 = 63488
-constexpr int kRegsLow = 80, kRegsHigh = 208;
+constexpr int kThreads = 512;               // 16 warps = 4 warpgroups
+// register split: launched at 128 per thread (512 x 128 = 65536); the producer / MMA warpgroup
+// gives back down to 56, the state epilogue rises to 208 and the two output groups settle at 120:
+// 128 x 56 + 128 x 208 + 256 x 120 = 64512
+constexpr int kRegsLow = 56, kRegsHigh = 208, kRegsOut = 120;
+static_assert(128 * kRegsLow + 128 * kRegsHigh + 256 * kRegsOut <= kThreads * 128, "register split");
 constexpr uint32_t oS = 0;                  // S bf16 operand: 2 atom columns x 128 rows = 32 KB
 constexpr uint32_t oA1 = 32768;             // V_new^T bf16 [128 x 64] SW128 = 16 KB
 constexpr uint32_t oStage = 49152;          // two stages
@@ -1086,9 +1088,9 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             }
         }
     }  // warps 2-3: idle
-    } else {
+    } else if (warp < 8) {
     reg_alloc<kRegsHigh>();
-    if (warp < 8) {
+    {
         // ================= state epilogue (serial chain) =================
         const int q4 = warp & 3;               // TMEM lane quarter
         const int r = q4 * 32 + lane;          // state row (d_v index) = TMEM lane
@@ -1248,22 +1250,27 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 if (r == 0) mbar_arrive(&bars[SBF]);
             }
         }
+    }
     } else {
+    reg_dealloc<kRegsOut>();
+    {
         // ================= output epilogue (O and the gate) =================
-        // O has tokens as rows (M = 64): token i lives in TMEM lane 32 (i / 16) + i % 16 of its
-        // warp's quarter.  Lane l < 16 reads its row and hands the upper 64 columns to lane l + 16,
-        // so all 32 lanes gate 64 columns each; the RMS over d_v is a private sum; z comes from a
-        // TMA-filled shared tile; finished rows are staged in that tile and written back with one
-        // coalesced 256-byte store per row.
+        // Two groups of four warps take alternate chunks (group 0: warps 8-11, even chunks; group 1:
+        // warps 12-15, odd chunks), each with its own O buffer, z buffer and named barrier, so a
+        // group has two chunk periods for one chunk.  O has tokens as rows (M = 64): token 16 q + r
+        // lives in TMEM lane 32 q + r of quarter q.  A 16x256b load gives this thread rows
+        // rA = 16 q + lane / 4 and rA + 8 and, in every group of 8 columns, the pair 2 (lane % 4),
+        // 2 (lane % 4) + 1; the four threads of a row add their squares with two shuffles.
+        const int og = (warp - 8) >> 2;
         const int q4 = warp & 3;
-        const int i = q4 * 16 + (lane & 15);   // token row of this lane
-        const int half = lane >> 4;            // columns 64 * half .. 64 * half + 63
+        const int rA = q4 * 16 + (lane >> 2);
+        const int cp = 2 * (lane & 3);
         const uint32_t lrow = static_cast<uint32_t>(q4 * 32) << 16;
+        const uint32_t gbar = 4u + (uint32_t)og;
         const long tok_stride = (long)a.H * kD;
-        const bool leader = (warp == 8 && lane == 0);
+        const bool leader = (q4 == 0 && lane == 0);
         const bool bf16_out = a.out_dtype == GDN_BF16;
-        constexpr int kStageRow = 272;         // staged bf16 row stride in bytes (256 + 16 padding)
-        // z of chunk c goes to buffer c & 1; it is requested two chunks ahead
+        // z of chunk c goes to buffer c & 1 (this group's); it is requested two chunks ahead
         auto issue_z = [&](int cz) {
             const int t0z = (int)(bos + (long)cz * kC);
             uint64_t* zb = &bars[ZFULL0 + (cz & 1)];
@@ -1271,140 +1278,131 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             for (int cb = 0; cb < 4; ++cb)
                 tma_load_3d(sm + oZ + (cz & 1) * 32768 + cb * 8192, mZ, zb, cb * 32, h, t0z);
         };
-        if (a.z && leader) {
-            if (nck > 0) issue_z(0);
-            if (nck > 1) issue_z(1);
-        }
-        for (int c = 0; c < nck; ++c) {
+        if (a.z && leader && og < nck) issue_z(og);
+        for (int c = og; c < nck; c += 2) {
             const int b = c & 1;
             const long t0 = bos + (long)c * kC;
             const int L = (eos - t0 < kC) ? (int)(eos - t0) : kC;
-            uint8_t* zt = sm + oZ + (c & 1) * 32768;
+            uint8_t* zt = sm + oZ + b * 32768;
             bool ok = mbar_wait(&bars[DO_0 + b], (c >> 1) & 1, kPolls);
             if (!ok) fail();
             tc_fence_after();
-            uint32_t v[4][32];
-            float ss = 0.f;
-            {
-                if (ok) {
+            uint32_t v[64];
+            if (ok) {
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.16x256b.x16.b32 "
+                    "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                    "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+                    "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+                    "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+                      "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+                      "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+                      "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
+                      "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
+                      "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+                      "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+                    : "r"(tDO0 + b * 128 + lrow));
+                tmem_wait_ld();
+            } else {
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk) tmem_ld32(tDO0 + b * 128 + blk * 32 + lrow, v[blk]);
-                    tmem_wait_ld();
-                }
-                float part[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) part[e] = 0.f;
-#pragma unroll
-                for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float x = __uint_as_float(v[blk][j]);
-                        part[j & 7] = fmaf(x, x, part[j & 7]);
-                    }
-                ss = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-                ss = __shfl_sync(0xffffffffu, ss, lane & 15);   // lanes >= 16: their row's sum
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {   // lanes >= 16 take the upper 64 columns of lane - 16
-                    const uint32_t up_half = __shfl_up_sync(0xffffffffu, v[2 + (j >> 5)][j & 31], 16);
-                    if (half) v[j >> 5][j & 31] = up_half;
-                }
+                for (int e = 0; e < 64; ++e) v[e] = 0u;
             }
-            float* o = reinterpret_cast<float*>(&v[0][0]);   // this lane's 64 columns (v[0], v[1])
+            float* o = reinterpret_cast<float*>(v);   // o[4 j + {0,1}]: row rA, o[4 j + {2,3}]: row rA + 8
+            float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                sA0 = fmaf(o[4 * j], o[4 * j], sA0);
+                sA1 = fmaf(o[4 * j + 1], o[4 * j + 1], sA1);
+                sB0 = fmaf(o[4 * j + 2], o[4 * j + 2], sB0);
+                sB1 = fmaf(o[4 * j + 3], o[4 * j + 3], sB1);
+            }
+            float ssA = sA0 + sA1, ssB = sB0 + sB1;
+            ssA += __shfl_xor_sync(0xffffffffu, ssA, 1);
+            ssB += __shfl_xor_sync(0xffffffffu, ssB, 1);
+            ssA += __shfl_xor_sync(0xffffffffu, ssA, 2);
+            ssB += __shfl_xor_sync(0xffffffffu, ssB, 2);
             tc_fence_before();
-            if (bar_sync_or(4, 128, *abort_flag != 0)) break;
+            if (bar_sync_or(gbar, 128, *abort_flag != 0)) break;
             if (leader) mbar_arrive(&bars[DOE_0 + b]);
             if (a.z) {
-                ok = mbar_wait(&bars[ZFULL0 + (c & 1)], (c >> 1) & 1, kPolls);
+                ok = mbar_wait(&bars[ZFULL0 + b], (c >> 1) & 1, kPolls);
                 if (!ok) fail();
-                const float rinv = rsqrtf(ss / kD + a.eps);
-                float4 zz[16];  // all of this lane's z first (independent loads), then the math
+                const float rA_inv = rsqrtf(ssA / kD + a.eps), rB_inv = rsqrtf(ssB / kD + a.eps);
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    const int col = 64 * half + 4 * c4, cb = col >> 5, ch = (col & 31) >> 2;
-                    zz[c4] = *reinterpret_cast<const float4*>(zt + cb * 8192 + i * 128 + ((ch ^ (i & 7)) << 4));
-                }
-#pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {        // columns 64 half + 4 c4 .. + 3
-                    const int col = 64 * half + 4 * c4;
-                    const float4 z = zz[c4];
-                    float4 w = make_float4(rinv, rinv, rinv, rinv);
+                for (int j = 0; j < 16; ++j) {
+                    const int col = 8 * j + cp, cb = col >> 5, ch = (col & 31) >> 2, sub = (col & 3) * 4;
+                    const float2 zA = *reinterpret_cast<const float2*>(zt + cb * 8192 + rA * 128 + ((ch ^ (rA & 7)) << 4) + sub);
+                    const float2 zB = *reinterpret_cast<const float2*>(zt + cb * 8192 + (rA + 8) * 128 +
+                                                                       ((ch ^ ((rA + 8) & 7)) << 4) + sub);
+                    float2 wA = make_float2(rA_inv, rA_inv), wB = make_float2(rB_inv, rB_inv);
                     if (a.w) {
-                        const float4 wv = __ldg(reinterpret_cast<const float4*>(a.w + col));
-                        w = make_float4(wv.x * rinv, wv.y * rinv, wv.z * rinv, wv.w * rinv);
+                        const float2 wv = __ldg(reinterpret_cast<const float2*>(a.w + col));
+                        wA = make_float2(wv.x * rA_inv, wv.y * rA_inv);
+                        wB = make_float2(wv.x * rB_inv, wv.y * rB_inv);
                     }
-                    const float2 s01 = fast_silu2(z.x, z.y), s23 = fast_silu2(z.z, z.w);
-                    o[4 * c4] *= w.x * s01.x;
-                    o[4 * c4 + 1] *= w.y * s01.y;
-                    o[4 * c4 + 2] *= w.z * s23.x;
-                    o[4 * c4 + 3] *= w.w * s23.y;
+                    const float2 sA = fast_silu2(zA.x, zA.y), sB = fast_silu2(zB.x, zB.y);
+                    o[4 * j] *= wA.x * sA.x;
+                    o[4 * j + 1] *= wA.y * sA.y;
+                    o[4 * j + 2] *= wB.x * sB.x;
+                    o[4 * j + 3] *= wB.y * sB.y;
                 }
             }
             if (bf16_out && L == kC) {
                 // a full chunk: stage the bf16 rows as two 128-byte-swizzled [64 x 64] boxes in the
                 // chunk's own z buffer (after every row has read its z) and let one thread store
                 // them with the tensor map of the output
-                if (a.z) bar_sync(4, 128);
-                uint8_t* box = zt + half * 8192 + i * 128;
+                if (a.z) bar_sync(gbar, 128);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    *reinterpret_cast<uint4*>(box + ((c8 ^ (i & 7)) << 4)) =
-                        make_uint4(pack_bf16x2(o[8 * c8], o[8 * c8 + 1]), pack_bf16x2(o[8 * c8 + 2], o[8 * c8 + 3]),
-                                   pack_bf16x2(o[8 * c8 + 4], o[8 * c8 + 5]), pack_bf16x2(o[8 * c8 + 6], o[8 * c8 + 7]));
+                for (int j = 0; j < 16; ++j) {
+                    uint8_t* box = zt + (j >> 3) * 8192;
+                    const int cj = j & 7;
+                    *reinterpret_cast<uint32_t*>(box + rA * 128 + ((cj ^ (rA & 7)) << 4) + cp * 2) =
+                        pack_bf16x2(o[4 * j], o[4 * j + 1]);
+                    *reinterpret_cast<uint32_t*>(box + (rA + 8) * 128 + ((cj ^ ((rA + 8) & 7)) << 4) + cp * 2) =
+                        pack_bf16x2(o[4 * j + 2], o[4 * j + 3]);
+                }
                 fence_async_smem();
-                bar_sync(4, 128);
+                bar_sync(gbar, 128);
                 if (leader && ok) {
                     tma_store_3d(mOut, zt, 0, h, (int)t0);
                     tma_store_3d(mOut, zt + 8192, 64, h, (int)t0);
                     bulk_commit();
                 }
-            } else if (bf16_out) {
-                // a partial chunk (last of its sequence): stage this half row (128 B) in the chunk's
-                // own z buffer, then one warp store per row inside the sequence.  The staged rows
-                // overlap z rows of other warps: with a gate, the whole group must have read its z
-                // first; without one the buffer holds no z and each warp only touches its own rows.
-                if (a.z) bar_sync(4, 128);
-                else __syncwarp();
-                uint4* dst = reinterpret_cast<uint4*>(zt + i * kStageRow + half * 128);
+            } else if (ok) {
+                // a partial chunk (the last of its sequence) or an fp32 output: the rows inside the
+                // sequence are written directly, two columns per store
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    dst[c8] = make_uint4(pack_bf16x2(o[8 * c8], o[8 * c8 + 1]), pack_bf16x2(o[8 * c8 + 2], o[8 * c8 + 3]),
-                                         pack_bf16x2(o[8 * c8 + 4], o[8 * c8 + 5]), pack_bf16x2(o[8 * c8 + 6], o[8 * c8 + 7]));
-                __syncwarp();
-#pragma unroll 4
-                for (int rr = 0; rr < 16; ++rr) {
-                    const int row = q4 * 16 + rr;
-                    if (ok && row < L) {
-                        const uint2 val = *reinterpret_cast<const uint2*>(zt + row * kStageRow + 8 * lane);
-                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (t0 + row) * tok_stride +
-                                                  (long)h * kD + 4 * lane) = val;
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int r = rA + 8 * hr;
+                    if (r < L) {
+                        const long base = (t0 + r) * tok_stride + (long)h * kD + cp;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float x0 = o[4 * j + 2 * hr], x1 = o[4 * j + 2 * hr + 1];
+                            if (bf16_out)
+                                *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + base + 8 * j) =
+                                    pack_bf16x2(x0, x1);
+                            else
+                                *reinterpret_cast<float2*>(static_cast<float*>(a.out) + base + 8 * j) = make_float2(x0, x1);
+                        }
                     }
                 }
-            } else if (ok && i < L) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + (t0 + i) * tok_stride +
-                                                        (long)h * kD + 64 * half);
-#pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) dst[c4] = make_float4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
             }
-            if (a.z) {
-                // every row has read its z and written its output: the buffer may be refilled once
-                // the tensor store issued from it has read it
-                if (bar_sync_or(4, 128, *abort_flag != 0)) break;
-                if (leader && c + 2 < nck) {
-                    bulk_wait_read();
-                    issue_z(c + 2);
-                }
-            } else {
-                // the staged rows are reused two chunks later
-                if (bar_sync_or(4, 128, *abort_flag != 0)) break;
-                if (leader) bulk_wait_read();
+            // every row has read its z and written its output: the buffers may be reused once the
+            // tensor store issued from the z buffer has read it
+            if (bar_sync_or(gbar, 128, *abort_flag != 0)) break;
+            if (leader) {
+                bulk_wait_read();
+                if (a.z && c + 2 < nck) issue_z(c + 2);
             }
         }
         if (leader) bulk_wait_all();  // output tensor stores complete before the CTA exits
         // a z tile still in flight (only after a timeout) must land before the CTA exits; its
         // completion is the one phase nobody waited for, so any completion state will do
         if (a.z && leader && *abort_flag) {
-            for (int zb = 0; zb < 2; ++zb)
-                for (int ph = 0; ph < 2; ++ph) mbar_wait(&bars[ZFULL0 + zb], ph, 1000000u);
+            for (int ph = 0; ph < 2; ++ph) mbar_wait(&bars[ZFULL0 + og], ph, 1000000u);
         }
     }
     }  // epilogue warpgroups
@@ -1446,10 +1444,10 @@ constexpr uint32_t oItem = oTmemBase + 16;        // prep role: work item of eac
 constexpr uint32_t kPrepBytes = oItem + 16;
 constexpr uint32_t kSmem = st::kSmem > kPrepBytes + 1024 ? st::kSmem : kPrepBytes + 1024;
 static_assert(kSmem <= 232448, "fused kernel shared memory exceeds the per-block limit");
-// register split of the prep role (launched at 168 per thread, 384 x 168 = 64512):
-// two preparing warpgroups at 232 and the third at 40: 2 x 128 x 232 + 128 x 40 = 64512
-constexpr int kRegsPrep = 232, kRegsIdle = 40;
-static_assert(2 * 128 * kRegsPrep + 128 * kRegsIdle <= 384 * 168, "register split above the launch total");
+// register split of the prep role (launched at 128 per thread, 512 x 128 = 65536):
+// two preparing warpgroups at 232 and the other two at 24: 2 x 128 x 232 + 2 x 128 x 24 = 65536
+constexpr int kRegsPrep = 232, kRegsIdle = 24;
+static_assert(2 * 128 * kRegsPrep + 2 * 128 * kRegsIdle <= st::kThreads * 128, "register split above the launch total");
 }  // namespace fz
 
 template <bool PC>
