@@ -754,12 +754,15 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
         if constexpr (PC) {
             pc_products(sm, a, gh, h, t0, L, tid, kinv, qsv, bts, Af, Tf, gb);
         } else {
+        // every element is formed in registers first (the loop has no stores, so its shared loads
+        // pipeline), then the row is stored
         if (tid < kC) {
             const int i = tid;
             const float gi = gcs[i], f = bts[i] * kinv[i];
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                Af[i * LDA + j] = j < i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
+            for (int j = 0; j < 64; ++j) row[j] = j < i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) Af[i * LDA + j] = row[j];
             // per-token factors for the state pass
             float* sc = a.scal + gh * 4 * kC;
             const float glast = gcs[kC - 1];
@@ -772,16 +775,11 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
             const float gi = gcs[i], f = qsv[i];
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Tf) + i * 128);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                float v[8];
+            for (int j = 0; j < 64; ++j) row[j] = j <= i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = c8 * 8 + e;
-                    v[e] = j <= i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
-                }
-                dst[c8 ^ (i & 7)] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-            }
+            for (int c8 = 0; c8 < 8; ++c8)
+                dst[c8 ^ (i & 7)] = make_uint4(pack_bf16x2(row[8 * c8], row[8 * c8 + 1]), pack_bf16x2(row[8 * c8 + 2], row[8 * c8 + 3]),
+                                               pack_bf16x2(row[8 * c8 + 4], row[8 * c8 + 5]), pack_bf16x2(row[8 * c8 + 6], row[8 * c8 + 7]));
         }
         // ---- scaled operand rows for the state pass: K~ = diag(e^(glast-gc) kinv) K,
         //      Q~ = diag(e^gc qs) Q; per-row factors first, then every warp writes whole rows ----
@@ -791,17 +789,30 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
             rowf[tid] = tid >= kC ? __expf(gcs[i]) * qsv[i] : __expf(gcs[kC - 1] - gcs[i]) * kinv[i];
         }
         gb.sync();
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {  // 2 tensors x 64 rows x 16 chunks of 16 B; a warp: 2 rows
-            const int flat = it * kThreads + tid, isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
-            const float f = rowf[isq * kC + r];
-            float v[8];
-            ld_sw128_chunk(sm + oKQ + (isq ? 8192 : 0) + (c16 >> 3) * 16384, r, c16 & 7, v);
+        // 2 tensors x 64 rows x 16 chunks of 16 B; a warp covers 2 whole rows.  Four chunks are
+        // read from the tiles before any of them is written to the workspace.
+#pragma unroll 1
+        for (int it0 = 0; it0 < 16; it0 += 4) {
+            uint4 raw[4];
+            float fr[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] *= f;
-            *reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)r * kD + c16 * 8) =
-                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                           pack_bf16x2(v[6], v[7]));
+            for (int u = 0; u < 4; ++u) {
+                const int flat = (it0 + u) * kThreads + tid, isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
+                raw[u] = *reinterpret_cast<const uint4*>(sm + oKQ + (isq ? 8192 : 0) + (c16 >> 3) * 16384 +
+                                                         sw128_offset(r, (c16 & 7) * 8));
+                fr[u] = rowf[isq * kC + r];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int flat = (it0 + u) * kThreads + tid, isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
+                float v[8];
+                unpack_bf16x8(raw[u], v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= fr[u];
+                *reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)r * kD + c16 * 8) =
+                    make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                               pack_bf16x2(v[6], v[7]));
+            }
         }
 #pragma unroll
         for (int it = 0; it < 4; ++it) {   // the staged Q K^T rows: 64 rows x 8 chunks; a warp: 4 rows
