@@ -226,17 +226,21 @@ namespace prep {
 constexpr int kThreads = 128;
 constexpr int LDA = kC + 1;  // A (fp32 64x64): odd stride, conflict-free row/column access
 constexpr int LD = kC + 4;   // T and the block scratch: rows stay 16-byte aligned for float4 loads
-constexpr uint32_t oKQ = 0;          // 2 atom columns x (K rows 0-63, Q rows 64-127) = 32 KB
-constexpr uint32_t oV = 32768;       // 2 atom columns x 64 rows = 16 KB
-constexpr uint32_t oTP = 49152;      // T' (bf16 SW128 64x64) 8 KB
-constexpr uint32_t oTPP = 57344;     // T'' 8 KB
-constexpr uint32_t oAf = 65536;      // A (fp32 64 x 65); later the W staging tile (bf16 64x128)
+// Three chunks fit on one SM (68 KB of shared memory, 128 TMEM columns, <= 168 registers each).
+// Regions are reused as the chunk proceeds:
+constexpr uint32_t oKQ = 0;          // 2 atom columns x (K rows 0-63, Q rows 64-127) = 32 KB; once Q
+                                     // is no longer read, V is loaded into Q's rows (MN-block stride 16 KB)
+constexpr uint32_t oV = oKQ + 8192;  // V's first 64-column half (the second is 16 KB further)
+constexpr uint32_t oAf = 32768;      // A (fp32 64 x 65); after the solve T' and T'' (bf16 SW128 64x64,
+constexpr uint32_t oTP = oAf;        // 8 KB each); after the W / U^T product the W staging tile
+constexpr uint32_t oTPP = oAf + 8192;
 constexpr uint32_t oTf = oAf + 16896;             // T (fp32 64 x 68), 1 KB past A
 constexpr uint32_t oSc = oTf + 4 * kC * LD;       // gc, beta, kinv, qs (fp32 x 64 each)
-constexpr uint32_t oBar = oSc + 4 * 4 * kC;       // 2 mbarriers + TMEM base
+constexpr uint32_t oBar = oSc + 4 * 4 * kC;       // 3 mbarriers (K and Q, products, V) + TMEM base
 constexpr uint32_t kBytes = oBar + 64;
 constexpr uint32_t kSmem = kBytes + 1024;          // + alignment slack
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 128;                // the Gram product, then W^T and U^T
+static_assert(3 * kSmem <= 232448, "three chunks per SM");
 }  // namespace prep
 
 // C[16 x 16] (+)= P[16 x 16] Q[16 x 16] for one warp: lane l owns row l / 2 and the 8 columns
@@ -282,7 +286,7 @@ struct GroupBar {
     __device__ __forceinline__ bool sync_or(bool p) const { return bar_sync_or(id, 128, p); }
 };
 
-__device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid, GroupBar gb) {
+__device__ void unit_lower_inverse(const float* Af, float* Tf, int tid, GroupBar gb) {
     constexpr int LD = prep::LD, LDA = prep::LDA;
     const int warp = tid >> 5, lane = tid & 31;
     {   // diagonal blocks
@@ -310,25 +314,27 @@ __device__ void unit_lower_inverse(const float* Af, float* Tf, float* X, int tid
         }
     }
     bar_sync(gb.id + 1, prep::kThreads);
-    float* Xw = X + warp * 16 * LD;
     const int ii = lane >> 1, c0 = (lane & 1) * 8;
     for (int b = 1; b < 4; ++b) {
         const int j = warp;  // block column handled by this warp (warps j >= b idle in this row)
         if (j < b) {
+            // Y = sum_k A_bk T_kj goes to the block T_bj itself (no other warp reads it in this
+            // step), then T_bj = -T_bb Y is formed in registers and written over it
+            float* Tbj = Tf + (b * 16) * LD + j * 16;
             float c[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) c[e] = 0.f;
             for (int k = j; k < b; ++k)
                 warp_mm16<LDA, LD>(Af + (b * 16) * LDA + k * 16, Tf + (k * 16) * LD + j * 16, c, lane);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) Xw[ii * LD + c0 + e] = c[e];
+            for (int e = 0; e < 8; ++e) Tbj[ii * LD + c0 + e] = c[e];
             __syncwarp();
 #pragma unroll
             for (int e = 0; e < 8; ++e) c[e] = 0.f;
-            warp_mm16<LD, LD>(Tf + (b * 16) * LD + b * 16, Xw, c, lane);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Tf[(b * 16 + ii) * LD + j * 16 + c0 + e] = -c[e];
+            warp_mm16<LD, LD>(Tf + (b * 16) * LD + b * 16, Tbj, c, lane);
             __syncwarp();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) Tbj[ii * LD + c0 + e] = -c[e];
         }
         bar_sync(gb.id + 1, prep::kThreads);
     }
@@ -344,79 +350,74 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 p, float* f) {
     }
 }
 
-// Short convolution + SiLU ("因果卷积") of the loaded Q, K, V tiles (128B-swizzled bf16), in place,
-// rows 0..L-1 of the chunk starting at token t0.  Thread tid owns 8 consecutive channels (one
-// 16-byte chunk: c8 = tid % 8 of column half (tid / 8) % 2) and 8 rows (segment tid / 16) of each
-// tile, so a quarter-warp reads or writes one whole 128-byte row.  Every thread first captures the
+// Short convolution + SiLU ("因果卷积") of one loaded tile (ten 0: Q, 1: K, 2: V; 128B-swizzled
+// bf16), in place, rows 0..L-1 of the chunk starting at token t0.  Thread tid owns 8 consecutive
+// channels (one 16-byte chunk: c8 = tid % 8 of column half (tid / 8) % 2) and 8 rows (segment
+// tid / 16), so a quarter-warp reads or writes one whole 128-byte row.  Every thread first captures the
 // three raw rows before its segment (from the tile, or, for the first segment, from the sequence
 // in global memory or the carried state); after a barrier it reads its 8 raw rows, convolves
 // them and writes them back, so no thread reads a row that another one has overwritten.
 __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, int h, int hk, long bos,
-                                           long t0, int L, int tid, GroupBar gb) {
+                                           long t0, int L, int tid, GroupBar gb, int ten) {
     using namespace prep;
     const int c8 = tid & 7, half = (tid >> 3) & 1, r0 = (tid >> 4) * 8;
     const int x0 = half * 64 + c8 * 8;
-    uint8_t* tiles[3] = {sm + oKQ + half * 16384 + 8192, sm + oKQ + half * 16384, sm + oV + half * 8192};
-    const __nv_bfloat16* srcs[3] = {a.q + hk * kD + x0, a.k + hk * kD + x0, a.v + (long)h * kD + x0};
-    const long strides[3] = {(long)a.Hk * kD, (long)a.Hk * kD, (long)a.H * kD};
-    const int chans[3] = {hk * kD + x0, a.Hk * kD + hk * kD + x0, 2 * a.Hk * kD + h * kD + x0};
+    // ten 0: Q, 1: K, 2: V (V occupies Q's rows once Q is no longer needed)
+    uint8_t* tile = sm + oKQ + half * 16384 + (ten == 1 ? 0 : 8192);
+    const __nv_bfloat16* src = ten == 0 ? a.q + hk * kD + x0 : (ten == 1 ? a.k + hk * kD + x0 : a.v + (long)h * kD + x0);
+    const long stride = ten == 2 ? (long)a.H * kD : (long)a.Hk * kD;
+    const int chan = ten == 0 ? hk * kD + x0 : (ten == 1 ? a.Hk * kD + hk * kD + x0 : 2 * a.Hk * kD + h * kD + x0);
     const bool live = r0 < L;
-    float hist[3][3][8];
+    float hist[3][8];
 #pragma unroll
-    for (int ten = 0; ten < 3; ++ten)
+    for (int j = 0; j < 3; ++j) {
+        const int r = r0 - 3 + j;
+        float* f = hist[j];
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            const int r = r0 - 3 + j;
-            float* f = hist[ten][j];
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        if (!live) continue;
+        if (r >= 0) {
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(tile + sw128_offset(r, c8 * 8)), f);
+        } else {
+            const long t = t0 + r;
+            if (t >= bos) {
+                unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + t * stride)), f);
+            } else if (a.conv.state_in) {
+                const float* st = a.conv.state_in + ((long)n * a.conv.dim + chan) * 3 + 3 + (t - bos);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            if (!live) continue;
-            if (r >= 0) {
-                unpack_bf16x8(*reinterpret_cast<const uint4*>(tiles[ten] + sw128_offset(r, c8 * 8)), f);
-            } else {
-                const long t = t0 + r;
-                if (t >= bos) {
-                    unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(srcs[ten] + t * strides[ten])), f);
-                } else if (a.conv.state_in) {
-                    const float* st = a.conv.state_in + ((long)n * a.conv.dim + chans[ten]) * 3 + 3 + (t - bos);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = st[e * 3];
-                }
+                for (int e = 0; e < 8; ++e) f[e] = st[e * 3];
             }
         }
+    }
     gb.sync();
     if (!live) return;
+    uint4 raw[8];
 #pragma unroll
-    for (int ten = 0; ten < 3; ++ten) {
-        uint4 raw[8];
+    for (int i = 0; i < 8; ++i)
+        raw[i] = r0 + i < L ? *reinterpret_cast<const uint4*>(tile + sw128_offset(r0 + i, c8 * 8)) : make_uint4(0, 0, 0, 0);
+    float4 w[8];
+    const float4* w4 = reinterpret_cast<const float4*>(a.conv.w) + chan;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            raw[i] = r0 + i < L ? *reinterpret_cast<const uint4*>(tiles[ten] + sw128_offset(r0 + i, c8 * 8))
-                                : make_uint4(0, 0, 0, 0);
-        float4 w[8];
-        const float4* w4 = reinterpret_cast<const float4*>(a.conv.w) + chans[ten];
+    for (int e = 0; e < 8; ++e) w[e] = __ldg(w4 + e);
+    float* h0 = hist[0];
+    float* h1 = hist[1];
+    float* h2 = hist[2];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = __ldg(w4 + e);
-        float* h0 = hist[ten][0];
-        float* h1 = hist[ten][1];
-        float* h2 = hist[ten][2];
+    for (int i = 0; i < 8; ++i) {
+        float x[8];
+        unpack_bf16x8(raw[i], x);
+        uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float x[8];
-            unpack_bf16x8(raw[i], x);
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float y0 = fast_silu(fmaf(w[e].w, x[e], fmaf(w[e].z, h2[e], fmaf(w[e].y, h1[e], w[e].x * h0[e]))));
-                const float y1 = fast_silu(fmaf(w[e + 1].w, x[e + 1],
-                                                fmaf(w[e + 1].z, h2[e + 1], fmaf(w[e + 1].y, h1[e + 1], w[e + 1].x * h0[e + 1]))));
-                o[e / 2] = pack_bf16x2(y0, y1);
-            }
-            if (r0 + i < L)
-                *reinterpret_cast<uint4*>(tiles[ten] + sw128_offset(r0 + i, c8 * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { h0[e] = h1[e]; h1[e] = h2[e]; h2[e] = x[e]; }
+        for (int e = 0; e < 8; e += 2) {
+            const float y0 = fast_silu(fmaf(w[e].w, x[e], fmaf(w[e].z, h2[e], fmaf(w[e].y, h1[e], w[e].x * h0[e]))));
+            const float y1 = fast_silu(fmaf(w[e + 1].w, x[e + 1],
+                                            fmaf(w[e + 1].z, h2[e + 1], fmaf(w[e + 1].y, h1[e + 1], w[e + 1].x * h0[e + 1]))));
+            o[e / 2] = pack_bf16x2(y0, y1);
         }
+        if (r0 + i < L)
+            *reinterpret_cast<uint4*>(tile + sw128_offset(r0 + i, c8 * 8)) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { h0[e] = h1[e]; h1[e] = h2[e]; h2[e] = x[e]; }
     }
 }
 
@@ -438,8 +439,8 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
 // K . e^G, the operand of W = T diag(beta kinv) (K . e^G).
 namespace pcx {
 constexpr int LDG = 68;                      // G^T row stride (floats): [channel][row], 16-byte rows
-constexpr int LDK = 68;                      // K^T, Q^T row stride (bf16): 136 bytes
-constexpr uint32_t oGT = prep::oTP;
+constexpr int LDK = 64;                      // K^T, Q^T row stride (bf16): 128 bytes
+constexpr uint32_t oGT = prep::oAf;
 constexpr uint32_t oKT = oGT + 64 * LDG * 4;
 constexpr uint32_t oQT = oKT + 64 * LDK * 2;
 constexpr uint32_t kEnd = oQT + 64 * LDK * 2;
@@ -664,11 +665,10 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
     gb.sync();
     tc_fence_after();
     if (tid == 0) {
-        mbar_arrive_expect_tx(&bars[0], 49152);
+        mbar_arrive_expect_tx(&bars[0], 32768);
         for (int c = 0; c < 2; ++c) {
             tma_load_3d(sm + oKQ + c * 16384, mK, &bars[0], c * 64, hk, (int)t0);
             tma_load_3d(sm + oKQ + c * 16384 + 8192, mQ, &bars[0], c * 64, hk, (int)t0);
-            tma_load_3d(sm + oV + c * 8192, mV, &bars[0], c * 64, h, (int)t0);
         }
     }
     if (warp == 0) {  // inclusive scan of g, two per lane
@@ -684,21 +684,18 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
         gcs[2 * lane + 1] = s;
     }
     bool ok = mbar_wait(&bars[0], tma_parity, kPolls);
-    if (a.conv.w) {  // fused short convolution of the loaded rows (group-uniform: has a barrier)
-        if (!gb.sync_or(!ok)) conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb);
+    if (a.conv.w) {  // fused short convolution of the loaded rows (group-uniform: has barriers)
+        if (!gb.sync_or(!ok)) {
+            conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb, 0);
+            conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb, 1);
+        }
     }
     if (ok && L < kC) {  // rows past the end of the sequence hold other tokens: zero them
-        for (int e = tid; e < (kC - L) * 8 * 5; e += kThreads) {
-            const int r = L + e / 40, part = e % 40;  // 5 tiles x 8 chunks of 16 B
+        for (int e = tid; e < (kC - L) * 8 * 4; e += kThreads) {
+            const int r = L + e / 32, part = e % 32;  // 4 tiles (K, Q x 2 halves) x 8 chunks of 16 B
             const int tile = part / 8, ch = part % 8;
-            uint8_t* base = tile < 2 ? sm + oKQ + tile * 16384 : (tile < 4 ? sm + oKQ + (tile - 2) * 16384 + 8192
-                                                                            : nullptr);
-            if (tile == 4) {
-                *reinterpret_cast<uint4*>(sm + oV + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + oV + 8192 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-            } else {
-                *reinterpret_cast<uint4*>(base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-            }
+            *reinterpret_cast<uint4*>(sm + oKQ + (tile & 1) * 16384 + (tile >> 1) * 8192 + r * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
         }
     }
     if (ok && (a.conv.w || L < kC)) fence_async_smem();  // generic writes, read next by the MMA
@@ -823,9 +820,14 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
         }  // per-head decay
         fence_async_smem();  // the K tile may have been rewritten (K . e^G) for the W product
         gb.sync();
-        // ---- T = (I + A)^-1 (the 16 x 48 fp32 scratch of the block steps lives in the T' tile,
-        //      which is written only after the inverse is complete) ----
-        unit_lower_inverse(Af, Tf, reinterpret_cast<float*>(sm + oTP), tid, gb);  // scratch: T' / T'' tiles
+        // Q is no longer read: V comes into its rows while the triangular solve runs
+        if (tid == 0) {
+            fence_async_smem();
+            mbar_arrive_expect_tx(&bars[2], 16384);
+            for (int c = 0; c < 2; ++c) tma_load_3d(sm + oV + c * 16384, mV, &bars[2], c * 64, h, (int)t0);
+        }
+        // ---- T = (I + A)^-1 ----
+        unit_lower_inverse(Af, Tf, tid, gb);
         // ---- T' = T diag(beta e^gc kinv) and T'' = T diag(beta) as bf16 SW128 operand tiles ----
         if (tid < kC) qsv[tid] = bts[tid] * __expf(gcs[tid]) * kinv[tid];  // q factors no longer needed
         gb.sync();
@@ -841,10 +843,21 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
                 st_sw128_chunk(dst, i, c8, v);
             }
         }
+        // V: landed, convolved, rows past the sequence zeroed
+        const bool okv = mbar_wait(&bars[2], tma_parity, kPolls);
+        if (a.conv.w && !gb.sync_or(!okv)) conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb, 2);
+        if (okv && L < kC) {
+            for (int e = tid; e < (kC - L) * 8 * 2; e += kThreads) {
+                const int r = L + e / 16, part = e % 16;
+                *reinterpret_cast<uint4*>(sm + oV + (part >> 3) * 16384 + r * 128 + (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+        }
         fence_async_smem();
         tc_fence_before();
-        gb.sync();
-        if (tid == 0) {
+        const bool vfail = gb.sync_or(!okv);
+        if (vfail) {
+            if (tid == 0) record_error(a.err, GDN_ERR_TIMEOUT);
+        } else if (tid == 0) {
             tc_fence_after();
             const uint32_t kq = smem_u32(sm + oKQ), vv = smem_u32(sm + oV);
             const uint32_t tp = smem_u32(sm + oTP), tpp = smem_u32(sm + oTPP);
@@ -852,11 +865,11 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
                 mma_bf16_ss(tm + 0, sdesc_sw128(kq + k * 2048, 16384, 1024), sdesc_sw128(tp + k * 32, 16, 1024),
                             idesc_bf16(128, 64, 1, 0), k > 0);
             for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tm + 64, sdesc_sw128(vv + k * 2048, 8192, 1024), sdesc_sw128(tpp + k * 32, 16, 1024),
+                mma_bf16_ss(tm + 64, sdesc_sw128(vv + k * 2048, 16384, 1024), sdesc_sw128(tpp + k * 32, 16, 1024),
                             idesc_bf16(128, 64, 1, 0), k > 0);
             mma_commit(&bars[1]);
         }
-        const bool ok2 = mbar_wait(&bars[1], 1, kPolls);
+        const bool ok2 = !vfail && mbar_wait(&bars[1], 1, kPolls);
         tc_fence_after();
         if (!ok2) {
             if (tid == 0) record_error(a.err, GDN_ERR_TIMEOUT);
@@ -911,7 +924,7 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
 }
 
 template <bool PC>
-__global__ void __launch_bounds__(prep::kThreads, 2)
+__global__ void __launch_bounds__(prep::kThreads, 3)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                   const __grid_constant__ CUtensorMap mV, TcArgs a) {
     using namespace prep;
@@ -920,13 +933,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     // keeps the shared address space (plain shared loads and stores, not generic ones)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 16);
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 32);
     const int tid = threadIdx.x, warp = tid >> 5;
     const long gh = blockIdx.x;  // chunk * H + head
     if (gh / a.H >= a.n_chunks[0]) return;
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         prefetch_tmap(&mQ);
         prefetch_tmap(&mK);
@@ -1443,22 +1455,24 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
 // With few (sequence, head) units the serial pass occupies few SMs, yet it can only start after the
 // whole preparation kernel.  The fused kernel runs both in one cooperative launch (one CTA per SM,
 // all resident at once): CTAs 0 .. n_units-1 each run the serial pass of one unit; every other CTA
-// prepares two chunks at a time (one per warpgroup, each with its own shared region, 256 TMEM
+// prepares three chunks at a time (one per warpgroup, each with its own shared region, 128 TMEM
 // columns and named barriers), taking chunks from a global counter position by position (the
 // first chunk of every unit, then the second, ...), so the serial passes find their next chunk
 // ready.  A prepared chunk is published by a release store of its flag, which the serial pass
 // acquires (bounded) before reading the chunk's entries.  Preparing CTAs never wait for serial ones.
 namespace fz {
 constexpr uint32_t kPrepStride = (prep::kBytes + 1023u) & ~1023u;
-constexpr uint32_t oTmemBase = 2 * kPrepStride;   // prep role: TMEM base address
+constexpr int kInst = 3;                          // chunk preparations per preparing CTA
+constexpr uint32_t oTmemBase = kInst * kPrepStride;  // prep role: TMEM base address
 constexpr uint32_t oItem = oTmemBase + 16;        // prep role: work item of each warpgroup
-constexpr uint32_t kPrepBytes = oItem + 16;
+constexpr uint32_t kPrepBytes = oItem + 8 * kInst;
 constexpr uint32_t kSmem = st::kSmem > kPrepBytes + 1024 ? st::kSmem : kPrepBytes + 1024;
 static_assert(kSmem <= 232448, "fused kernel shared memory exceeds the per-block limit");
 // register split of the prep role (launched at 128 per thread, 512 x 128 = 65536):
-// two preparing warpgroups at 232 and the other two at 24: 2 x 128 x 232 + 2 x 128 x 24 = 65536
-constexpr int kRegsPrep = 232, kRegsIdle = 24;
-static_assert(2 * 128 * kRegsPrep + 2 * 128 * kRegsIdle <= st::kThreads * 128, "register split above the launch total");
+// three preparing warpgroups at 160 and the fourth at 24: 3 x 128 x 160 + 128 x 24 = 64512
+constexpr int kRegsPrep = 160, kRegsIdle = 24;
+static_assert(kInst * 128 * kRegsPrep + (4 - kInst) * 128 * kRegsIdle <= st::kThreads * 128,
+              "register split above the launch total");
 }  // namespace fz
 
 template <bool PC>
@@ -1479,10 +1493,9 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oTmemBase);
     volatile long* item_slot = reinterpret_cast<volatile long*>(sm + oItem);
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kInst; ++i) {
             uint64_t* b = reinterpret_cast<uint64_t*>(sm + i * kPrepStride + prep::oBar);
-            mbar_init(&b[0], 1);
-            mbar_init(&b[1], 1);
+            for (int j = 0; j < 3; ++j) mbar_init(&b[j], 1);
         }
         fence_mbar_init();
         prefetch_tmap(&mQ);
@@ -1497,7 +1510,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tbase;
-    if (wg < 2) {
+    if (wg < kInst) {
         reg_alloc<kRegsPrep>();
         uint8_t* smi = sm + wg * kPrepStride;
         uint64_t* bars = reinterpret_cast<uint64_t*>(smi + prep::oBar);
@@ -1515,7 +1528,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
             const int first = a.chunk_first[nn];
             if (pos >= a.chunk_first[nn + 1] - first) continue;  // this sequence is shorter
             const long gh = (long)(first + pos) * a.H + hh;
-            prep_chunk<PC>(smi, tm + (uint32_t)wg * 256u, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a);
+            prep_chunk<PC>(smi, tm + (uint32_t)wg * prep::kTmemCols, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a);
             parity ^= 1u;
             __threadfence();
             gb.sync();
