@@ -62,6 +62,31 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
     return x[0];
 }
 
+// The raw per-token inputs one lane needs: its q and k columns, the value of its state row, the
+// decay (its key channels' logits, or the head's in g[0]), beta, and, for threads below D, the gate
+// input of output channel threadIdx.x.
+template <int EPT>
+struct TokenInputs {
+    float q[EPT], k[EPT], g[EPT], v, beta, z;
+};
+
+template <int D, typename TIn, bool GATE>
+__device__ __forceinline__ TokenInputs<D / 32> load_token(const DecodeArgs& a, long tok, int h, int hk, int lane,
+                                                          int vrow) {
+    constexpr int EPT = D / 32;
+    TokenInputs<EPT> in;
+    const long vt = tok * a.H + h;      // [.., H] row of this value head
+    const long qt = tok * a.Hk + hk;    // [.., Hk] row of its query/key head
+    load_vec<EPT>(static_cast<const TIn*>(a.q) + qt * D + lane * EPT, in.q);
+    load_vec<EPT>(static_cast<const TIn*>(a.k) + qt * D + lane * EPT, in.k);
+    in.v = to_f32(static_cast<const TIn*>(a.v)[vt * D + vrow]);
+    if (a.g_per_channel) load_vec<EPT>(a.g + vt * D + lane * EPT, in.g);
+    else in.g[0] = a.g[vt];
+    in.beta = a.beta[vt];
+    in.z = GATE && threadIdx.x < D ? a.z[vt * D + threadIdx.x] : 0.f;
+    return in;
+}
+
 // One CTA per (sequence, value head).  The state comes from slot idx[n] of the pool (slot n when
 // idx is null), stays in registers for the T tokens, and is written back once.  Per token:
 //     x' = silu(conv(x)) for x in q, k, v        (optional short convolution)
@@ -111,16 +136,26 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
         for (int j = 0; j < 3; ++j) hv[j] = si ? si[(long)cv * 3 + j] : 0.f;
     }
 
+    // Without the convolution the raw inputs of token t + 1 are loaded while token t computes, so
+    // only the first token's loads sit on the chain of a multi-token unit.  The convolution's
+    // history already fills the register budget: there each token loads its own inputs.
+    constexpr bool kPrefetch = !CONV;
+    TokenInputs<EPT> nxt;
+    if constexpr (kPrefetch) nxt = load_token<D, TIn, GATE>(a, (long)n * a.T, h, hk, lane, vrow);
     for (int t = 0; t < a.T; ++t) {
         const long tok = (long)n * a.T + t;
         const long vt = tok * a.H + h;          // [.., H] row of this value head
-        const long qt = tok * a.Hk + hk;        // [.., Hk] row of its query/key head
-        const TIn* q = static_cast<const TIn*>(a.q) + qt * D;
-        const TIn* k = static_cast<const TIn*>(a.k) + qt * D;
+        TokenInputs<EPT> cur;
+        if constexpr (kPrefetch) {
+            cur = nxt;
+            if (t + 1 < a.T) nxt = load_token<D, TIn, GATE>(a, tok + 1, h, hk, lane, vrow);
+        } else {
+            cur = load_token<D, TIn, GATE>(a, tok, h, hk, lane, vrow);
+        }
         float qv[EPT], kv[EPT], alpha[EPT];
-        load_vec<EPT>(q + lane * EPT, qv);
-        load_vec<EPT>(k + lane * EPT, kv);
-        float vr = to_f32(static_cast<const TIn*>(a.v)[vt * D + vrow]);
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) { qv[e] = cur.q[e]; kv[e] = cur.k[e]; }
+        float vr = cur.v;
         if constexpr (CONV) {
 #pragma unroll
             for (int e = 0; e < EPT; ++e) {  // taps read here (L1) rather than held across the tokens
@@ -135,16 +170,14 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
             hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
         }
         if (a.g_per_channel) {
-            float gv[EPT];
-            load_vec<EPT>(a.g + vt * D + lane * EPT, gv);
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) alpha[e] = expf(gv[e]);
+            for (int e = 0; e < EPT; ++e) alpha[e] = expf(cur.g[e]);
         } else {
-            const float a0 = expf(a.g[vt]);
+            const float a0 = expf(cur.g[0]);
 #pragma unroll
             for (int e = 0; e < EPT; ++e) alpha[e] = a0;
         }
-        const float beta = a.beta[vt];
+        const float beta = cur.beta;
 
         float ssq = 0.f, ssk = 0.f;
 #pragma unroll
@@ -196,7 +229,7 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
             const float rinv = rsqrtf(ss / D + a.eps);
             if (threadIdx.x < D) {
                 const int r = threadIdx.x;
-                const float z = a.z[vt * D + r];
+                const float z = cur.z;
                 const float w = a.w ? a.w[r] : 1.0f;
                 store_out(a.out, vt * D + r, a.out_dtype, w * ys[r] * rinv * z * sigmoidf_(z));
             }
