@@ -264,6 +264,19 @@ __device__ __forceinline__ void warp_mm16(const float* P, const float* Q, float 
 // substitution (one warp per block, one lane per column); then block rows 1..3 in order,
 // T_bj = -T_bb sum_{k=j}^{b-1} A_bk T_kj, one warp per block (b, j) with the 16x16 products held
 // in registers; X is a per-warp 16 x LD scratch (warps 0-2 only: 3 x 16 x 68 x 4 B = 13 KB).
+// Element i (0..63) of the 64 values lo[0..31] | hi[0..31], chosen by a tree of selects: a register
+// array indexed by a thread-dependent value would be placed in local memory.
+__device__ __forceinline__ float pick64(const uint32_t (&lo)[32], const uint32_t (&hi)[32], int i) {
+    uint32_t t[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) t[j] = (i & 32) ? hi[j] : lo[j];
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = (i & w) ? t[j + w] : t[j];
+    return __uint_as_float(t[0]);
+}
+
 // Bounded wait (2 s at the top SM clock) for another CTA of the fused kernel to publish a chunk's
 // workspace entries; false when the bound runs out.
 __device__ __forceinline__ bool wait_ready(const int32_t* flag) {
@@ -725,26 +738,20 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
             tmem_ld32(lane_addr + 0, r0);
             tmem_ld32(lane_addr + 32, r1);
             tmem_wait_ld();
+            if (tid < kC) {
+                const float diag = pick64(r0, r1, tid);  // k_i . k_i
+                kinv[tid] = a.use_l2 ? rsqrtf(diag + kL2Eps) : 1.0f;
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) { row[j] = __uint_as_float(r0[j]); row[32 + j] = __uint_as_float(r1[j]); }
         }
-        float diag = 0.f;
-        if (tid < kC) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) if (j == tid) diag = row[j];
-            kinv[tid] = a.use_l2 ? rsqrtf(diag + kL2Eps) : 1.0f;
-        } else {
+        if (tid >= kC) {
             uint32_t r2[32], r3[32];
             tmem_ld32(lane_addr + 64, r2);
             tmem_ld32(lane_addr + 96, r3);
             tmem_wait_ld();
-            const int ii = tid - kC;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j == ii) diag = __uint_as_float(r2[j]);
-                if (j + 32 == ii) diag = __uint_as_float(r3[j]);
-            }
-            qsv[ii] = a.scale * (a.use_l2 ? rsqrtf(diag + kL2Eps) : 1.0f);
+            const float diag = pick64(r2, r3, tid - kC);  // q_i . q_i
+            qsv[tid - kC] = a.scale * (a.use_l2 ? rsqrtf(diag + kL2Eps) : 1.0f);
         }
         tc_fence_before();
         gb.sync();
