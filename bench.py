@@ -216,6 +216,10 @@ def oracle_rate(inp, H, seconds_budget=20.0, threads=None):
 # GPU measurements
 # ---------------------------------------------------------------------------------------------
 
+# time slices per sequence of the streamed end-to-end prefill step (host link overlapped with the kernels)
+E2E_PARTS = 2
+
+
 def ev():
     return torch.cuda.Event(enable_timing=True)
 
@@ -270,23 +274,78 @@ def bench_prefill(args, dev):
     assert gdn.gdn_get_device_error() == 0
 
     # ---- end to end through the ABI with host buffers ----
+    # Every step copies all inputs in from pinned host memory and the outputs back.  The host link
+    # (about 0.2 TB/s each way on this machine) takes 5x longer than the kernels, so the step is
+    # streamed: every sequence is cut into E2E_PARTS time slices (each a contiguous host range, so one
+    # copy per tensor), slice (s, p) is copied in on one stream, run by gdn_decay_from_logits +
+    # gdn_chunk_fwd on another (one sequence; its initial state is slice p - 1's final state, in
+    # place) and copied out on a third.  The copies of later slices overlap the kernels and the
+    # copy-out of earlier ones.  Slices are whole chunks, so the result is bit-identical to the
+    # single call (checked below).
     pinned = {k_: v_.pin_memory() for k_, v_ in inp_cpu.items()
-              if isinstance(v_, torch.Tensor) and k_ in ("q", "k", "v", "a", "A_log", "b", "z")}
+              if isinstance(v_, torch.Tensor) and k_ in ("q", "k", "v", "a", "b", "z")}
+    A_log_h = inp_cpu["A_log"].pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + A_log_h.numel() * A_log_h.element_size()
     d2h = out_h.numel() * out_h.element_size() + Sf_h.numel() * Sf_h.element_size()
+    P = E2E_PARTS
+    Tn = total_T // n                      # tokens per sequence
+    Tp = Tn // P                           # tokens per slice (a multiple of the chunk)
+    assert Tn % P == 0 and Tp % 64 == 0
+    slices = [(sq, p_, sq * Tn + p_ * Tp) for sq in range(n) for p_ in range(P)]  # (sequence, slice, first token)
+    bufs = [{k_: torch.empty((Tp,) + t.shape[1:], dtype=t.dtype, device=dev) for k_, t in pinned.items()}
+            for _ in slices]
+    A_log_d = torch.empty_like(A_log_h, device=dev)
+    g_p = [torch.empty(Tp, H, device=dev) for _ in slices]
+    b_p = [torch.empty(Tp, H, device=dev) for _ in slices]
+    o_p = [torch.empty(Tp, H, d, dtype=torch.bfloat16, device=dev) for _ in slices]
+    S_e = torch.empty(n, H, d, d, device=dev)
+    ws_p = gdn.lib().gdn_chunk_fwd_workspace_size(1, Tp, H, d, d, gdn.GDN_BF16)
+    ws_e = torch.empty(max(ws_p, 1), dtype=torch.uint8, device=dev)
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_step():
-        for k_, t in pinned.items():
-            d_in[k_].copy_(t, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        Sf_h.copy_(Sf, non_blocking=True)
+        start = ev()
+        start.record(stream)
+        for s_ in (s_in, s_run, s_out):
+            s_.wait_event(start)
+        # all copies in are enqueued first, then the kernels, then the copies out: enqueued in
+        # another order, a copy can queue behind a kernel when the streams share a hardware queue
+        copied, ran = [], []
+        with torch.cuda.stream(s_in):
+            A_log_d.copy_(A_log_h, non_blocking=True)
+            for i, (_, _, t0) in enumerate(slices):
+                for k_, t in pinned.items():
+                    bufs[i][k_].copy_(t[t0:t0 + Tp], non_blocking=True)
+                e_ = ev()
+                e_.record(s_in)
+                copied.append(e_)
+        with torch.cuda.stream(s_run):
+            for i, (sq, p_, _) in enumerate(slices):
+                s_run.wait_event(copied[i])
+                x, S_seq = bufs[i], S_e[sq:sq + 1]
+                gdn.gdn_decay_from_logits(x["a"], A_log_d, b=x["b"], g_out=g_p[i], beta_out=b_p[i])
+                gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], g_p[i], b_p[i], num_seqs=1,
+                                  initial_state=S_seq if p_ > 0 else None, gate_z=x["z"], out=o_p[i],
+                                  final_state=S_seq, workspace=ws_e)
+                e_ = ev()
+                e_.record(s_run)
+                ran.append(e_)
+        with torch.cuda.stream(s_out):
+            for i, (_, _, t0) in enumerate(slices):
+                s_out.wait_event(ran[i])
+                out_h[t0:t0 + Tp].copy_(o_p[i], non_blocking=True)
+            Sf_h.copy_(S_e, non_blocking=True)
+        for s_ in (s_in, s_run, s_out):
+            stream.wait_stream(s_)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
+    assert gdn.gdn_get_device_error() == 0
+    # the streamed step reproduces the single call exactly
+    assert torch.equal(out_h, out.cpu()) and torch.equal(Sf_h, Sf.cpu()), "streamed e2e step differs"
     e2e_ms = []
     for _ in range(args.steps):
         flush.zero_()
@@ -297,9 +356,12 @@ def bench_prefill(args, dev):
         e2e_ms.append((e0, e1))
     torch.cuda.synchronize()
     e2e = statistics.mean(a.elapsed_time(b_) for a, b_ in e2e_ms)
-    # kernels per step: gdn_decay_from_logits (1) + gdn_chunk_fwd (3 on the tensor-core path:
-    # chunk map, chunk prep, state pass; 1 on the CUDA-core path)
-    per_step = 1 + (3 if ws_bytes > 0 else 1)
+    # kernels per step: gdn_decay_from_logits (1) + gdn_chunk_fwd (tensor-core path: chunk map and
+    # either the fused kernel, taken when the units are at most half the SMs, or chunk prep + state
+    # pass; 1 on the CUDA-core path)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused = os.environ.get("GDN_PREFILL_FUSED", "1") != "0" and n * H <= sms // 2
+    per_step = 1 + ((2 if fused else 3) if ws_bytes > 0 else 1)
     return dict(ms=ms, kernel_ms=kms, clocks=clk, e2e_ms=e2e, h2d=h2d, d2h=d2h, total_T=total_T,
                 H=H, d=d, num_seqs=n, inp=inp_cpu, launches=per_step * args.steps)
 
@@ -317,11 +379,15 @@ def bench_decode(args, dev):
     beta = torch.empty(N, H, device=dev)
     out = torch.empty(N, H, d, dtype=torch.bfloat16, device=dev)
     gdn.gdn_decay_from_logits(a, A_log, b=b, g_out=g, beta_out=beta)
+    # L2 is flushed before every timed iteration (the state, 1.07 GB, is larger than L2, but the
+    # tail written by the previous iteration would otherwise still be cached)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(args.warmup):
         gdn.gdn_recurrent_step(q, k, v, g, beta, state, out=out)
     torch.cuda.synchronize()
     times = []
     for _ in range(max(args.steps, 20)):
+        flush.zero_()
         e0, e1 = ev(), ev()
         e0.record(stream)
         gdn.gdn_decay_from_logits(a, A_log, b=b, g_out=g, beta_out=beta)
@@ -351,6 +417,7 @@ def bench_decode(args, dev):
     torch.cuda.synchronize()
     mt = []
     for _ in range(max(args.steps, 20)):
+        flush.zero_()
         e0, e1 = ev(), ev()
         e0.record(stream)
         gdn.gdn_recurrent_multi_step(qm, km, vm, gm, bm, pool, state_indices=idx, out=outm)
@@ -446,6 +513,7 @@ def bench_variants(args, dev):
     torch.cuda.synchronize()
     ts = []
     for _ in range(max(args.steps, 20)):
+        flush.zero_()
         e0, e1 = ev(), ev()
         e0.record(stream)
         dcall()
@@ -485,8 +553,9 @@ def run_gdn(args):
     tokens = pf["total_T"] * world
     value = tokens / (ms / 1e3)
 
-    # roofline of the dominant launch unit: the gdn_chunk_fwd call (chunk map + chunk prep + state
-    # pass, inseparable behind the C ABI), timed live with CUDA events around the call
+    # roofline of the dominant launch unit: the gdn_chunk_fwd call (chunk map + the fused chunk
+    # preparation / serial pass kernel for this few-unit workload; inseparable behind the C ABI),
+    # timed live with CUDA events around the call
     th = pf["total_T"] * pf["H"]
     flops = th * prefill_flops_per_token_head(pf["d"])
     byts = prefill_bytes(pf["total_T"], pf["H"], pf["d"], pf["num_seqs"])
@@ -494,7 +563,9 @@ def run_gdn(args):
     tr = traffic_record("gdn_chunk_fwd[prefill]")
     roof = {"bound": "hbm", "achieved": byts / k_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": byts / k_s / 1e9 / peaks["hbm_gbs"], "traffic": tr,
-            "kernel": "gdn_chunk_fwd (chunk_map_kernel + chunk_prep_kernel + chunk_state_kernel)",
+            "kernel": ("gdn_chunk_fwd (chunk_map_kernel + chunk_fused_kernel: chunk preparation and serial "
+                       "pass in one cooperative launch)" if os.environ.get("GDN_PREFILL_FUSED", "1") != "0" else
+                       "gdn_chunk_fwd (chunk_map_kernel + chunk_prep_kernel + chunk_state_kernel)"),
             "algorithmic_bytes": byts, "algorithmic_flops": flops,
             "tensor_tflops": flops / k_s / 1e12,
             "tensor_frac": flops / k_s / 1e12 / peaks["bf16_tflops"],
