@@ -529,10 +529,73 @@ def bench_variants(args, dev):
     return res
 
 
+def bench_workloads(args, dev, names):
+    """The parity-case prefill workloads (varlen: 64 sequences of 128-8192 tokens with initial
+    states; long: one 131,072-token sequence, H = 32, fused gate), timed like the headline step:
+    gdn_decay_from_logits + gdn_chunk_fwd, L2 flushed before every step, CUDA events.  Opt-in
+    (--workloads); prints one JSON line."""
+    import gated_deltanet_recurrence_gb300 as gdn
+    from gated_deltanet_recurrence_gb300 import synthetic
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {}
+    for wl in names:
+        inp = synthetic.prefill_inputs(wl)
+        cfg = inp["cfg"]
+        H, d, n, T = cfg["H"], cfg["d"], inp["num_seqs"], inp["total_T"]
+        q, k, v, a, A_log, b = (inp[x].to(dev) for x in ("q", "k", "v", "a", "A_log", "b"))
+        z = inp["z"].to(dev) if inp["z"] is not None else None
+        S0 = inp["initial_state"].to(dev) if inp["initial_state"] is not None else None
+        cu = inp["cu_seqlens"].to(dev) if inp["cu_seqlens"] is not None else None
+        g = torch.empty(T, H, device=dev)
+        beta = torch.empty(T, H, device=dev)
+        out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+        Sf = torch.empty(n, H, d, d, device=dev)
+        ws = torch.empty(max(gdn.lib().gdn_chunk_fwd_workspace_size(n, T, H, d, d, gdn.GDN_BF16), 1),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            gdn.gdn_decay_from_logits(a, A_log, b=b, g_out=g, beta_out=beta)
+            gdn.gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=cu, num_seqs=n, initial_state=S0, gate_z=z,
+                              out=out, final_state=Sf, workspace=ws)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(min(args.steps, 10)):
+            flush.zero_()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        assert gdn.gdn_get_device_error() == 0
+        ms = statistics.mean(x.elapsed_time(y) for x, y in ts)
+        byts = prefill_bytes(T, H, d, n, gated=z is not None, init_state=S0 is not None)
+        fused = os.environ.get("GDN_PREFILL_FUSED", "1") != "0" and n * H <= sms // 2
+        res[wl] = {"tokens": T, "num_seqs": n, "units": n * H, "ms": ms, "tokens_per_s": T / (ms / 1e3),
+                   "hbm_gbs": byts / (ms / 1e3) / 1e9, "algorithmic_bytes": byts,
+                   "path": "fused" if fused else "two-kernel"}
+        del q, k, v, a, b, z, S0, out, ws, g, beta, Sf
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gdn(args):
     dev = torch.device("cuda", args.local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
+    if args.workloads:
+        res = bench_workloads(args, dev, [w for w in args.workloads.split(",") if w])
+        if args.rank == 0:
+            for r in res.values():
+                r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm_gbs"]
+            print(json.dumps({"workloads": res, "l2": "flushed (512 MB write) before each step",
+                              "step": "gdn_decay_from_logits + gdn_chunk_fwd"}), flush=True)
+        return
     if args.only == "decode":
         dc = bench_decode(args, dev)
         if args.rank == 0:
@@ -651,6 +714,8 @@ def main():
                     help="skip the grouped-head / per-channel-decay / convolution measurements")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time only one workload (profiling runs); the driver uses the default")
+    ap.add_argument("--workloads", default="",
+                    help="comma list of parity-case workloads to time instead (varlen, long)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: warm-up raised to 3 steps", file=sys.stderr)

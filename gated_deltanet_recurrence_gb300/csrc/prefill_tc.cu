@@ -994,11 +994,7 @@ constexpr uint32_t kSmem = kBytes + 1024;
 static_assert(kSmem <= 232448, "state kernel shared memory exceeds the per-block limit");
 constexpr uint32_t kStageTx = 32768 + 16384 + 8192;
 // barriers
-// SBF_LO / SBF_HI: the bf16 mirror of S, columns 0-63 / 64-127 (one 128-byte atom column each);
-// A12_LO / A12_HI: V_new^T, tokens 0-31 / 32-63.  The products reading a half start once it is written.
-enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF_LO, SBF_HI, DA1, A12_LO, A12_HI, SFULL, DO_0, DO_1, DOE_0, DOE_1, ZFULL0,
-       ZFULL1, NBAR };
-static_assert(8 * NBAR + 8 <= 256, "barriers, TMEM base and abort flag in the barrier region");
+enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF, DA1, A12, SFULL, DO_0, DO_1, DOE_0, DOE_1, ZFULL0, ZFULL1, NBAR };
 constexpr uint32_t kTmemCols = 512;
 }  // namespace st
 
@@ -1090,37 +1086,29 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 const uint64_t dSt = dStage0 + (uint64_t)((s * kStage) >> 4);
                 const uint64_t dK = dStageK0 + (uint64_t)((s * kStage) >> 4);
                 if (!mbar_wait(&bars[FULL0 + s], (c >> 1) & 1, kPolls)) { fail(); break; }
-                if (!mbar_wait(&bars[SBF_LO], c & 1, kPolls)) { fail(); break; }
+                if (!mbar_wait(&bars[SBF], c & 1, kPolls)) { fail(); break; }
+                if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
                 if (*abort_flag) break;
                 tc_fence_after();
                 const uint32_t tDA = tDA0 + b * 64, tDO = tDO0 + b * 128;
-                // the serial chain first: S W^T, columns 0-63 of S, then 64-127 once mirrored
+                // the serial chain first: S W^T
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_bf16_ss(tDA, dS + k * 2, dSt + sWQ / 16 + k * 2, kIdW, k > 0);
-                if (!mbar_wait(&bars[SBF_HI], c & 1, kPolls)) { fail(); break; }
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mma_bf16_ss(tDA, dS + 1024 + k * 2, dSt + (sWQ + 16384) / 16 + k * 2, kIdW, 1);
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                    mma_bf16_ss(tDA, dS + off, dSt + sWQ / 16 + off, kIdW, k > 0);
+                }
                 mma_commit(&bars[DA1]);
-                // while the state epilogue forms V_new: O = Q~ S^T (tokens as rows, M = 64), once the
-                // output group has taken chunk c - 2's O out of this buffer
-                if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
-                tc_fence_after();
+                // while the state epilogue forms V_new: O = Q~ S^T (tokens as rows, M = 64)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
                     mma_bf16_ss(tDO, dSt + (sWQ + 8192) / 16 + off, dS + off, kIdO, k > 0);
                 }
-                // S += V_new^T K~ (TMEM S was pre-decayed by this chunk's gamma), tokens 0-31 first
-                if (!mbar_wait(&bars[A12_LO], c & 1, kPolls)) { fail(); break; }
+                if (!mbar_wait(&bars[A12], c & 1, kPolls)) { fail(); break; }
                 tc_fence_after();
-                mma_bf16_ss(tS, dA1 + 0, dK + 0, kIdS, 1);
-                mma_bf16_ss(tS, dA1 + 2, dK + 128, kIdS, 1);
-                if (!mbar_wait(&bars[A12_HI], c & 1, kPolls)) { fail(); break; }
-                tc_fence_after();
-                mma_bf16_ss(tS, dA1 + 4, dK + 256, kIdS, 1);
-                mma_bf16_ss(tS, dA1 + 6, dK + 384, kIdS, 1);
+                // S += V_new^T K~   (TMEM S was pre-decayed by this chunk's gamma)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mma_bf16_ss(tS, dA1 + k * 2, dK + k * 128, kIdS, 1);
                 mma_commit(&bars[SFULL]);
                 // O += Aqk V_new   (B = V_new^T rows, K-major)
 #pragma unroll
@@ -1185,10 +1173,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 fence_async_smem();
                 tc_fence_before();
                 bar_sync(1, 128);
-                if (r == 0) {
-                    mbar_arrive(&bars[SBF_LO]);
-                    mbar_arrive(&bars[SBF_HI]);
-                }
+                if (r == 0) mbar_arrive(&bars[SBF]);
             }
         }
         uint4 up_next[8];
@@ -1222,100 +1207,78 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             bool ok = mbar_wait(&bars[DA1], c & 1, kPolls);
             if (!ok) fail();
             tc_fence_after();
-            // ---- V_new^T row r = U^T row r - (S W^T) row r, tokens 0-31 then 32-63 (each half
-            //      signalled as soon as written; after a timed-out wait the values are garbage, the
-            //      error is recorded, and the registers stay unconditional) ----
-            uint32_t dv[2][32];
-            tmem_ld32(tDA0 + b * 64 + lrow, dv[0]);
-            tmem_ld32(tDA0 + b * 64 + lrow + 32, dv[1]);
-            tmem_wait_ld();
-            auto vnew_half = [&](int hf) {
-                float u[32];
+            // ---- V_new^T row r = U^T row r - (S W^T) row r ----
+            if (ok) {
+                uint32_t v[2][32];
+                tmem_ld32(tDA0 + b * 64 + lrow, v[0]);
+                tmem_ld32(tDA0 + b * 64 + lrow + 32, v[1]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    const uint4 q = up[4 * hf + c8];
-                    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                for (int hf = 0; hf < 2; ++hf) {
+                    float u[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
-                        u[8 * c8 + 2 * e] = f.x - __uint_as_float(dv[hf][8 * c8 + 2 * e]);
-                        u[8 * c8 + 2 * e + 1] = f.y - __uint_as_float(dv[hf][8 * c8 + 2 * e + 1]);
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const uint4 q = up[4 * hf + c8];
+                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+                            u[8 * c8 + 2 * e] = f.x - __uint_as_float(v[hf][8 * c8 + 2 * e]);
+                            u[8 * c8 + 2 * e + 1] = f.y - __uint_as_float(v[hf][8 * c8 + 2 * e + 1]);
+                        }
                     }
-                }
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(sm + oA1, r, 4 * hf + c8, u + 8 * c8);
-            };
-            vnew_half(0);
+                    for (int c8 = 0; c8 < 4; ++c8) st_sw128_chunk(sm + oA1, r, 4 * hf + c8, u + 8 * c8);
+                }
+            }
             fence_async_smem();
             tc_fence_before();
             if (bar_sync_or(1, 128, *abort_flag != 0)) break;
-            if (r == 0) mbar_arrive(&bars[A12_LO]);
-            vnew_half(1);
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_sync_or(1, 128, *abort_flag != 0)) break;
-            if (r == 0) mbar_arrive(&bars[A12_HI]);
+            if (r == 0) mbar_arrive(&bars[A12]);
             ok = mbar_wait(&bars[SFULL], c & 1, kPolls);
             if (!ok) fail();
             tc_fence_after();
-            // ---- S: mirror as bf16 operand, one 64-column atom column at a time (each signalled as
-            //      soon as written), then that half pre-decayed by the next chunk's gamma back to TMEM;
-            //      the stores are complete before the group reaches the next A12 barrier ----
-            // After a timed-out wait (error recorded, results void) the loads and stores below still
-            // run on the allocated TMEM columns and shared tiles: values are garbage, nothing is
-            // out of bounds, and the array stays in registers (conditional uses would spill it).
-            uint32_t sv[4][32];
+            // ---- S: mirror as bf16 operand, pre-decay by the next chunk's gamma ----
+            if (ok) {
+                uint32_t v[4][32];
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) tmem_ld32(tS + lrow + blk * 32, sv[blk]);
-            tmem_wait_ld();
-            if (last) {
-                if (ok && a.final_state) {
+                for (int blk = 0; blk < 4; ++blk) tmem_ld32(tS + lrow + blk * 32, v[blk]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk) {
-                        float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
+                for (int blk = 0; blk < 4; ++blk) {
+                    float* f = reinterpret_cast<float*>(v[blk]);
+                    if (last) {
+                        if (a.final_state) {
+                            float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<uint4*>(dst + j) = make_uint4(sv[blk][j], sv[blk][j + 1], sv[blk][j + 2], sv[blk][j + 3]);
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4*>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            st_sw128_chunk(Sb + (blk >> 1) * 16384, r, (blk & 1) * 4 + c8, f + 8 * c8);
+                        if constexpr (PC) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 t = *reinterpret_cast<const float4*>(gvec + blk * 32 + j);
+                                f[j] *= t.x; f[j + 1] *= t.y; f[j + 2] *= t.z; f[j + 3] *= t.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) f[j] *= gnext;
+                        }
+                        tmem_st32(tS + lrow + blk * 32, v[blk]);
                     }
                 }
-                continue;
             }
-            // (element-wise bit casts: the array's address is never taken, so it stays in registers
-            // across the barriers)
-            auto mirror = [&](int blk) {
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                    *reinterpret_cast<uint4*>(Sb + (blk >> 1) * 16384 + sw128_offset(r, ((blk & 1) * 4 + c8) * 8)) =
-                        make_uint4(pack_bf16x2(__uint_as_float(sv[blk][8 * c8]), __uint_as_float(sv[blk][8 * c8 + 1])),
-                                   pack_bf16x2(__uint_as_float(sv[blk][8 * c8 + 2]), __uint_as_float(sv[blk][8 * c8 + 3])),
-                                   pack_bf16x2(__uint_as_float(sv[blk][8 * c8 + 4]), __uint_as_float(sv[blk][8 * c8 + 5])),
-                                   pack_bf16x2(__uint_as_float(sv[blk][8 * c8 + 6]), __uint_as_float(sv[blk][8 * c8 + 7])));
-            };
-            auto predecay = [&](int blk) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float gj = PC ? gvec[blk * 32 + j] : gnext;
-                    sv[blk][j] = __float_as_uint(__uint_as_float(sv[blk][j]) * gj);
-                }
-                tmem_st32(tS + lrow + blk * 32, sv[blk]);
-            };
-            mirror(0);
-            mirror(1);
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_sync_or(1, 128, *abort_flag != 0)) break;
-            if (r == 0) mbar_arrive(&bars[SBF_LO]);
-            predecay(0);
-            predecay(1);
-            mirror(2);
-            mirror(3);
-            fence_async_smem();
-            tc_fence_before();
-            if (bar_sync_or(1, 128, *abort_flag != 0)) break;
-            if (r == 0) mbar_arrive(&bars[SBF_HI]);
-            predecay(2);
-            predecay(3);
-            tmem_wait_st();  // the registers of a TMEM store stay live until its wait
+            if (!last) {
+                tmem_wait_st();
+                fence_async_smem();
+                tc_fence_before();
+                if (bar_sync_or(1, 128, *abort_flag != 0)) break;
+                if (r == 0) mbar_arrive(&bars[SBF]);
+            }
         }
     }
     } else {
