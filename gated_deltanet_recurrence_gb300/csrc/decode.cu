@@ -94,30 +94,19 @@ __device__ __forceinline__ TokenInputs<D / 32> load_token(const DecodeArgs& a, l
 //     value for the head; alpha s . k = s . (alpha k))
 //     sk_r = s_r . ka,  sq_r = s_r . qa,  delta_r = beta (v_r - sk_r)
 //     s_r <- alpha . s_r + delta_r k,     y_r = sq_r + delta_r (k . q)
+// The T tokens of one (sequence n, value head h) unit on this warp's 16 state rows `s` (this lane's
+// columns, kept in registers), plus the convolution history when fused; `ys` is D floats of shared
+// memory (gate only).  Called by every thread of the CTA: it synchronises the CTA when a gate or a
+// convolution history is written.
 template <int D, typename TIn, bool GATE, bool CONV>
-__global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
+__device__ __forceinline__ void decode_tokens(float (&s)[kRowsPerWarp][D / 32], const DecodeArgs& a, int n, int h,
+                                              int slot, float* ys) {
     constexpr int EPT = D / 32;
-    static_assert(D / kRowsPerWarp * 32 == D * 2, "one warp per 16 rows");
-    __shared__ float ys[GATE ? D : 1];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int unit = blockIdx.x;  // n * H + h
-    const int n = unit / a.H, h = unit % a.H;
     const int grp = a.H / a.Hk, hk = h / grp;   // value head h reads query/key head h / grp
-    const int slot = a.idx ? a.idx[n] : n;
-    if (slot < 0) return;                       // padding entry: nothing to do
-    if (slot >= a.num_slots) {                  // checked before any state access
-        if (threadIdx.x == 0) record_error(a.err, GDN_ERR_ARG);
-        return;
-    }
     const int r0 = warp * kRowsPerWarp;
     const int vrow = r0 + (lane & (kRowsPerWarp - 1));
-    float* S = a.state + ((long)slot * a.H + h) * D * D + (long)r0 * D + lane * EPT;
-
-    // state rows first: they are the bytes that matter
-    float s[kRowsPerWarp][EPT];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::load(S + (long)i * D, s[i]);
 
     // short convolution: taps and the three previous raw inputs of this lane's channels
     const int cq = hk * D + lane * EPT, ck = a.Hk * D + cq, cv = 2 * a.Hk * D + h * D + vrow;
@@ -197,14 +186,20 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
         }
         kq = warp_sum(kq);
 
+        // the row dot products and the update run on column pairs with the packed two-wide fp32
+        // FMA / multiply (half the instructions); a dot product adds its two pair sums at the end
         float x[32];
 #pragma unroll
         for (int i = 0; i < kRowsPerWarp; ++i) {
-            float dk = 0.f, dq = 0.f;
+            float2 pk = make_float2(0.f, 0.f), pq = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) { dk += s[i][e] * ka[e]; dq += s[i][e] * qa[e]; }
-            x[i] = dk;
-            x[kRowsPerWarp + i] = dq;
+            for (int e = 0; e < EPT; e += 2) {
+                const float2 sv = make_float2(s[i][e], s[i][e + 1]);
+                pk = __ffma2_rn(sv, make_float2(ka[e], ka[e + 1]), pk);
+                pq = __ffma2_rn(sv, make_float2(qa[e], qa[e + 1]), pq);
+            }
+            x[i] = pk.x + pk.y;
+            x[kRowsPerWarp + i] = pq.x + pq.y;
         }
         const float tt = transpose_reduce32(x, lane);  // lane < 16: s_r . ka of row r0 + lane; else s_r . qa
         const float delta = beta * (vr - tt);           // meaningful on lanes < 16
@@ -214,7 +209,12 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
         for (int i = 0; i < kRowsPerWarp; ++i) {
             const float di = __shfl_sync(0xffffffffu, delta, i);
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) s[i][e] = alpha[e] * s[i][e] + di * kv[e];
+            for (int e = 0; e < EPT; e += 2) {
+                const float2 t = __fmul2_rn(make_float2(alpha[e], alpha[e + 1]), make_float2(s[i][e], s[i][e + 1]));
+                const float2 r = __ffma2_rn(make_float2(di, di), make_float2(kv[e], kv[e + 1]), t);
+                s[i][e] = r.x;
+                s[i][e + 1] = r.y;
+            }
         }
 
         if constexpr (!GATE) {
@@ -236,9 +236,6 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
             __syncthreads();  // ys is rewritten by the next token
         }
     }
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::store(S + (long)i * D, s[i]);
-
     if constexpr (CONV) {
         if (a.conv.state_out) {
             float* so = a.conv.state_out + (long)slot * a.conv.dim * 3;
@@ -257,6 +254,32 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
                 for (int j = 0; j < 3; ++j) so[(long)cv * 3 + j] = hv[j];
         }
     }
+}
+
+// One CTA per (sequence, value head): the state rows are loaded into registers first (they are
+// the bytes that matter), the tokens run, and the state is written back once.
+template <int D, typename TIn, bool GATE, bool CONV>
+__global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
+    constexpr int EPT = D / 32;
+    static_assert(D / kRowsPerWarp * 32 == D * 2, "one warp per 16 rows");
+    __shared__ float ys[GATE ? D : 1];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int unit = blockIdx.x;  // n * H + h
+    const int n = unit / a.H, h = unit % a.H;
+    const int slot = a.idx ? a.idx[n] : n;
+    if (slot < 0) return;                       // padding entry: nothing to do
+    if (slot >= a.num_slots) {                  // checked before any state access
+        if (threadIdx.x == 0) record_error(a.err, GDN_ERR_ARG);
+        return;
+    }
+    float* S = a.state + ((long)slot * a.H + h) * D * D + (long)(warp * kRowsPerWarp) * D + lane * EPT;
+    float s[kRowsPerWarp][EPT];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::load(S + (long)i * D, s[i]);
+    decode_tokens<D, TIn, GATE, CONV>(s, a, n, h, slot, ys);
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::store(S + (long)i * D, s[i]);
 }
 
 template <int D, typename TIn>
