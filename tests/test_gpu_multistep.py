@@ -84,3 +84,24 @@ def test_multi_step_bad_index_is_reported():
     gdn.gdn_recurrent_multi_step(q.to(dev), k.to(dev), v.to(dev), g.to(dev), beta.to(dev), p, state_indices=idx)
     assert gdn.gdn_get_device_error() == -1
     assert torch.equal(p[[1, 3, 4, 5]].cpu(), pool[[1, 3, 4, 5]])
+
+
+@pytest.mark.parametrize("T", [2, 3, 4, 6, 9])
+def test_block_and_token_forms_agree(T, monkeypatch):
+    """The block form (the chunked update over blocks of four tokens, padded at the end) and the
+    token-by-token form compute the same recurrence: outputs and states agree to fp32 rounding,
+    gate included, with skipped sequences."""
+    N, H, d, slots = 21, 4, 128, 30
+    q, k, v, g, beta, pool, idx, z = _case(N, T, H, d, torch.bfloat16, slots, True, seed=300 + T)
+    dev = "cuda"
+    res = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("GDN_DECODE_BLOCKS", mode)
+        p = pool.to(dev)
+        y = gdn.gdn_recurrent_multi_step(q.to(dev), k.to(dev), v.to(dev), g.to(dev), beta.to(dev), p,
+                                         state_indices=idx.to(dev), gate_z=z.to(dev), out_dtype=torch.float32)
+        assert gdn.gdn_get_device_error() == 0
+        res[mode] = (y.cpu(), p.cpu())
+    live = idx >= 0
+    torch.testing.assert_close(res["1"][0][live], res["0"][0][live], rtol=1e-5, atol=1e-5)
+    torch.testing.assert_close(res["1"][1], res["0"][1], rtol=1e-5, atol=1e-7)
