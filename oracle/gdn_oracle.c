@@ -33,10 +33,11 @@
  *   state     [num_seqs][H][dv][dk] (the [LLM-Alg-2] section 1 orientation:
  *                                    S maps a key to a value, y = S q)
  *   cu_seqlens[num_seqs + 1]        prefix sums of the sequence lengths
- * Readings of points the pages leave open are listed in the design doc's oracle
- * section; the two that change numbers are (a) the delta is read from the
- * decayed state ([LLM-Alg-2] 4.3) and (b) l2(x) = x / sqrt(sum x^2 + 1e-6)
- * ([GDN-book] 6.6.4 l2norm).
+ * Of the points the pages leave open, two change the numbers of every call:
+ * (a) the delta is read from the decayed state ([LLM-Alg-2] 4.3) and (b)
+ * l2(x) = x / sqrt(sum x^2 + 1e-6) ([GDN-book] 6.6.4 l2norm).  The readings
+ * behind the options (decay per key channel, grouped heads, convolution
+ * history) are stated beside the entry points that use them.
  */
 #include <math.h>
 #include <pthread.h>
