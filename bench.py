@@ -193,8 +193,10 @@ def time_oracle(inp, heads, threads):
 def oracle_rate(inp, H, seconds_budget=20.0, threads=None):
     """Tokens/s of the oracle on the full workload, estimated from a bounded sample of heads."""
     threads = threads or os.cpu_count() or 1
-    # a one-head probe sizes the sample so that the measurement takes roughly the budget
+    # a one-head probe on one thread sizes the sample so that the measurement takes roughly the
+    # budget; it also gives the single-thread rate
     t1 = time_oracle(inp, [0], 1)
+    oracle_rate.single_thread = inp["total_T"] / (H * t1)
     per_head_parallel = t1 / min(threads, inp["num_seqs"])
     n_heads = max(1, min(H, int(seconds_budget / max(per_head_parallel, 1e-6) / 2)))
     heads = list(range(n_heads))
@@ -550,9 +552,10 @@ def bench_workloads(args, dev, names):
         cu = inp["cu_seqlens"].to(dev) if inp["cu_seqlens"] is not None else None
         g = torch.empty(T, H, device=dev)
         beta = torch.empty(T, H, device=dev)
-        out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(T, H, d, dtype=q.dtype, device=dev)
         Sf = torch.empty(n, H, d, d, device=dev)
-        ws = torch.empty(max(gdn.lib().gdn_chunk_fwd_workspace_size(n, T, H, d, d, gdn.GDN_BF16), 1),
+        dt = gdn.GDN_BF16 if q.dtype == torch.bfloat16 else gdn.GDN_F32
+        ws = torch.empty(max(gdn.lib().gdn_chunk_fwd_workspace_size(n, T, H, d, d, dt), 1),
                          dtype=torch.uint8, device=dev)
 
         def step():
@@ -574,11 +577,14 @@ def bench_workloads(args, dev, names):
         torch.cuda.synchronize()
         assert gdn.gdn_get_device_error() == 0
         ms = statistics.mean(x.elapsed_time(y) for x, y in ts)
-        byts = prefill_bytes(T, H, d, n, gated=z is not None, init_state=S0 is not None)
+        eb = q.element_size()
+        byts = prefill_bytes(T, H, d, n, qkv_bytes=eb, out_bytes=eb, gated=z is not None,
+                             init_state=S0 is not None)
         fused = os.environ.get("GDN_PREFILL_FUSED", "1") != "0" and n * H <= sms // 2
+        path = ("CUDA-core" if q.dtype != torch.bfloat16 or d != 128 else
+                "tensor-core fused" if fused else "tensor-core two-kernel")
         res[wl] = {"tokens": T, "num_seqs": n, "units": n * H, "ms": ms, "tokens_per_s": T / (ms / 1e3),
-                   "hbm_gbs": byts / (ms / 1e3) / 1e9, "algorithmic_bytes": byts,
-                   "path": "fused" if fused else "two-kernel"}
+                   "hbm_gbs": byts / (ms / 1e3) / 1e9, "algorithmic_bytes": byts, "path": path}
         del q, k, v, a, b, z, S0, out, ws, g, beta, Sf
         torch.cuda.empty_cache()
     return res
@@ -670,7 +676,8 @@ def run_gdn(args):
     if args.rank == 0 and not args.no_cpu_baseline:
         rate, th, sample, _ = oracle_rate(pf["inp"], pf["H"], seconds_budget=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": th, "kind": "oracle",
-                                "sample": sample}
+                                "sample": sample, "single_thread_value": oracle_rate.single_thread,
+                                "host_cores": os.cpu_count()}
     if args.rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -715,7 +722,7 @@ def main():
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time only one workload (profiling runs); the driver uses the default")
     ap.add_argument("--workloads", default="",
-                    help="comma list of parity-case workloads to time instead (varlen, long)")
+                    help="comma list of parity-case prefill workloads to time instead (tiny, varlen, long)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: warm-up raised to 3 steps", file=sys.stderr)
