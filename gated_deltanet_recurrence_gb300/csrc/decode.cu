@@ -72,16 +72,18 @@ struct TokenInputs {
     float q[EPT], k[EPT], g[EPT], v, beta, z;
 };
 
-template <int D, typename TIn, bool GATE>
+template <int D, typename TIn, bool GATE, bool QKV = true>
 __device__ __forceinline__ TokenInputs<D / 32> load_token(const DecodeArgs& a, long tok, int h, int hk, int lane,
                                                           int vrow) {
     constexpr int EPT = D / 32;
     TokenInputs<EPT> in;
     const long vt = tok * a.H + h;      // [.., H] row of this value head
     const long qt = tok * a.Hk + hk;    // [.., Hk] row of its query/key head
-    load_vec<EPT>(static_cast<const TIn*>(a.q) + qt * D + lane * EPT, in.q);
-    load_vec<EPT>(static_cast<const TIn*>(a.k) + qt * D + lane * EPT, in.k);
-    in.v = to_f32(static_cast<const TIn*>(a.v)[vt * D + vrow]);
+    if constexpr (QKV) {  // (with the convolution, the channel owners load the raw inputs instead)
+        load_vec<EPT>(static_cast<const TIn*>(a.q) + qt * D + lane * EPT, in.q);
+        load_vec<EPT>(static_cast<const TIn*>(a.k) + qt * D + lane * EPT, in.k);
+        in.v = to_f32(static_cast<const TIn*>(a.v)[vt * D + vrow]);
+    }
     if (a.g_per_channel) load_vec<EPT>(a.g + vt * D + lane * EPT, in.g);
     else in.g[0] = a.g[vt];
     in.beta = a.beta[vt];
@@ -97,12 +99,16 @@ __device__ __forceinline__ TokenInputs<D / 32> load_token(const DecodeArgs& a, l
 //     sk_r = s_r . ka,  sq_r = s_r . qa,  delta_r = beta (v_r - sk_r)
 //     s_r <- alpha . s_r + delta_r k,     y_r = sq_r + delta_r (k . q)
 // The T tokens of one (sequence n, value head h) unit on this warp's 16 state rows `s` (this lane's
-// columns, kept in registers), plus the convolution history when fused; `ys` is D floats of shared
-// memory (gate only).  Called by every thread of the CTA: it synchronises the CTA when a gate or a
-// convolution history is written.
+// columns, kept in registers); `ys` is D floats of shared memory (gate only), `cx` 3 D floats
+// (convolution only).  Called by every thread of the CTA: it synchronises the CTA when a gate or
+// a convolution is applied.
+//
+// The convolution runs once per CTA and token: each thread owns one or two of the 3 D (q | k | v,
+// channel) items, keeps their three previous raw inputs in registers, convolves the token's raw
+// input and writes the result to `cx`, from which every lane takes its q, k columns and v row.
 template <int D, typename TIn, bool GATE, bool CONV>
 __device__ __forceinline__ void decode_tokens(float (&s)[kRowsPerWarp][D / 32], const DecodeArgs& a, int n, int h,
-                                              int slot, float* ys) {
+                                              int slot, float* ys, float* cx) {
     constexpr int EPT = D / 32;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -110,21 +116,21 @@ __device__ __forceinline__ void decode_tokens(float (&s)[kRowsPerWarp][D / 32], 
     const int r0 = warp * kRowsPerWarp;
     const int vrow = r0 + (lane & (kRowsPerWarp - 1));
 
-    // short convolution: taps and the three previous raw inputs of this lane's channels
-    const int cq = hk * D + lane * EPT, ck = a.Hk * D + cq, cv = 2 * a.Hk * D + h * D + vrow;
+    // convolution items owned by this thread: item = tid + u * blockDim (u = 0, 1), group item / D
+    // (0: q, 1: k, 2: v), channel item % D; their three previous raw inputs, oldest first
+    constexpr int kItems = 3 * D, kOwn = (kItems + 2 * D - 1) / (2 * D);
     const float4* w4 = reinterpret_cast<const float4*>(a.conv.w);
-    float hq[CONV ? EPT : 1][3], hkk[CONV ? EPT : 1][3], hv[3];
+    float hist[CONV ? kOwn : 1][3];
+    int chan[CONV ? kOwn : 1];
     if constexpr (CONV) {
         const float* si = a.conv.state_in ? a.conv.state_in + (long)slot * a.conv.dim * 3 : nullptr;
 #pragma unroll
-        for (int e = 0; e < EPT; ++e)
+        for (int u = 0; u < kOwn; ++u) {
+            const int item = threadIdx.x + u * blockDim.x, gq = item / D, c = item % D;
+            chan[u] = gq == 0 ? hk * D + c : (gq == 1 ? a.Hk * D + hk * D + c : 2 * a.Hk * D + h * D + c);
 #pragma unroll
-            for (int j = 0; j < 3; ++j) {
-                hq[e][j] = si ? si[(long)(cq + e) * 3 + j] : 0.f;
-                hkk[e][j] = si ? si[(long)(ck + e) * 3 + j] : 0.f;
-            }
-#pragma unroll
-        for (int j = 0; j < 3; ++j) hv[j] = si ? si[(long)cv * 3 + j] : 0.f;
+            for (int j = 0; j < 3; ++j) hist[u][j] = (item < kItems && si) ? si[(long)chan[u] * 3 + j] : 0.f;
+        }
     }
 
     // Without the convolution the raw inputs of token t + 1 are loaded while token t computes, so
@@ -133,6 +139,7 @@ __device__ __forceinline__ void decode_tokens(float (&s)[kRowsPerWarp][D / 32], 
     constexpr bool kPrefetch = !CONV;
     TokenInputs<EPT> nxt;
     if constexpr (kPrefetch) nxt = load_token<D, TIn, GATE>(a, (long)n * a.T, h, hk, lane, vrow);
+    (void)w4;
     for (int t = 0; t < a.T; ++t) {
         const long tok = (long)n * a.T + t;
         const long vt = tok * a.H + h;          // [.., H] row of this value head
@@ -141,24 +148,36 @@ __device__ __forceinline__ void decode_tokens(float (&s)[kRowsPerWarp][D / 32], 
             cur = nxt;
             if (t + 1 < a.T) nxt = load_token<D, TIn, GATE>(a, tok + 1, h, hk, lane, vrow);
         } else {
-            cur = load_token<D, TIn, GATE>(a, tok, h, hk, lane, vrow);
+            cur = load_token<D, TIn, GATE, false>(a, tok, h, hk, lane, vrow);
         }
         float qv[EPT], kv[EPT], alpha[EPT];
 #pragma unroll
         for (int e = 0; e < EPT; ++e) { qv[e] = cur.q[e]; kv[e] = cur.k[e]; }
         float vr = cur.v;
         if constexpr (CONV) {
+            if (t > 0) __syncthreads();  // every lane has read the previous token's cx
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) {  // taps read here (L1) rather than held across the tokens
-                const float xq = qv[e], xk = kv[e];
-                qv[e] = round_to<TIn>(conv4_silu(__ldg(w4 + cq + e), hq[e][0], hq[e][1], hq[e][2], xq));
-                kv[e] = round_to<TIn>(conv4_silu(__ldg(w4 + ck + e), hkk[e][0], hkk[e][1], hkk[e][2], xk));
-                hq[e][0] = hq[e][1]; hq[e][1] = hq[e][2]; hq[e][2] = xq;
-                hkk[e][0] = hkk[e][1]; hkk[e][1] = hkk[e][2]; hkk[e][2] = xk;
+            for (int u = 0; u < kOwn; ++u) {
+                const int item = threadIdx.x + u * blockDim.x;
+                if (item < kItems) {
+                    const int gq = item / D, c = item % D;
+                    const TIn* src = gq == 0 ? static_cast<const TIn*>(a.q) + (tok * a.Hk + hk) * D
+                                   : (gq == 1 ? static_cast<const TIn*>(a.k) + (tok * a.Hk + hk) * D
+                                              : static_cast<const TIn*>(a.v) + vt * D);
+                    const float x = to_f32(src[c]);
+                    cx[item] = round_to<TIn>(conv4_silu(__ldg(w4 + chan[u]), hist[u][0], hist[u][1], hist[u][2], x));
+                    hist[u][0] = hist[u][1];
+                    hist[u][1] = hist[u][2];
+                    hist[u][2] = x;
+                }
             }
-            const float xv = vr;
-            vr = round_to<TIn>(conv4_silu(__ldg(w4 + cv), hv[0], hv[1], hv[2], xv));
-            hv[0] = hv[1]; hv[1] = hv[2]; hv[2] = xv;
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                qv[e] = cx[lane * EPT + e];
+                kv[e] = cx[D + lane * EPT + e];
+            }
+            vr = cx[2 * D + vrow];
         }
         if (a.g_per_channel) {
 #pragma unroll
@@ -239,21 +258,17 @@ __device__ __forceinline__ void decode_tokens(float (&s)[kRowsPerWarp][D / 32], 
         }
     }
     if constexpr (CONV) {
+        // the final history of the owned items (each thread read its own items' input history
+        // before the loop; with grouped heads the query/key items are written by one value head)
         if (a.conv.state_out) {
             float* so = a.conv.state_out + (long)slot * a.conv.dim * 3;
-            __syncthreads();  // every warp has read its input history (the update may be in place)
-            if (warp == 0 && h % grp == 0) {  // one writer per query/key head
 #pragma unroll
-                for (int e = 0; e < EPT; ++e)
+            for (int u = 0; u < kOwn; ++u) {
+                const int item = threadIdx.x + u * blockDim.x;
+                if (item < kItems && (item >= 2 * D || h % grp == 0))
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) {
-                        so[(long)(cq + e) * 3 + j] = hq[e][j];
-                        so[(long)(ck + e) * 3 + j] = hkk[e][j];
-                    }
+                    for (int j = 0; j < 3; ++j) so[(long)chan[u] * 3 + j] = hist[u][j];
             }
-            if (lane < kRowsPerWarp)
-#pragma unroll
-                for (int j = 0; j < 3; ++j) so[(long)cv * 3 + j] = hv[j];
         }
     }
 }
@@ -265,6 +280,7 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
     constexpr int EPT = D / 32;
     static_assert(D / kRowsPerWarp * 32 == D * 2, "one warp per 16 rows");
     __shared__ float ys[GATE ? D : 1];
+    __shared__ float cx[CONV ? 3 * D : 1];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int unit = blockIdx.x;  // n * H + h
@@ -279,7 +295,7 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
     float s[kRowsPerWarp][EPT];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::load(S + (long)i * D, s[i]);
-    decode_tokens<D, TIn, GATE, CONV>(s, a, n, h, slot, ys);
+    decode_tokens<D, TIn, GATE, CONV>(s, a, n, h, slot, ys, cx);
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::store(S + (long)i * D, s[i]);
 }
