@@ -332,8 +332,8 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
     __shared__ __align__(16) float Kd[kBlk][D];   // e^(G_last - G_j) . k_j
     __shared__ __align__(16) float gL[D];         // e^G_last
     __shared__ __align__(16) float zz[GATE ? kBlk : 1][GATE ? D : 1];
-    __shared__ __align__(16) float ys[GATE ? kBlk : 1][GATE ? D : 1];
-    __shared__ float bet[kBlk], Am[kBlk][kBlk], Mm[kBlk][kBlk], Uc[kBlk][kBlk], rinv[kBlk];
+    __shared__ float part[GATE ? kBlk : 1][NW];  // per warp: sum of y^2 over its 16 rows
+    __shared__ float bet[kBlk], Am[kBlk][kBlk], Mm[kBlk][kBlk], Uc[kBlk][kBlk];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x;  // n * H + h
     const int n = unit / a.H, h = unit % a.H;
@@ -433,12 +433,13 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < kBlk; ++j) { acc += Gs[j][c]; G[j] = acc; Gs[j][c] = acc; }
-            gL[c] = expf(G[kBlk - 1]);
+            gL[c] = __expf(G[kBlk - 1]);  // every exponent here is <= 0
 #pragma unroll
             for (int j = 0; j < kBlk; ++j) {
-                Wm[j][c] = expf(G[j]) * kn[j][c];
-                Qd[j][c] = expf(G[j]) * qn[j][c];
-                Kd[j][c] = expf(G[kBlk - 1] - G[j]) * kn[j][c];
+                const float eg = __expf(G[j]);
+                Wm[j][c] = eg * kn[j][c];
+                Qd[j][c] = eg * qn[j][c];
+                Kd[j][c] = __expf(G[kBlk - 1] - G[j]) * kn[j][c];
             }
         }
         __syncthreads();
@@ -456,14 +457,14 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
 #pragma unroll
                 for (int e = 0; e < EPT; ++e) {
                     const int c = c0 + e;
-                    part += x[c] * kn[j][c] * expf(Gs[i][c] - Gs[j][c]);
+                    part += x[c] * kn[j][c] * __expf(Gs[i][c] - Gs[j][c]);
                 }
             } else {
 #pragma unroll
                 for (int e = 0; e < EPT; ++e) part += x[c0 + e] * kn[j][c0 + e];
             }
             part = warp_sum(part);
-            if (!a.g_per_channel) part *= expf(Gs[i][0] - Gs[j][0]);
+            if (!a.g_per_channel) part *= __expf(Gs[i][0] - Gs[j][0]);
             if (lane == 0) {
                 if (isM) Mm[i][j] = part;
                 else Am[i][j] = bet[i] * part;
@@ -544,13 +545,16 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
             for (int j = 0; j <= i; ++j) y += Mm[i][j] * vn[j];
             yv[i] = y;
         }
-        // outputs (or the rows the gate normalises)
+        // outputs, or for the gate each warp's sum of y^2 over its 16 rows (lanes < 16)
 #pragma unroll
         for (int i = 0; i < kBlk; ++i) {
             const int t = t0 + i;
             const long vt = ((long)n * a.T + t) * a.H + h;
             if constexpr (GATE) {
-                if (lane < kRowsPerWarp) ys[i][vrow] = yv[i];
+                float sq = lane < kRowsPerWarp ? yv[i] * yv[i] : 0.f;
+#pragma unroll
+                for (int o = kRowsPerWarp / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                if (lane == 0) part[i][warp] = sq;
             } else {
                 if (t < a.T && (lane >> 4) == (i & 1)) store_out(a.out, vt * D + vrow, a.out_dtype, yv[i]);
             }
@@ -581,22 +585,22 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
             }
         }
         if constexpr (GATE) {
-            __syncthreads();
-            if (warp < kBlk) {  // RMS of token t0 + warp over the D output rows
-                float ss = 0.f;
+            __syncthreads();  // every warp's partial sums are in
+            if (lane < kRowsPerWarp) {
+                const float w = a.w ? a.w[vrow] : 1.0f;
 #pragma unroll
-                for (int e = 0; e < EPT; ++e) { const float y = ys[warp][c0 + e]; ss += y * y; }
-                ss = warp_sum(ss);
-                if (lane == 0) rinv[warp] = rsqrtf(ss / D + a.eps);
-            }
-            __syncthreads();
-            for (int e = tid; e < kBlk * D; e += blockDim.x) {
-                const int i = e / D, r = e % D, t = t0 + i;
-                if (t >= a.T) continue;
-                const long vt = ((long)n * a.T + t) * a.H + h;
-                const float z = zz[i][r];
-                const float w = a.w ? a.w[r] : 1.0f;
-                store_out(a.out, vt * D + r, a.out_dtype, w * ys[i][r] * rinv[i] * z * sigmoidf_(z));
+                for (int i = 0; i < kBlk; ++i) {
+                    const int t = t0 + i;
+                    if (t < a.T) {
+                        float ss = 0.f;
+#pragma unroll
+                        for (int ww = 0; ww < NW; ++ww) ss += part[i][ww];
+                        const long vt = ((long)n * a.T + t) * a.H + h;
+                        const float z = zz[i][vrow];
+                        store_out(a.out, vt * D + vrow, a.out_dtype,
+                                  w * yv[i] * rsqrtf(ss / D + a.eps) * z * sigmoidf_(z));
+                    }
+                }
             }
         }
         __syncthreads();  // the block's shared rows are rewritten by the next block
@@ -642,10 +646,11 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
 }
 
 template <int D, typename TIn, bool GATE, bool CONV>
-void launch_variant(const DecodeArgs& a, cudaStream_t s, bool blocks) {
-    dim3 grid((unsigned)((long)a.N * a.H)), block(D * 2);
-    if (blocks) decode_block_kernel<D, TIn, GATE, CONV><<<grid, block, 0, s>>>(a);
-    else decode_kernel<D, TIn, GATE, CONV><<<grid, block, 0, s>>>(a);
+cudaError_t launch_variant(const DecodeArgs& a, cudaStream_t s, bool blocks) {
+    const unsigned units = (unsigned)((long)a.N * a.H);
+    if (blocks) decode_block_kernel<D, TIn, GATE, CONV><<<units, D * 2, 0, s>>>(a);
+    else decode_kernel<D, TIn, GATE, CONV><<<units, D * 2, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 // The block form when a unit's tokens fill its blocks to within one token, or there are many of
@@ -658,13 +663,11 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
     bool blocks = a.T >= 3 && (a.T % kBlk == 0 || a.T % kBlk == kBlk - 1 || a.T >= 10);
     if (const char* env = getenv("GDN_DECODE_BLOCKS")) blocks = env[0] == '1';
     if (a.conv.w) {
-        if (a.z) launch_variant<D, TIn, true, true>(a, s, blocks);
-        else launch_variant<D, TIn, false, true>(a, s, blocks);
-    } else {
-        if (a.z) launch_variant<D, TIn, true, false>(a, s, blocks);
-        else launch_variant<D, TIn, false, false>(a, s, blocks);
+        if (a.z) return launch_variant<D, TIn, true, true>(a, s, blocks);
+        return launch_variant<D, TIn, false, true>(a, s, blocks);
     }
-    return cudaGetLastError();
+    if (a.z) return launch_variant<D, TIn, true, false>(a, s, blocks);
+    return launch_variant<D, TIn, false, false>(a, s, blocks);
 }
 
 }  // namespace
