@@ -1273,11 +1273,14 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 }
             }
             if (!last) {
-                tmem_wait_st();
+                // the products this signal starts read the shared-memory mirror and write other TMEM
+                // columns; the pre-decayed TMEM copy of S is needed only by the next S update, so
+                // its stores are waited for after the signal
                 fence_async_smem();
                 tc_fence_before();
                 if (bar_sync_or(1, 128, *abort_flag != 0)) break;
                 if (r == 0) mbar_arrive(&bars[SBF]);
+                tmem_wait_st();
             }
         }
     }
