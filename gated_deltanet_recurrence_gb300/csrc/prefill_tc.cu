@@ -1087,7 +1087,6 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 const uint64_t dK = dStageK0 + (uint64_t)((s * kStage) >> 4);
                 if (!mbar_wait(&bars[FULL0 + s], (c >> 1) & 1, kPolls)) { fail(); break; }
                 if (!mbar_wait(&bars[SBF], c & 1, kPolls)) { fail(); break; }
-                if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
                 if (*abort_flag) break;
                 tc_fence_after();
                 const uint32_t tDA = tDA0 + b * 64, tDO = tDO0 + b * 128;
@@ -1098,7 +1097,10 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                     mma_bf16_ss(tDA, dS + off, dSt + sWQ / 16 + off, kIdW, k > 0);
                 }
                 mma_commit(&bars[DA1]);
-                // while the state epilogue forms V_new: O = Q~ S^T (tokens as rows, M = 64)
+                // while the state epilogue forms V_new: O = Q~ S^T (tokens as rows, M = 64), once the
+                // output group has taken chunk c - 2's O out of this buffer
+                if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
+                tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
