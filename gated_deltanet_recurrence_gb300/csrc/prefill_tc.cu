@@ -1240,48 +1240,48 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             ok = mbar_wait(&bars[SFULL], c & 1, kPolls);
             if (!ok) fail();
             tc_fence_after();
-            // ---- S: mirror as bf16 operand, pre-decay by the next chunk's gamma ----
-            if (ok) {
-                uint32_t v[4][32];
+            // ---- S: mirror as bf16 operand (signalled), then pre-decay the TMEM copy by the next
+            //      chunk's gamma: the products the signal starts read the mirror and write other
+            //      TMEM columns, and only the next S update reads S.  After a timed-out wait (error
+            //      recorded) the loads still run, on garbage but in bounds: under a condition of
+            //      their own the 128 values would go to local memory. ----
+            uint32_t v[4][32];
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk) tmem_ld32(tS + lrow + blk * 32, v[blk]);
-                tmem_wait_ld();
+            for (int blk = 0; blk < 4; ++blk) tmem_ld32(tS + lrow + blk * 32, v[blk]);
+            tmem_wait_ld();
+            if (last) {
+                if (ok && a.final_state) {
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    float* f = reinterpret_cast<float*>(v[blk]);
-                    if (last) {
-                        if (a.final_state) {
-                            float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
+                    for (int blk = 0; blk < 4; ++blk) {
+                        float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4*>(dst + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8)
-                            st_sw128_chunk(Sb + (blk >> 1) * 16384, r, (blk & 1) * 4 + c8, f + 8 * c8);
-                        if constexpr (PC) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 t = *reinterpret_cast<const float4*>(gvec + blk * 32 + j);
-                                f[j] *= t.x; f[j + 1] *= t.y; f[j + 2] *= t.z; f[j + 3] *= t.w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) f[j] *= gnext;
-                        }
-                        tmem_st32(tS + lrow + blk * 32, v[blk]);
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<uint4*>(dst + j) = make_uint4(v[blk][j], v[blk][j + 1], v[blk][j + 2], v[blk][j + 3]);
                     }
                 }
-            }
-            if (!last) {
-                // the products this signal starts read the shared-memory mirror and write other TMEM
-                // columns; the pre-decayed TMEM copy of S is needed only by the next S update, so
-                // its stores are waited for after the signal
+            } else {
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4*>(Sb + (blk >> 1) * 16384 + sw128_offset(r, ((blk & 1) * 4 + c8) * 8)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(v[blk][8 * c8]), __uint_as_float(v[blk][8 * c8 + 1])),
+                                       pack_bf16x2(__uint_as_float(v[blk][8 * c8 + 2]), __uint_as_float(v[blk][8 * c8 + 3])),
+                                       pack_bf16x2(__uint_as_float(v[blk][8 * c8 + 4]), __uint_as_float(v[blk][8 * c8 + 5])),
+                                       pack_bf16x2(__uint_as_float(v[blk][8 * c8 + 6]), __uint_as_float(v[blk][8 * c8 + 7])));
                 fence_async_smem();
                 tc_fence_before();
                 if (bar_sync_or(1, 128, *abort_flag != 0)) break;
                 if (r == 0) mbar_arrive(&bars[SBF]);
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float gj = PC ? gvec[blk * 32 + j] : gnext;
+                        v[blk][j] = __float_as_uint(__uint_as_float(v[blk][j]) * gj);
+                    }
+                    tmem_st32(tS + lrow + blk * 32, v[blk]);
+                }
                 tmem_wait_st();
             }
         }
