@@ -503,13 +503,16 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
 
     for (int hf = 0; hf < 2; ++hf) {
         // (a) per-channel inclusive sums, in log2 units; e^(G_last) for the state pass
-        if (tid < 64) {
+        if (tid < 64) {  // all 64 loads of a channel in flight at once, then the running sum
             const float* gp = a.g + (t0 * a.H + h) * (long)kD + hf * 64 + tid;
             const long gs = (long)a.H * kD;
+            float gv[kC];
+#pragma unroll
+            for (int i = 0; i < kC; ++i) gv[i] = i < L ? __ldg(gp + i * gs) : 0.f;
             float acc = 0.f;
-#pragma unroll 16
+#pragma unroll
             for (int i = 0; i < kC; ++i) {
-                acc += i < L ? __ldg(gp + i * gs) : 0.f;
+                acc += gv[i];
                 GT[tid * LG + i] = acc * kLog2e;
             }
             a.gam[gh * kD + hf * 64 + tid] = ex2_approx(acc * kLog2e);
