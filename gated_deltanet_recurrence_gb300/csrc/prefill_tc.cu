@@ -51,7 +51,8 @@ constexpr uint64_t kPolls = 2000000000ull;  // bound on any single mbarrier wait
 
 struct WsLayout {
     long nch;          // chunk-head slots = max_chunks * H
-    size_t off_map, off_first, off_count, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, off_gam, off_ready, total;
+    size_t off_map, off_first, off_count, off_order, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, off_gam,
+        off_ready, total;
 };
 
 __host__ __device__ inline long max_chunks(int num_seqs, int total_T) { return (long)total_T / kC + num_seqs; }
@@ -65,6 +66,7 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
     w.off_map = o;   o = al(o + sizeof(int32_t) * mc);               // chunk -> sequence
     w.off_first = o; o = al(o + sizeof(int32_t) * (num_seqs + 1));   // first chunk of each sequence
     w.off_count = o; o = al(o + sizeof(int32_t) * 4);                 // number of chunks
+    w.off_order = o; o = al(o + sizeof(int32_t) * num_seqs);          // sequences, most chunks first
     w.off_W = o;     o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);
     w.off_Ut = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kD * kC);
     w.off_Aqk = o;   o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kC);
@@ -91,6 +93,7 @@ struct TcArgs {
     int32_t* chunk_seq;
     int32_t* chunk_first;
     int32_t* n_chunks;
+    int32_t* seq_order;  // sequences by decreasing chunk count (the two-kernel serial pass runs them in it)
     __nv_bfloat16* W;
     __nv_bfloat16* Ut;
     __nv_bfloat16* Aqk;
@@ -167,6 +170,25 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
         a.n_chunks[0] = part[1023];
         a.n_chunks[1] = longest;  // chunks of the longest sequence
         a.n_chunks[2] = 0;        // fused kernel: work counter of the preparing CTAs
+    }
+    // the order in which the serial pass starts the sequences: most chunks first, so that the long
+    // chains are not the last to begin (ties by index; more than 1024 sequences keep their order)
+    __syncthreads();  // part[] is reused for the chunk counts
+    if (a.num_seqs <= 1024) {
+        long bos, eos;
+        const int32_t c = (tid < a.num_seqs && seq_bounds(a, tid, bos, eos)) ? (int32_t)((eos - bos + kC - 1) / kC) : -1;
+        part[tid] = c;
+        __syncthreads();
+        if (tid < a.num_seqs) {
+            int rank = 0;
+            for (int m = 0; m < a.num_seqs; ++m) {
+                const int32_t cm = part[m];
+                rank += (cm > c) || (cm == c && m < tid);
+            }
+            a.seq_order[rank] = tid;
+        }
+    } else {
+        for (int n = tid; n < a.num_seqs; n += 1024) a.seq_order[n] = n;
     }
 }
 
@@ -1461,7 +1483,8 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
     // 1024-byte aligned base, derived by offsetting the shared array itself so that the compiler
     // keeps the shared address space (plain shared loads and stores, not generic ones)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
-    state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, a);
+    const int unit = a.seq_order[blockIdx.x / a.H] * a.H + blockIdx.x % a.H;  // longest sequences first
+    state_unit<PC>(sm, unit, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, a);
 }
 
 
@@ -1632,6 +1655,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.chunk_seq = reinterpret_cast<int32_t*>(ws + L.off_map);
     a.chunk_first = reinterpret_cast<int32_t*>(ws + L.off_first);
     a.n_chunks = reinterpret_cast<int32_t*>(ws + L.off_count);
+    a.seq_order = reinterpret_cast<int32_t*>(ws + L.off_order);
     a.W = reinterpret_cast<__nv_bfloat16*>(ws + L.off_W);
     a.Ut = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Ut);
     a.Aqk = reinterpret_cast<__nv_bfloat16*>(ws + L.off_Aqk);
