@@ -218,8 +218,9 @@ def oracle_rate(inp, H, seconds_budget=20.0, threads=None):
 # GPU measurements
 # ---------------------------------------------------------------------------------------------
 
-# time slices per sequence of the streamed end-to-end prefill step (host link overlapped with the kernels)
-E2E_PARTS = 2
+# time slices of each sequence in the streamed end-to-end prefill step, as shares of the sequence
+# (host link overlapped with the kernels); the short last slices keep the tail after the last copy short
+E2E_SPLIT = (3, 1)
 
 
 def ev():
@@ -278,7 +279,7 @@ def bench_prefill(args, dev):
     # ---- end to end through the ABI with host buffers ----
     # Every step copies all inputs in from pinned host memory and the outputs back.  The host link
     # (about 0.2 TB/s each way on this machine) takes 5x longer than the kernels, so the step is
-    # streamed: every sequence is cut into E2E_PARTS time slices (each a contiguous host range, so one
+    # streamed: every sequence is cut into time slices (E2E_SPLIT; each a contiguous host range, so one
     # copy per tensor), slice (s, p) is copied in on one stream, run by gdn_decay_from_logits +
     # gdn_chunk_fwd on another (one sequence; its initial state is slice p - 1's final state, in
     # place) and copied out on a third.  The copies of later slices overlap the kernels and the
@@ -291,19 +292,21 @@ def bench_prefill(args, dev):
     Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + A_log_h.numel() * A_log_h.element_size()
     d2h = out_h.numel() * out_h.element_size() + Sf_h.numel() * Sf_h.element_size()
-    P = E2E_PARTS
     Tn = total_T // n                      # tokens per sequence
-    Tp = Tn // P                           # tokens per slice (a multiple of the chunk)
-    assert Tn % P == 0 and Tp % 64 == 0
-    slices = [(sq, p_, sq * Tn + p_ * Tp) for sq in range(n) for p_ in range(P)]  # (sequence, slice, first token)
-    bufs = [{k_: torch.empty((Tp,) + t.shape[1:], dtype=t.dtype, device=dev) for k_, t in pinned.items()}
-            for _ in slices]
+    unit_ = Tn // sum(E2E_SPLIT)
+    assert unit_ * sum(E2E_SPLIT) == Tn and unit_ % 64 == 0  # slices are whole chunks
+    lens = [unit_ * w for w in E2E_SPLIT]
+    starts = [sum(lens[:p_]) for p_ in range(len(lens))]
+    # (sequence, slice, first token, length), slice-major: the first slices of every sequence first
+    slices = [(sq, p_, sq * Tn + starts[p_], lens[p_]) for p_ in range(len(lens)) for sq in range(n)]
+    bufs = [{k_: torch.empty((Ls,) + t.shape[1:], dtype=t.dtype, device=dev) for k_, t in pinned.items()}
+            for (_, _, _, Ls) in slices]
     A_log_d = torch.empty_like(A_log_h, device=dev)
-    g_p = [torch.empty(Tp, H, device=dev) for _ in slices]
-    b_p = [torch.empty(Tp, H, device=dev) for _ in slices]
-    o_p = [torch.empty(Tp, H, d, dtype=torch.bfloat16, device=dev) for _ in slices]
+    g_p = [torch.empty(Ls, H, device=dev) for (_, _, _, Ls) in slices]
+    b_p = [torch.empty(Ls, H, device=dev) for (_, _, _, Ls) in slices]
+    o_p = [torch.empty(Ls, H, d, dtype=torch.bfloat16, device=dev) for (_, _, _, Ls) in slices]
     S_e = torch.empty(n, H, d, d, device=dev)
-    ws_p = gdn.lib().gdn_chunk_fwd_workspace_size(1, Tp, H, d, d, gdn.GDN_BF16)
+    ws_p = gdn.lib().gdn_chunk_fwd_workspace_size(1, max(lens), H, d, d, gdn.GDN_BF16)
     ws_e = torch.empty(max(ws_p, 1), dtype=torch.uint8, device=dev)
     s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
@@ -317,14 +320,14 @@ def bench_prefill(args, dev):
         copied, ran = [], []
         with torch.cuda.stream(s_in):
             A_log_d.copy_(A_log_h, non_blocking=True)
-            for i, (_, _, t0) in enumerate(slices):
+            for i, (_, _, t0, Ls) in enumerate(slices):
                 for k_, t in pinned.items():
-                    bufs[i][k_].copy_(t[t0:t0 + Tp], non_blocking=True)
+                    bufs[i][k_].copy_(t[t0:t0 + Ls], non_blocking=True)
                 e_ = ev()
                 e_.record(s_in)
                 copied.append(e_)
         with torch.cuda.stream(s_run):
-            for i, (sq, p_, _) in enumerate(slices):
+            for i, (sq, p_, _, _) in enumerate(slices):
                 s_run.wait_event(copied[i])
                 x, S_seq = bufs[i], S_e[sq:sq + 1]
                 gdn.gdn_decay_from_logits(x["a"], A_log_d, b=x["b"], g_out=g_p[i], beta_out=b_p[i])
@@ -335,9 +338,9 @@ def bench_prefill(args, dev):
                 e_.record(s_run)
                 ran.append(e_)
         with torch.cuda.stream(s_out):
-            for i, (_, _, t0) in enumerate(slices):
+            for i, (_, _, t0, Ls) in enumerate(slices):
                 s_out.wait_event(ran[i])
-                out_h[t0:t0 + Tp].copy_(o_p[i], non_blocking=True)
+                out_h[t0:t0 + Ls].copy_(o_p[i], non_blocking=True)
             Sf_h.copy_(S_e, non_blocking=True)
         for s_ in (s_in, s_run, s_out):
             stream.wait_stream(s_)
