@@ -1,5 +1,7 @@
 // decode.cu -- gated delta rule decode on kept fp32 states (gdn_recurrent_step and
-// gdn_recurrent_multi_step, which is the same kernel with T tokens and a state pool).
+// gdn_recurrent_multi_step: T tokens per sequence from a state pool, token by token in
+// decode_kernel or, for several tokens, in blocks of four in the chunked form in
+// decode_block_kernel).
 //
 // "6.6 Gated DeltaNet" 6.6.8 and "[LLM Algorithms-2] Gated DeltaNet" section 4: per (sequence,
 // head) and per state row r (d_k contiguous), with alpha one value or one per key channel,

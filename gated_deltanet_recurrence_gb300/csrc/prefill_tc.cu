@@ -13,18 +13,26 @@
 //   O      = diag(e^gc qs) Q S^T + Aqk V_new
 //   S'     = e^{gc_last} S + V_new^T diag(e^{gc_last - gc} kinv) K
 //
-// Three launches on the caller's stream:
-//   chunk_map_kernel    numbers the chunks of all sequences (varlen) in the workspace.
+// Launches on the caller's stream:
+//   chunk_map_kernel    numbers the chunks of all sequences (varlen) in the workspace, and ranks the
+//                       sequences by length for the serial pass.
+//   then either (few (sequence, head) units: at most half the SMs)
+//   chunk_fused_kernel  one cooperative launch, one CTA per SM: CTAs 0 .. units-1 run the serial
+//                       pass, the others prepare chunks (three at a time) and publish each by a
+//                       ready flag the serial pass acquires;
+//   or
 //   chunk_prep_kernel   one CTA per (chunk, head), all in parallel: TMA loads of K, Q, V; one MMA
 //                       [K;Q][K;Q]^T (M=128, N=128, K=128); the triangular solve on the CUDA
 //                       cores; two MMAs W^T = K^T T'^T and U^T = V^T T''^T (MN-major A from the
-//                       same K / V tiles); W, U^T, Aqk (bf16) and per-token factors to workspace.
+//                       same K / V tiles); W, U^T, Aqk, the scaled rows Q~ and K~ (bf16) and
+//                       per-token factors to the workspace;
 //   chunk_state_kernel  one CTA per (sequence, head), walking the chunks in order, warp-specialised:
 //                       warp 0 issues TMA loads of the next chunk's operands (two-stage ring),
 //                       warp 1 issues the MMAs (warps 0-3 run with few registers), warps 4-7 run
-//                       the state epilogue (the serial chain: V_new, then S), warps 8-11 the
-//                       output epilogue (O and the fused RMSNorm * SiLU gate).  The state S is fp32 in TMEM (lanes = rows d_v,
-//                       columns = d_k) and is mirrored as a bf16 operand tile in shared memory.
+//                       the state epilogue (the serial chain: V_new, then S), warps 8-11 and 12-15
+//                       the output epilogue of alternate chunks (O and the fused RMSNorm * SiLU
+//                       gate).  The state S is fp32 in TMEM (lanes = rows d_v, columns = d_k) and
+//                       is mirrored as a bf16 operand tile in shared memory.
 //   TMEM per state CTA: S [0,128), two buffers of S W^T [128,256), two of O (tokens as rows) [256,512).
 //
 // Every mbarrier wait is bounded; on a timeout the kernel records GDN_ERR_TIMEOUT and its roles
@@ -228,18 +236,6 @@ __device__ __forceinline__ void st_sw128_chunk(uint8_t* tile, int row, int chunk
     p.z = pack_bf16x2(v[4], v[5]);
     p.w = pack_bf16x2(v[6], v[7]);
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, chunk * 8)) = p;
-}
-
-__device__ __forceinline__ void ld_sw128_chunk(const uint8_t* tile, int row, int chunk, float* v) {
-    uint4 p = *reinterpret_cast<const uint4*>(tile + sw128_offset(row, chunk * 8));
-    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-        float2 f = __bfloat1622float2(t);
-        v[2 * e] = f.x;
-        v[2 * e + 1] = f.y;
-    }
 }
 
 // ---- 2. chunk preparation (parallel) ------------------------------------------------------------
@@ -1025,7 +1021,7 @@ constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns of the state CTA: S [0,128); S W^T (M=128, 64 columns) x 2 buffers [128,256);
 // O = Q~ S^T + Aqk V_new (M=64, rows = tokens, 128 columns) x 2 buffers [256,512).
-// The serial pass of one (sequence, head) unit by the whole CTA (384 threads).  When a.ready is set
+// The serial pass of one (sequence, head) unit by the whole CTA (512 threads).  When a.ready is set
 // (fused kernel) the chunks' workspace entries are produced concurrently by other CTAs: the TMA
 // producer and the state epilogue wait for a chunk's ready flag before they read its entries.  The
 // epilogue's read-only-path loads (__ldg) of those entries stay correct there: every entry is
