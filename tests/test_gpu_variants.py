@@ -283,3 +283,30 @@ def test_conv_prefill_then_decode_continues_the_sequence():
     err = np.linalg.norm(yd.cpu().double().numpy()[0] - y_ref[T], axis=1) / np.linalg.norm(y_ref[T], axis=1)
     assert err.max() <= TOL_BF16
     assert rel_l2_states(S.cpu(), S_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 7])
+def test_multi_step_conv_history_in_place(T):
+    """With H_k == H the convolution history may be updated in place: every read of the input history
+    happens before the writes (token-by-token form at T = 1, 2; block form at T = 4, 7, where only
+    the first block reads it).  In place and out of place give the same outputs, states and
+    histories, bit for bit."""
+    N, H, d, slots = 9, 4, 128, 12
+    q, k, v, g, beta, S0, w, cs, z = _decode_case(N, T, H, H, d, torch.bfloat16, False, True, seed=120 + T)
+    idx = torch.randperm(slots, generator=torch.Generator().manual_seed(7))[:N].to(torch.int32)
+    pool = torch.zeros(slots, H, d, d)
+    pool[idx.long()] = S0
+    C = synthetic.conv_dim(H, H, d)
+    hist = torch.randn(slots, C, 3, generator=torch.Generator().manual_seed(8))
+    res = []
+    for in_place in (False, True):
+        P = pool.to(DEV)
+        cin = hist.to(DEV)
+        cout = cin if in_place else torch.zeros_like(cin)
+        y = gdn.gdn_recurrent_multi_step(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), P,
+                                         state_indices=idx.to(DEV), conv_weight=w.to(DEV), conv_state=cin,
+                                         conv_state_out=cout, gate_z=z.to(DEV), out_dtype=torch.float32)
+        assert gdn.gdn_get_device_error() == 0
+        res.append((y.cpu(), P.cpu(), cout.cpu()[idx.long()]))
+    for a_, b_ in zip(res[0], res[1]):
+        assert torch.equal(a_, b_)
