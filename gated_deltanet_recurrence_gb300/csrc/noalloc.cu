@@ -60,6 +60,15 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
     void* ws = nullptr;
     if (need > 0) {
+        // Argument errors first, before the CUDA runtime is touched: gdn_chunk_fwd checks every
+        // argument on the host ahead of its workspace, so without one it answers
+        // GDN_ERR_WORKSPACE exactly when everything else is valid, and launches nothing.
+        const int rc = gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, num_seqs, total_T, H, H_k, d_k,
+                                     d_v, qkv_dtype, decay, scale, use_qk_l2norm, conv_weight,
+                                     conv_state_in, conv_state_out, initial_state, final_state,
+                                     gate_z, norm_weight, norm_eps, out, out_dtype, nullptr, 0,
+                                     stream);
+        if (rc != GDN_ERR_WORKSPACE) return rc;
         ws = scratch_ptr();
         if (!ws) return GDN_ERR_CUDA;
     }

@@ -157,3 +157,29 @@ def test_recurrent_multi_step_rejects_bad_arguments():
     assert ms(w=P) == -1
     assert ms(H=2, Hk=4) == -1
     assert ms(H=8, Hk=2, cw=P, cin=P, cout=P) == -1
+
+
+def test_chunk_fwd_noalloc_checks_arguments_before_cuda():
+    """The no-allocation entry point reports argument errors exactly as gdn_chunk_fwd does, on the
+    host, without first touching the CUDA runtime for its scratch array (no GPU here: a call that
+    reached the runtime would answer GDN_ERR_CUDA instead)."""
+    L = gdn.lib()
+
+    def na(**kw):
+        a = dict(q=P, k=P, v=P, g=P, beta=P, cu=NUL, num_seqs=1, total_T=64, H=2, Hk=2, dk=128,
+                 dv=128, dt=1, decay=0, scale=0.0, l2=1, cw=NUL, cin=NUL, cout=NUL, S0=NUL, Sf=NUL,
+                 z=NUL, w=NUL, eps=1e-6, out=P, odt=1, stream=NUL)
+        a.update(kw)
+        return L.gdn_chunk_fwd_noalloc(*a.values())
+
+    assert na(q=NUL) == -1
+    assert na(out=NUL) == -1
+    assert na(dt=7) == -2
+    assert na(odt=4) == -2
+    assert na(dk=96, dv=96) == -7
+    assert na(H=6, Hk=4) == -1
+    assert na(w=P) == -1
+    assert na(k=ctypes.c_void_p(0x10004)) == -1
+    assert na(cin=P) == -1
+    assert na(num_seqs=1, total_T=64 * 2048, H=16, Hk=16) == -4   # beyond the fixed array
+    assert na(num_seqs=0) == -1
