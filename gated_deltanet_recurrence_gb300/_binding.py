@@ -1,8 +1,9 @@
 """ctypes binding of libgdn.so: same names as the C ABI (include/gdn.h), torch tensors in.
 
-Argument marshalling only: shapes are read from the tensors, outputs that the caller does not
-pass are allocated with torch, and the call goes to the library on the current torch CUDA stream
-(or the stream given).  Every computation happens in the library's CUDA kernels; there is no
+Argument marshalling only: shapes are read from the tensors, every tensor is checked to sit on
+the call's device and to hold at least what the call touches (the library sees bare pointers),
+outputs that the caller does not pass are allocated with torch, and the call goes to the library
+with the tensors' device current, on that device's current torch stream (or the stream given).  Every computation happens in the library's CUDA kernels; there is no
 fallback: if libgdn.so is missing or cannot be loaded, every call raises.
 """
 from __future__ import annotations
@@ -99,12 +100,35 @@ def _f32(t, name):
     return t
 
 
-def _stream(stream):
+def _sizes(ref, **tensors):
+    """The library sees only pointers, so the binding refuses, before the call, a tensor on another
+    device than `ref` or holding fewer elements than the call reads or writes through it.
+    Each keyword is name=(tensor or None, elements the call touches)."""
+    for name, (t, numel) in tensors.items():
+        if t is None:
+            continue
+        if t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device}, the call runs on {ref.device}")
+        if t.numel() < numel:
+            raise ValueError(f"{name} holds {t.numel()} elements; the call touches {numel}")
+
+
+def _stream(stream, ref=None):
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(ref.device if ref is not None else None).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
+
+
+def _run(ref, fn, *args):
+    """Call library function `fn` with the device of `ref` current: the library launches its
+    kernels on the calling thread's current device."""
+    dev = ref.get_device()
+    if dev == torch.cuda.current_device():
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def _check(fn, rc):
@@ -156,16 +180,27 @@ def gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scale=0.0, u
                     ("final_state", final_state), ("gate_z", gate_z), ("norm_weight", norm_weight)):
         _f32(t, name)
     _conv_f32(conv_weight, conv_state, conv_state_out)
+    conv_dim = 2 * H_k * d_k + H * d_v
+    _sizes(q, k=(k, total_T * H_k * d_k), v=(v, total_T * H * d_v),
+           g=(g, total_T * H * (1 if g.dim() == 2 else d_k)), beta=(beta, total_T * H),
+           cu_seqlens=(cu_seqlens, num_seqs + 1), initial_state=(initial_state, num_seqs * H * d_v * d_k),
+           final_state=(final_state, num_seqs * H * d_v * d_k), gate_z=(gate_z, total_T * H * d_v),
+           norm_weight=(norm_weight, d_v), out=(out, total_T * H * d_v),
+           conv_weight=(conv_weight, conv_dim * GDN_CONV_KERNEL),
+           conv_state=(conv_state, num_seqs * conv_dim * (GDN_CONV_KERNEL - 1)),
+           conv_state_out=(conv_state_out, num_seqs * conv_dim * (GDN_CONV_KERNEL - 1)),
+           workspace=(workspace, 0))
     L = lib()
     ws_need = L.gdn_chunk_fwd_workspace_size(num_seqs, total_T, H, d_k, d_v, dt)
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
-    rc = L.gdn_chunk_fwd(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs, total_T,
-                         H, H_k, d_k, d_v, dt, _decay_mode(g, 2), float(scale),
-                         int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state),
-                         _p(conv_state_out), _p(initial_state), _p(final_state), _p(gate_z),
-                         _p(norm_weight), float(norm_eps), _p(out), odt, _p(workspace),
-                         workspace.numel() if workspace is not None else 0, _stream(stream))
+    rc = _run(q, L.gdn_chunk_fwd,
+              _p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs, total_T, H, H_k, d_k,
+              d_v, dt, _decay_mode(g, 2), float(scale), int(bool(use_qk_l2norm)), _p(conv_weight),
+              _p(conv_state), _p(conv_state_out), _p(initial_state), _p(final_state), _p(gate_z),
+              _p(norm_weight), float(norm_eps), _p(out), odt, _p(workspace),
+              workspace.numel() * workspace.element_size() if workspace is not None else 0,
+              _stream(stream, q))
     _check("gdn_chunk_fwd", rc)
     return out, final_state
 
@@ -191,12 +226,20 @@ def gdn_chunk_fwd_noalloc(q, k, v, g, beta, cu_seqlens=None, num_seqs=None, scal
                     ("final_state", final_state), ("gate_z", gate_z), ("norm_weight", norm_weight)):
         _f32(t, name)
     _conv_f32(conv_weight, conv_state, conv_state_out)
-    rc = lib().gdn_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs,
-                                     total_T, H, H_k, d_k, d_v, dt, _decay_mode(g, 2), float(scale),
-                                     int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state),
-                                     _p(conv_state_out), _p(initial_state), _p(final_state),
-                                     _p(gate_z), _p(norm_weight), float(norm_eps), _p(out), _dt(out),
-                                     _stream(stream))
+    conv_dim = 2 * H_k * d_k + H * d_v
+    _sizes(q, k=(k, total_T * H_k * d_k), v=(v, total_T * H * d_v),
+           g=(g, total_T * H * (1 if g.dim() == 2 else d_k)), beta=(beta, total_T * H),
+           cu_seqlens=(cu_seqlens, num_seqs + 1), initial_state=(initial_state, num_seqs * H * d_v * d_k),
+           final_state=(final_state, num_seqs * H * d_v * d_k), gate_z=(gate_z, total_T * H * d_v),
+           norm_weight=(norm_weight, d_v), out=(out, total_T * H * d_v),
+           conv_weight=(conv_weight, conv_dim * GDN_CONV_KERNEL),
+           conv_state=(conv_state, num_seqs * conv_dim * (GDN_CONV_KERNEL - 1)),
+           conv_state_out=(conv_state_out, num_seqs * conv_dim * (GDN_CONV_KERNEL - 1)))
+    rc = _run(q, lib().gdn_chunk_fwd_noalloc,
+              _p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), num_seqs, total_T, H, H_k, d_k,
+              d_v, dt, _decay_mode(g, 2), float(scale), int(bool(use_qk_l2norm)), _p(conv_weight),
+              _p(conv_state), _p(conv_state_out), _p(initial_state), _p(final_state), _p(gate_z),
+              _p(norm_weight), float(norm_eps), _p(out), _dt(out), _stream(stream, q))
     _check("gdn_chunk_fwd_noalloc", rc)
     return out, final_state
 
@@ -220,10 +263,18 @@ def gdn_recurrent_step(q, k, v, g, beta, state, scale=0.0, use_qk_l2norm=True, c
                     ("norm_weight", norm_weight)):
         _f32(t, name)
     _conv_f32(conv_weight, conv_state, conv_state_out)
-    rc = lib().gdn_recurrent_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state), N, H, H_k, d_k,
-                                  d_v, dt, _decay_mode(g, 2), float(scale), int(bool(use_qk_l2norm)),
-                                  _p(conv_weight), _p(conv_state), _p(conv_state_out), _p(gate_z),
-                                  _p(norm_weight), float(norm_eps), _p(out), odt, _stream(stream))
+    conv_dim = 2 * H_k * d_k + H * d_v
+    _sizes(q, k=(k, N * H_k * d_k), v=(v, N * H * d_v), g=(g, N * H * (1 if g.dim() == 2 else d_k)),
+           beta=(beta, N * H), state=(state, N * H * d_v * d_k), gate_z=(gate_z, N * H * d_v),
+           norm_weight=(norm_weight, d_v), out=(out, N * H * d_v),
+           conv_weight=(conv_weight, conv_dim * GDN_CONV_KERNEL),
+           conv_state=(conv_state, N * conv_dim * (GDN_CONV_KERNEL - 1)),
+           conv_state_out=(conv_state_out, N * conv_dim * (GDN_CONV_KERNEL - 1)))
+    rc = _run(q, lib().gdn_recurrent_step,
+              _p(q), _p(k), _p(v), _p(g), _p(beta), _p(state), N, H, H_k, d_k, d_v, dt,
+              _decay_mode(g, 2), float(scale), int(bool(use_qk_l2norm)), _p(conv_weight),
+              _p(conv_state), _p(conv_state_out), _p(gate_z), _p(norm_weight), float(norm_eps),
+              _p(out), odt, _stream(stream, q))
     _check("gdn_recurrent_step", rc)
     return out
 
@@ -250,12 +301,19 @@ def gdn_recurrent_multi_step(q, k, v, g, beta, state_pool, state_indices=None, s
                     ("norm_weight", norm_weight)):
         _f32(t, name)
     _conv_f32(conv_weight, conv_state, conv_state_out)
-    rc = lib().gdn_recurrent_multi_step(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool),
-                                        state_pool.shape[0], _p(state_indices), N, T, H, H_k, d_k,
-                                        d_v, dt, _decay_mode(g, 3), float(scale),
-                                        int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state),
-                                        _p(conv_state_out), _p(gate_z), _p(norm_weight),
-                                        float(norm_eps), _p(out), odt, _stream(stream))
+    conv_dim, slots = 2 * H_k * d_k + H * d_v, state_pool.shape[0]
+    _sizes(q, k=(k, N * T * H_k * d_k), v=(v, N * T * H * d_v),
+           g=(g, N * T * H * (1 if g.dim() == 3 else d_k)), beta=(beta, N * T * H),
+           state_pool=(state_pool, slots * H * d_v * d_k), state_indices=(state_indices, N),
+           gate_z=(gate_z, N * T * H * d_v), norm_weight=(norm_weight, d_v), out=(out, N * T * H * d_v),
+           conv_weight=(conv_weight, conv_dim * GDN_CONV_KERNEL),
+           conv_state=(conv_state, slots * conv_dim * (GDN_CONV_KERNEL - 1)),
+           conv_state_out=(conv_state_out, slots * conv_dim * (GDN_CONV_KERNEL - 1)))
+    rc = _run(q, lib().gdn_recurrent_multi_step,
+              _p(q), _p(k), _p(v), _p(g), _p(beta), _p(state_pool), state_pool.shape[0],
+              _p(state_indices), N, T, H, H_k, d_k, d_v, dt, _decay_mode(g, 3), float(scale),
+              int(bool(use_qk_l2norm)), _p(conv_weight), _p(conv_state), _p(conv_state_out),
+              _p(gate_z), _p(norm_weight), float(norm_eps), _p(out), odt, _stream(stream, q))
     _check("gdn_recurrent_multi_step", rc)
     return out
 
@@ -271,8 +329,10 @@ def gdn_gate_rmsnorm_silu(y, z, norm_weight=None, eps=1e-6, out=None, out_dtype=
         odt = _dt(out)
     _f32(z, "z")
     _f32(norm_weight, "norm_weight")
-    rc = lib().gdn_gate_rmsnorm_silu(_p(y), _dt(y), _p(z), _p(norm_weight), float(eps), _p(out), odt,
-                                     rows, d_v, _stream(stream))
+    _sizes(y, z=(z, rows * d_v), norm_weight=(norm_weight, d_v), out=(out, rows * d_v))
+    rc = _run(y, lib().gdn_gate_rmsnorm_silu,
+              _p(y), _dt(y), _p(z), _p(norm_weight), float(eps), _p(out), odt, rows, d_v,
+              _stream(stream, y))
     _check("gdn_gate_rmsnorm_silu", rc)
     return out
 
@@ -286,8 +346,11 @@ def gdn_decay_from_logits(a, A_log, dt_bias=None, b=None, g_out=None, beta_out=N
         g_out = torch.empty_like(a)
     if b is not None and beta_out is None:
         beta_out = torch.empty_like(b)
-    rc = lib().gdn_decay_from_logits(_p(a), _p(A_log), _p(dt_bias), _p(b), _p(g_out), _p(beta_out),
-                                     total_T, H, _stream(stream))
+    _sizes(a, A_log=(A_log, H), dt_bias=(dt_bias, H), b=(b, total_T * H), g_out=(g_out, total_T * H),
+           beta_out=(beta_out, total_T * H))
+    rc = _run(a, lib().gdn_decay_from_logits,
+              _p(a), _p(A_log), _p(dt_bias), _p(b), _p(g_out), _p(beta_out), total_T, H,
+              _stream(stream, a))
     _check("gdn_decay_from_logits", rc)
     return (g_out, beta_out) if b is not None else g_out
 
