@@ -511,6 +511,55 @@ def test_conv_varlen_split_and_state():
 
 
 # --------------------------------------------------------------------------------------
+# q/k normalisation and the query scale: "6.6 Gated DeltaNet" 6.6.4 (x / sqrt(sum x^2 + 1e-6),
+# q scaled by 1/sqrt(d_k))
+# --------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("form", ["recurrence", "chunked4"])
+def test_qk_normalisation_and_scale_closed_form(form):
+    """One token from a zero state with beta = 1 and q = k = delta u (u a unit vector): the state is
+    v k^T / sqrt(delta^2 + eps) and y = S q_hat = v * scale * delta^2 / (delta^2 + eps).  With
+    delta^2 = eps the factor is exactly one half, which fixes where eps sits; with the
+    normalisation off, y = v * scale * delta^2."""
+    run = {"recurrence": oracle.recurrence,
+           "chunked4": lambda *a, **kw: oracle.chunked(*a, C=4, **kw)}[form]
+    rng = np.random.default_rng(21)
+    dk, dv = 8, 5
+    u = rng.standard_normal(dk)
+    u /= np.linalg.norm(u)
+    v = rng.standard_normal((1, 1, dv))
+    g, beta = np.zeros((1, 1)), np.ones((1, 1))
+    for delta2, scale in [(1e-6, None), (1e-6, 0.3), (4.0, None)]:
+        x = (math.sqrt(delta2) * u)[None, None, :]
+        y, _ = run(x, x, v, g, beta, batch=1, scale=scale)
+        sc = 1 / math.sqrt(dk) if scale is None else scale
+        np.testing.assert_allclose(y[0, 0], v[0, 0] * sc * delta2 / (delta2 + 1e-6), rtol=1e-12)
+        y, _ = run(x, x, v, g, beta, batch=1, scale=scale, use_qk_l2norm=False)
+        np.testing.assert_allclose(y[0, 0], v[0, 0] * sc * delta2, rtol=1e-12)
+
+
+@pytest.mark.parametrize("form", ["recurrence", "chunked16"])
+def test_output_invariant_to_raw_qk_scale(form):
+    """With the normalisation on, multiplying the raw q or k of any token by a positive constant
+    changes nothing beyond the eps term (relative ~eps / |x|^2)."""
+    run = {"recurrence": oracle.recurrence,
+           "chunked16": lambda *a, **kw: oracle.chunked(*a, C=16, **kw)}[form]
+    rng = np.random.default_rng(22)
+    T, H, dk, dv = 37, 2, 16, 8
+    # raw norms around 40, so the eps term stays below 1e-8 relative even after scaling by 0.3
+    q, k = 10 * rng.standard_normal((T, H, dk)), 10 * rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    g, beta = -rng.uniform(0, 1, (T, H)), rng.uniform(0, 1, (T, H))
+    S0 = rng.standard_normal((1, H, dv, dk)) * 0.1
+    y0, s0 = run(q, k, v, g, beta, batch=1, initial_state=S0)
+    cq = rng.uniform(0.3, 5.0, (T, H, 1))
+    ck = rng.uniform(0.3, 5.0, (T, H, 1))
+    y1, s1 = run(q * cq, k * ck, v, g, beta, batch=1, initial_state=S0)
+    np.testing.assert_allclose(y1, y0, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(s1, s0, rtol=1e-6, atol=1e-9)
+
+
+# --------------------------------------------------------------------------------------
 # planted mistakes: each mutation of the oracle must be caught by a pin above
 # --------------------------------------------------------------------------------------
 
@@ -552,6 +601,42 @@ MUTATIONS = {
     # SiLU left out of the convolution
     "conv_no_silu": ("out[(bos + t) * channels + c] = silu ? acc * sigmoid(acc) : acc;",
                      "out[(bos + t) * channels + c] = acc;"),
+    # the query left unnormalised in the token recurrence
+    "query_unnormalised": ("l2_normalise(qt, qn, dk, s->use_l2);", "l2_normalise(qt, qn, dk, 0);"),
+    # the key left unnormalised in the chunked form
+    "chunk_key_unnormalised": ("l2_normalise(s->k + t * s->qk_stride, K + (long)i * dk, dk, s->use_l2);",
+                               "l2_normalise(s->k + t * s->qk_stride, K + (long)i * dk, dk, 0);"),
+    # eps outside the square root of the normalisation
+    "l2_eps_outside_sqrt": ("1.0 / sqrt(ss + L2_EPS)", "1.0 / (sqrt(ss) + L2_EPS)"),
+    # query scale dropped in the token recurrence
+    "query_scale_dropped": ("for (int j = 0; j < dk; ++j) qn[j] *= s->scale;",
+                            "for (int j = 0; j < dk; ++j) qn[j] *= 1.0;"),
+    # the initial state ignored by the token recurrence
+    "initial_state_ignored": ("    if (s->S0) memcpy(S, s->S0, sizeof(double) * dv * dk);\n\n    for (int t = 0;",
+                              "\n\n    for (int t = 0;"),
+    # beta left out of U = T diag(beta) V in the chunked form
+    "chunk_u_without_beta": ("acc += attn[(long)i * L + j] * bt[j] * V[(long)j * dv + r];",
+                             "acc += attn[(long)i * L + j] * V[(long)j * dv + r];"),
+    # the decay left out of W = T diag(beta e^gc) K
+    "chunk_w_without_decay": ("acc += attn[(long)i * L + j] * bt[j] * exp(gcum[j]) * K[(long)j * dk + x];",
+                              "acc += attn[(long)i * L + j] * bt[j] * K[(long)j * dk + x];"),
+    # the diagonal kept in the strictly lower A
+    "chunk_a_with_diagonal": ("                if (j < i) {", "                if (j <= i) {"),
+    # the diagonal dropped from the intra-chunk Q K^T mask
+    "chunk_qk_strict": ("                if (j <= i)\n", "                if (j < i)\n"),
+    # the inter-chunk term not decayed to the token
+    "chunk_inter_undecayed": ("                inter *= exp(gcum[i]);", "                inter *= 1.0;"),
+    # SiLU replaced by the bare sigmoid in the gate
+    "gate_sigmoid_not_silu": ("out[r * dv + c] = wc * yr[c] * inv * zr[c] * sigmoid(zr[c]);",
+                              "out[r * dv + c] = wc * yr[c] * inv * sigmoid(zr[c]);"),
+    # the norm weight ignored
+    "gate_weight_ignored": ("double wc = w ? w[c] : 1.0;", "double wc = 1.0;"),
+    # dt_bias left out of the softplus
+    "softplus_without_bias": ("g[i] = -exp(A_log[h]) * softplus(a[i] + bias);",
+                              "g[i] = -exp(A_log[h]) * softplus(a[i]);"),
+    # A_log used as A
+    "a_log_not_exponentiated": ("g[i] = -exp(A_log[h]) * softplus(a[i] + bias);",
+                                "g[i] = -A_log[h] * softplus(a[i] + bias);"),
 }
 
 
@@ -590,6 +675,9 @@ PIN_TESTS = [
     test_conv_impulse_response,
     test_conv_matches_library_conv1d,
     test_conv_varlen_split_and_state,
+    test_gates_from_logits,
+    lambda: [test_qk_normalisation_and_scale_closed_form(f) for f in ("recurrence", "chunked4")],
+    lambda: [test_output_invariant_to_raw_qk_scale(f) for f in ("recurrence", "chunked16")],
 ]
 
 
