@@ -14,8 +14,10 @@ from ._binding import (  # noqa: F401
     gdn_get_device_error,
     gdn_recurrent_multi_step,
     gdn_recurrent_step,
+    gdn_selftest_bounded_wait,
     lib,
 )
 
-__all__ = ["gdn_chunk_fwd", "gdn_chunk_fwd_noalloc", "gdn_recurrent_step", "gdn_recurrent_multi_step", "gdn_gate_rmsnorm_silu", "gdn_decay_from_logits",
-           "gdn_get_device_error", "GdnError", "lib", "GDN_F32", "GDN_BF16"]
+__all__ = ["gdn_chunk_fwd", "gdn_chunk_fwd_noalloc", "gdn_recurrent_step", "gdn_recurrent_multi_step",
+           "gdn_gate_rmsnorm_silu", "gdn_decay_from_logits", "gdn_get_device_error",
+           "gdn_selftest_bounded_wait", "GdnError", "lib", "GDN_F32", "GDN_BF16"]

@@ -44,6 +44,7 @@ SIGNATURES = {
                                    _fp, _fp, _fp, _fp, _fp, _fp, _fp, _f, _vp, _i, _vp]),
     "gdn_get_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "gdn_status_string": (ctypes.c_char_p, [_i]),
+    "gdn_selftest_bounded_wait": (_i, [ctypes.c_ulonglong, _vp, _vp]),
 }
 
 
@@ -353,6 +354,20 @@ def gdn_decay_from_logits(a, A_log, dt_bias=None, b=None, g_out=None, beta_out=N
               _stream(stream, a))
     _check("gdn_decay_from_logits", rc)
     return (g_out, beta_out) if b is not None else g_out
+
+
+def gdn_selftest_bounded_wait(limit_ns, status=None, stream=None):
+    """Run the library's bounded device wait on a phase that never completes (limit_ns in
+    [1e3, 1e9]); returns the int32 device tensor the kernel writes its status to
+    (GDN_ERR_TIMEOUT = -6 once the wait has given up)."""
+    if status is None:
+        status = torch.full((1,), 1, dtype=torch.int32, device="cuda")
+    if status.dtype != torch.int32 or status.numel() < 1:
+        raise ValueError("status must be an int32 tensor with at least one element")
+    rc = _run(status, lib().gdn_selftest_bounded_wait, int(limit_ns), _p(status),
+              _stream(stream, status))
+    _check("gdn_selftest_bounded_wait", rc)
+    return status
 
 
 def gdn_get_device_error(stream=None) -> int:

@@ -238,6 +238,18 @@ int gdn_get_device_error(void* stream, int* device_status);
 /* Human-readable name of a gdn_status value (static string). */
 const char* gdn_status_string(int status);
 
+/*
+ * gdn_selftest_bounded_wait -- a check of the bounded device wait every tensor-core kernel uses
+ * (the pages have no counterpart: it belongs to this library's failure handling).  One thread
+ * waits on an mbarrier phase that nothing completes, with that same wait bounded at limit_ns
+ * nanoseconds (at least limit_ns of wall time, at most limit_ns x 2.1 GHz / SM clock plus 0.1 ms);
+ * the wait gives up and the kernel writes GDN_ERR_TIMEOUT to *device_status, a caller-owned
+ * device int (4-byte aligned), and returns.  Nothing faults or hangs, and the context stays usable.
+ * Asynchronous on `stream`.  Returns GDN_OK once launched, GDN_ERR_ARG for a null or misaligned
+ * status or limit_ns outside [1e3, 1e9], GDN_ERR_LAUNCH if the launch failed.
+ */
+int gdn_selftest_bounded_wait(unsigned long long limit_ns, int* device_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,6 +84,8 @@ int main(void)
                                 GDN_DECAY_PER_HEAD, 0.0f, 1, NULL, NULL, NULL, NULL, NULL, NULL,
                                 NULL, 1e-6f, DP, GDN_BF16, NULL) == GDN_ERR_ARG);
     CHECK(gdn_get_device_error(NULL, NULL) == GDN_ERR_ARG);
+    CHECK(gdn_selftest_bounded_wait(1000000ull, NULL, NULL) == GDN_ERR_ARG);
+    CHECK(gdn_selftest_bounded_wait(10ull, (int*)fake_storage, NULL) == GDN_ERR_ARG);
 
     if (failures == 0)
         printf("c consumer ok\n");

@@ -183,3 +183,11 @@ def test_chunk_fwd_noalloc_checks_arguments_before_cuda():
     assert na(cin=P) == -1
     assert na(num_seqs=1, total_T=64 * 2048, H=16, Hk=16) == -4   # beyond the fixed array
     assert na(num_seqs=0) == -1
+
+
+def test_selftest_bounded_wait_checks_arguments():
+    L = gdn.lib()
+    assert L.gdn_selftest_bounded_wait(1_000_000, NUL, NUL) == -1
+    assert L.gdn_selftest_bounded_wait(1_000_000, ctypes.c_void_p(0x10002), NUL) == -1   # misaligned
+    assert L.gdn_selftest_bounded_wait(999, P, NUL) == -1                                 # below 1 us
+    assert L.gdn_selftest_bounded_wait(1_000_000_001, P, NUL) == -1                       # above 1 s
