@@ -31,6 +31,8 @@ def _degenerate(inp, g32, b32, mode):
         g32, b32 = torch.zeros_like(g32), torch.ones_like(b32)
     elif mode == "total_decay":
         g32 = torch.full_like(g32, -30.0)
+    else:
+        assert mode == "none", mode
     return inp, g32, b32
 
 
@@ -76,3 +78,42 @@ def test_decode_degenerate_values(mode):
     assert np.max(np.linalg.norm(yd[nz] - yr[nz], axis=1) / np.linalg.norm(yr[nz], axis=1)) <= TOL_BF16
     assert np.abs(yd[~nz]).max(initial=0.0) == 0.0
     assert rel_l2_states(S, S_ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T", [4, 7])
+def test_multi_token_decode_degenerate_values(mode, T):
+    """Pooled multi-token decode; T = 4 and T = 7 take the block form (blocks of four tokens, the
+    last one padded with one token at T = 7)."""
+    N, H, d, slots = 6, 4, 128, 9
+    gen = torch.Generator().manual_seed(97 + T)
+    q, k, v = (torch.randn(N, T, H, d, generator=gen).to(torch.bfloat16) for _ in range(3))
+    a, b = torch.randn(N, T, H, generator=gen) - 1, torch.randn(N, T, H, generator=gen)
+    A_log = torch.rand(H, generator=gen) * np.log(8)
+    g64, b64 = oracle.gates_from_logits(a.reshape(-1, H), A_log, b=b.reshape(-1, H))
+    g = torch.from_numpy(g64).float().reshape(N, T, H)
+    beta = torch.from_numpy(b64).float().reshape(N, T, H)
+    pool = torch.randn(slots, H, d, d, generator=gen) * 0.3
+    idx = torch.tensor([3, 0, 8, 5, 1, 6], dtype=torch.int32)
+    if mode == "zero_qk":            # whole tokens: t = 1 has a zero query, t = 2 a zero key
+        q[:, 1] = 0
+        k[:, 2] = 0
+    inp = {"q": q, "k": k}
+    _, g, beta = _degenerate(inp, g, beta, mode if mode != "zero_qk" else "none")
+    pool_gpu = pool.cuda()
+    out = gdn.gdn_recurrent_multi_step(q.cuda(), k.cuda(), v.cuda(), g.cuda(), beta.cuda(), pool_gpu,
+                                       state_indices=idx.cuda(), out_dtype=torch.float32)
+    assert gdn.gdn_get_device_error() == 0
+    out, pool_new = out.cpu(), pool_gpu.cpu()
+    assert torch.isfinite(out).all() and torch.isfinite(pool_new).all()
+    flat = lambda x: x.reshape(N * T, H, *x.shape[3:])  # noqa: E731
+    cu = np.arange(0, N * T + 1, T, dtype=np.int32)
+    y_ref, S_ref = oracle.recurrence(flat(q), flat(k), flat(v), flat(g), flat(beta), cu_seqlens=cu,
+                                     initial_state=pool[idx.long()])
+    y = out.reshape(N * T, H, d).double().numpy()
+    slab = lambda x: x.reshape(N, T, H, d).transpose(0, 2, 1, 3).reshape(N * H, -1)  # noqa: E731
+    err = np.linalg.norm(slab(y - y_ref), axis=1) / np.linalg.norm(slab(y_ref), axis=1)
+    assert float(np.max(err)) <= TOL_BF16
+    assert rel_l2_states(pool_new[idx.long()], S_ref) <= TOL_BF16
+    if mode == "zero_qk":
+        assert torch.count_nonzero(out[:, 1]) == 0
