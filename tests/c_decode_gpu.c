@@ -5,7 +5,7 @@
  * oracle's C entry point (test infrastructure, linked from oracle/_build), and the program prints
  * the worst relative L2 error per (sequence, head) of the outputs and of the new states.
  * Exit status 0 when both are within the fp32 tolerance (1e-4), 1 when not, 2 on a CUDA or
- * library error.  Built and run by tests/test_gpu_c_program.py.
+ * library error.  Built and run by tests/test_zzz_gpu_c_program.py.
  */
 #include <cuda_runtime.h>
 #include <math.h>

@@ -1,6 +1,7 @@
 """The C ABI without Python on the data path: tests/c_decode_gpu.c allocates device memory with the
 CUDA runtime, runs gdn_recurrent_step through libgdn.so and checks it against the oracle's C entry
-point.  The CPU test only compiles and links the program; the GPU test runs it."""
+point.  The CPU test only compiles and links the program; the GPU test runs it.  The file name
+makes pytest run it after the kernel parity tests."""
 import glob
 import os
 import shutil
