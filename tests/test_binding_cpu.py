@@ -123,3 +123,21 @@ def test_gate_and_decay_sizes():
         gdn.gdn_decay_from_logits(a, torch.zeros(3))
     with pytest.raises(ValueError, match="beta_out holds"):
         gdn.gdn_decay_from_logits(a, torch.zeros(4), b=b, beta_out=torch.empty(9, 4))
+
+
+def test_missing_or_broken_library_fails_loudly(monkeypatch, tmp_path):
+    """There is no fallback: without a loadable libgdn.so every call raises."""
+    from gated_deltanet_recurrence_gb300 import _binding, build
+    monkeypatch.setattr(build, "is_stale", lambda: False)      # do not rebuild it here
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "absent" / "libgdn.so"))
+    with pytest.raises(RuntimeError, match="not found"):
+        gdn.lib()
+    pos, kw = _decode_args()
+    with pytest.raises(RuntimeError, match="not found"):
+        gdn.gdn_recurrent_step(*pos, **kw)
+    broken = tmp_path / "libgdn.so"
+    broken.write_bytes(b"not a shared library")
+    monkeypatch.setattr(_binding, "LIB_PATH", str(broken))
+    with pytest.raises(OSError):
+        gdn.lib()
