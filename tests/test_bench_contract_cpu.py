@@ -55,3 +55,22 @@ def test_reference_arm_under_torchrun_two_ranks():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], 2)
+
+
+def test_roofline_numerators_follow_the_stated_formulas():
+    """The algorithmic bytes and FLOPs behind the roofline fractions: per (sequence, head) and token,
+    the decode step reads and writes the fp32 state once and moves q, k, v (bf16), g, beta (fp32)
+    and y (bf16); the prefill call moves q, k, v, g, beta, z (fp32) and out once per token-head and
+    the final state once; the chunk products cost 10 C d + 6 d^2 + C^2 / 3 FLOP per token-head."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    # decode workload: 256 sequences x 32 heads x (2 * 128^2 * 4 + 3 * 128 * 2 + 8 + 128 * 2) bytes
+    assert bench.decode_bytes(256, 32, 128) == 256 * 32 * 132_104 == 1_082_195_968
+    # prefill workload: 2 x 4096 tokens, 16 heads, fused gate, final state only
+    assert bench.prefill_bytes(8192, 16, 128, 2) == 8192 * 16 * 1_544 + 2 * 16 * 128 * 128 * 4 == 204_472_320
+    # with an initial state read as well (varlen workload), and without the gate
+    assert bench.prefill_bytes(100, 2, 64, 3, gated=False, init_state=True) == \
+        100 * 2 * (3 * 64 * 2 + 8 + 64 * 2) + 3 * 2 * 64 * 64 * 4 * 2
+    assert abs(bench.prefill_flops_per_token_head(128) - (10 * 64 * 128 + 6 * 128 ** 2 + 64 ** 2 / 3)) < 1e-9
