@@ -62,9 +62,10 @@ def _source_digest(files):
     return h.hexdigest()[:16]
 
 
-def traffic_record(key):
-    """DRAM bytes per launch of a kernel, from the committed ncu capture in profiles/traffic.json;
-    null when missing or when the kernel's sources changed after the capture."""
+def profile_record(key):
+    """The committed ncu figures of a launch unit in profiles/traffic.json (DRAM bytes per launch
+    and, for the chunk kernels, the tensor-pipe utilisation); None when missing or when the
+    kernel's sources changed after the capture (the record holds a digest of them)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[key]
@@ -72,7 +73,20 @@ def traffic_record(key):
         return None
     if _source_digest(rec["sources"]) != rec["digest"]:
         return None
-    return rec["dram_bytes_per_launch"]
+    return rec
+
+
+def traffic_record(key):
+    """DRAM bytes per launch of a kernel from the committed ncu capture, or None (see above)."""
+    rec = profile_record(key)
+    return rec.get("dram_bytes_per_launch") if rec else None
+
+
+def tensor_pipe_record(key):
+    """ncu sm__pipe_tensor_cycles_active (% of peak sustained over active SM cycles) per kernel of
+    a launch unit, from the same digest-keyed record, or None."""
+    rec = profile_record(key)
+    return rec.get("tensor_pipe_pct") if rec else None
 
 
 def load_peaks():
@@ -365,7 +379,7 @@ def bench_prefill(args, dev):
     # either the fused kernel, taken when the units are at most half the SMs, or chunk prep + state
     # pass; 1 on the CUDA-core path)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    fused = os.environ.get("GDN_PREFILL_FUSED", "1") != "0" and n * H <= sms // 2
+    fused = n * H <= sms // 2
     per_step = 1 + ((2 if fused else 3) if ws_bytes > 0 else 1)
     return dict(ms=ms, kernel_ms=kms, clocks=clk, e2e_ms=e2e, h2d=h2d, d2h=d2h, total_T=total_T,
                 H=H, d=d, num_seqs=n, inp=inp_cpu, launches=per_step * args.steps)
@@ -534,11 +548,46 @@ def bench_variants(args, dev):
     return res
 
 
+def serial_pass_share(call, dev):
+    """Share of the serial state pass in one gdn_chunk_fwd call in the two-kernel form (chunk
+    preparation, then the serial pass), from the device times of the launches recorded by
+    torch.profiler (CUPTI) around one call; the fused form overlaps the two, so it is split only
+    here.  None when the profiler records no device kernels."""
+    import gated_deltanet_recurrence_gb300 as gdn
+    from torch.profiler import ProfilerActivity, profile
+    gdn.gdn_set_kernel_forms(prefill_fused=gdn.GDN_FORM_OFF)
+    try:
+        call()
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            call()
+            torch.cuda.synchronize()
+    finally:
+        gdn.gdn_set_kernel_forms()
+    times = {}
+    for e in prof.key_averages():
+        dt = 0.0
+        for attr in ("self_device_time_total", "self_cuda_time_total", "device_time_total", "cuda_time_total"):
+            v_ = getattr(e, attr, None)
+            if v_:
+                dt = float(v_)
+                break
+        if dt > 0 and ("chunk_" in e.key or "gate_prep" in e.key):
+            times[e.key] = times.get(e.key, 0.0) + dt
+    total = sum(times.values())
+    if total <= 0:
+        return {"error": "no device kernels recorded", "events": [e.key[:60] for e in prof.key_averages()][:8]}
+    state = sum(t for n_, t in times.items() if "state" in n_)
+    return {"serial_pass_share": state / total, "two_kernel_ms": total / 1e3,
+            "kernels_ms": {n_.split("(")[0].split("<")[0].split(" ")[-1]: t / 1e3 for n_, t in times.items()},
+            "how": "two-kernel form, one call under torch.profiler (CUPTI device times)"}
+
+
 def bench_workloads(args, dev, names):
-    """The parity-case prefill workloads (varlen: 64 sequences of 128-8192 tokens with initial
-    states; long: one 131,072-token sequence, H = 32, fused gate), timed like the headline step:
-    gdn_decay_from_logits + gdn_chunk_fwd, L2 flushed before every step, CUDA events.  Opt-in
-    (--workloads); prints one JSON line."""
+    """The other prefill workloads (tiny: 1 x 256 tokens, H = 2, d = 64, fp32; varlen: 64 sequences
+    of 128-8192 tokens with initial states; long: one 131,072-token sequence, H = 32, fused gate),
+    timed like the headline step: gdn_decay_from_logits + gdn_chunk_fwd, L2 flushed before every
+    step, CUDA events.  The long workload also reports the serial pass's share of the call."""
     import gated_deltanet_recurrence_gb300 as gdn
     from gated_deltanet_recurrence_gb300 import synthetic
     stream = torch.cuda.current_stream()
@@ -583,11 +632,27 @@ def bench_workloads(args, dev, names):
         eb = q.element_size()
         byts = prefill_bytes(T, H, d, n, qkv_bytes=eb, out_bytes=eb, gated=z is not None,
                              init_state=S0 is not None)
-        fused = os.environ.get("GDN_PREFILL_FUSED", "1") != "0" and n * H <= sms // 2
-        path = ("CUDA-core" if q.dtype != torch.bfloat16 or d != 128 else
-                "tensor-core fused" if fused else "tensor-core two-kernel")
-        res[wl] = {"tokens": T, "num_seqs": n, "units": n * H, "ms": ms, "tokens_per_s": T / (ms / 1e3),
-                   "hbm_gbs": byts / (ms / 1e3) / 1e9, "algorithmic_bytes": byts, "path": path}
+        fused = n * H <= sms // 2
+        tc = q.dtype == torch.bfloat16 and d == 128
+        path = ("CUDA-core" if not tc else "tensor-core fused" if fused else "tensor-core two-kernel")
+        peaks, peak_src = load_peaks()
+        gbs = byts / (ms / 1e3) / 1e9
+        res[wl] = {"metric": "prefill tokens/s", "value": T / (ms / 1e3), "unit": "tokens/s",
+                   "tokens": T, "num_seqs": n, "units": n * H, "H": H, "d": d,
+                   "dtype": "bf16" if q.dtype == torch.bfloat16 else "f32", "ms_per_step": ms,
+                   "path": path, "steps": len(ts),
+                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": byts,
+                                "traffic": traffic_record(f"gdn_chunk_fwd[{wl}]"),
+                                "peak_source": f"{peak_src} hbm_gbs", "timed": "whole step"}}
+        if wl == "long" and tc:
+            def call():
+                gdn.gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=cu, num_seqs=n, initial_state=S0, gate_z=z,
+                                  out=out, final_state=Sf, workspace=ws)
+            try:
+                res[wl]["serial_pass"] = serial_pass_share(call, dev)
+            except Exception as ex:  # the profiler is diagnostic only
+                res[wl]["serial_pass"] = {"error": str(ex)[:200]}
         del q, k, v, a, b, z, S0, out, ws, g, beta, Sf
         torch.cuda.empty_cache()
     return res
@@ -600,8 +665,6 @@ def run_gdn(args):
     if args.workloads:
         res = bench_workloads(args, dev, [w for w in args.workloads.split(",") if w])
         if args.rank == 0:
-            for r in res.values():
-                r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm_gbs"]
             print(json.dumps({"workloads": res, "l2": "flushed (512 MB write) before each step",
                               "step": "gdn_decay_from_logits + gdn_chunk_fwd"}), flush=True)
         return
@@ -618,6 +681,7 @@ def run_gdn(args):
         return
     dc = bench_decode(args, dev)
     variants = bench_variants(args, dev) if not args.no_variants else None
+    workloads = bench_workloads(args, dev, ["tiny", "varlen", "long"]) if not args.no_workloads else None
     world = args.world
     ms = max_over_ranks(pf["ms"], world)
     e2e_ms = max_over_ranks(pf["e2e_ms"], world)
@@ -636,10 +700,10 @@ def run_gdn(args):
     roof = {"bound": "hbm", "achieved": byts / k_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": byts / k_s / 1e9 / peaks["hbm_gbs"], "traffic": tr,
             "kernel": ("gdn_chunk_fwd (chunk_map_kernel + chunk_fused_kernel: chunk preparation and serial "
-                       "pass in one cooperative launch)" if os.environ.get("GDN_PREFILL_FUSED", "1") != "0" else
-                       "gdn_chunk_fwd (chunk_map_kernel + chunk_prep_kernel + chunk_state_kernel)"),
+                       "pass in one cooperative launch)"),
             "algorithmic_bytes": byts, "algorithmic_flops": flops,
             "tensor_tflops": flops / k_s / 1e12,
+            "tensor_pipe_pct_ncu": tensor_pipe_record("gdn_chunk_fwd[prefill]"),
             "tensor_frac": flops / k_s / 1e12 / peaks["bf16_tflops"],
             "peak_source": f"{peak_src} hbm_gbs; tensor_frac of {peak_src} bf16_tflops (burst)",
             "note": "arithmetic intensity 116 FLOP/B is below the bf16 ridge, so HBM is the bound; "
@@ -670,6 +734,7 @@ def run_gdn(args):
         "roofline": roof,
         "decode": decode,
         "variants": variants,
+        "workloads": workloads,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": pf["h2d"],
                 "d2h_bytes_per_step": pf["d2h"], "ms_per_step": e2e_ms},
         "gpu_launches": pf["launches"],
@@ -725,7 +790,9 @@ def main():
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time only one workload (profiling runs); the driver uses the default")
     ap.add_argument("--workloads", default="",
-                    help="comma list of parity-case prefill workloads to time instead (tiny, varlen, long)")
+                    help="comma list of prefill workloads to time alone instead (tiny, varlen, long)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the tiny / varlen / long workload lines of the default run")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: warm-up raised to 3 steps", file=sys.stderr)

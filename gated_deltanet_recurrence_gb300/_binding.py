@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libgdn.so")
 GDN_F32, GDN_BF16 = 0, 1
 GDN_DECAY_PER_HEAD, GDN_DECAY_PER_KEY_CHANNEL = 0, 1
 GDN_CONV_KERNEL = 4
+GDN_FORM_AUTO, GDN_FORM_OFF, GDN_FORM_ON = 0, 1, 2
 STATUS = {0: "GDN_OK", -1: "GDN_ERR_ARG", -2: "GDN_ERR_DTYPE", -3: "GDN_ERR_CU_SEQLENS",
           -4: "GDN_ERR_WORKSPACE", -5: "GDN_ERR_LAUNCH", -6: "GDN_ERR_TIMEOUT",
           -7: "GDN_ERR_UNSUPPORTED", -8: "GDN_ERR_CUDA"}
@@ -45,6 +46,7 @@ SIGNATURES = {
     "gdn_get_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "gdn_status_string": (ctypes.c_char_p, [_i]),
     "gdn_selftest_bounded_wait": (_i, [ctypes.c_ulonglong, _vp, _vp]),
+    "gdn_set_kernel_forms": (_i, [_i, _i]),
 }
 
 
@@ -375,3 +377,10 @@ def gdn_get_device_error(stream=None) -> int:
     st = ctypes.c_int(0)
     _check("gdn_get_device_error", lib().gdn_get_device_error(_stream(stream), ctypes.byref(st)))
     return st.value
+
+
+def gdn_set_kernel_forms(prefill_fused=GDN_FORM_AUTO, decode_blocks=GDN_FORM_AUTO):
+    """Process-wide choice between the library's equivalent kernel forms (GDN_FORM_AUTO / _OFF /
+    _ON for the fused prefill launch and for the four-token block decode); for comparisons and
+    tests.  Call it with no arguments to restore the automatic choice."""
+    _check("gdn_set_kernel_forms", lib().gdn_set_kernel_forms(int(prefill_fused), int(decode_blocks)))

@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points of libgdn.so: argument checks, dispatch, error word.
 // Declarations and the meaning of every argument are in include/gdn.h.
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -21,7 +22,10 @@ int* device_error_ptr() {
     std::lock_guard<std::mutex> lk(g_err_mu);
     if (!g_err_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_gdn_device_error) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_gdn_device_error) != cudaSuccess) {
+            cudaGetLastError();  // do not leave the failure for a later launch check to report
+            return nullptr;
+        }
         g_err_ptr[dev] = static_cast<int*>(p);
     }
     return g_err_ptr[dev];
@@ -48,7 +52,17 @@ int conv_args(const float* w, const float* st_in, float* st_out, int H, int H_k,
 
 int launch_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH; }
 
+std::atomic<int> g_prefill_fused_form{GDN_FORM_AUTO};
+std::atomic<int> g_decode_blocks_form{GDN_FORM_AUTO};
+
+bool valid_form(int f) { return f == GDN_FORM_AUTO || f == GDN_FORM_OFF || f == GDN_FORM_ON; }
+
 }  // namespace
+
+namespace gdn {
+int prefill_fused_form() { return g_prefill_fused_form.load(std::memory_order_relaxed); }
+int decode_blocks_form() { return g_decode_blocks_form.load(std::memory_order_relaxed); }
+}  // namespace gdn
 
 extern "C" {
 
@@ -65,6 +79,13 @@ const char* gdn_status_string(int status) {
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA runtime call failed";
         default: return "unknown gdn_status";
     }
+}
+
+int gdn_set_kernel_forms(int prefill_fused, int decode_blocks) {
+    if (!valid_form(prefill_fused) || !valid_form(decode_blocks)) return GDN_ERR_ARG;
+    g_prefill_fused_form.store(prefill_fused, std::memory_order_relaxed);
+    g_decode_blocks_form.store(decode_blocks, std::memory_order_relaxed);
+    return GDN_OK;
 }
 
 int gdn_get_device_error(void* stream, int* device_status) {

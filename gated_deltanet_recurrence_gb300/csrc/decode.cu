@@ -659,11 +659,12 @@ cudaError_t launch_variant(const DecodeArgs& a, cudaStream_t s, bool blocks) {
 // them; otherwise token by token.  Measured (N = 256, H = 32, d = 128, bf16, gate; ms):
 // T = 2: 0.222 vs 0.265 (blocks), 3: 0.292 vs 0.270, 4: 0.347 vs 0.272, 5: 0.404 vs 0.448,
 // 8: 0.565 vs 0.467: a block costs about 0.19 ms here, a token about 0.06 ms.
-// GDN_DECODE_BLOCKS=0/1 overrides the choice.
+// gdn_set_kernel_forms can force either form (for comparisons and tests).
 template <int D, typename TIn>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
     bool blocks = a.T >= 3 && (a.T % kBlk == 0 || a.T % kBlk == kBlk - 1 || a.T >= 10);
-    if (const char* env = getenv("GDN_DECODE_BLOCKS")) blocks = env[0] == '1';
+    const int form = decode_blocks_form();
+    if (form != GDN_FORM_AUTO) blocks = form == GDN_FORM_ON && a.T >= 2;
     if (a.conv.w) {
         if (a.z) return launch_variant<D, TIn, true, true>(a, s, blocks);
         return launch_variant<D, TIn, false, true>(a, s, blocks);

@@ -81,6 +81,10 @@ __device__ __forceinline__ void record_error(int* err, int status) {
     if (err) atomicCAS(err, 0, status);
 }
 
+// Kernel-form overrides set through gdn_set_kernel_forms (process-wide, GDN_FORM_AUTO by default).
+int prefill_fused_form();
+int decode_blocks_form();
+
 // ---- launchers (one translation unit each; called from abi.cu after argument checks) --------
 
 // The fused short convolution ("因果卷积"): weight [dim, 4]; states [rows, dim, 3], oldest first.

@@ -6,8 +6,9 @@
 // not grow its footprint after start-up, or a host program that only holds raw pointers to
 // buffers somebody else owns.  For them this entry point keeps the prefill's scratch (the chunk
 // numbering and the per-chunk intermediates of the tensor-core path) in a fixed array that lives
-// in the library's own device memory image: every GPU that loads libgdn.so holds the array until
-// the process exits, and no call here allocates or frees anything.
+// in the library's own device memory image: every GPU that loads libgdn.so (or, under lazy module
+// loading, that first runs this entry point) holds the array until the process exits, and no call
+// here allocates or frees anything.
 //
 // Rules of use:
 //   * The array holds GDN_NOALLOC_SCRATCH_BYTES.  A call whose scratch need (what
@@ -19,6 +20,8 @@
 //     between them) race on the array.  Order such calls on one stream.
 //   * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
 //     that device current).  Make that first call before any stream capture that includes it.
+//     With lazy module loading the array may only be placed on the device at that first lookup;
+//     if the device has no room for it, the call returns GDN_ERR_CUDA and launches nothing.
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -39,7 +42,12 @@ void* scratch_ptr() {
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (!g_scratch_ptr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            // clear the runtime's last-error slot, so the failure is not reported again by the
+            // launch check of a later, unrelated call
+            cudaGetLastError();
+            return nullptr;
+        }
         g_scratch_ptr[dev] = p;
     }
     return g_scratch_ptr[dev];

@@ -38,7 +38,6 @@
 // Every mbarrier wait is bounded; on a timeout the kernel records GDN_ERR_TIMEOUT and its roles
 // stop issuing work, wait (bounded) for what they issued, free TMEM and return.
 #include <cuda.h>
-#include <stdlib.h>
 #include <cudaTypedefs.h>
 
 #include <cuda_fp16.h>
@@ -1386,24 +1385,33 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 ok = mbar_wait(&bars[ZFULL0 + b], (c >> 1) & 1, kPolls);
                 if (!ok) fail();
                 const float rA_inv = rsqrtf(ssA / kD + a.eps), rB_inv = rsqrtf(ssB / kD + a.eps);
+                // bf16 output: SiLU with the packed half-precision tanh (error near 1e-3, below the
+                // output's 2^-9 rounding); fp32 output: SiLU at fp32 accuracy.  The choice is taken
+                // once, outside the loop, so that only one of the two is evaluated per element.
+                auto gate = [&](auto silu2) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int col = 8 * j + cp, cb = col >> 5, ch = (col & 31) >> 2, sub = (col & 3) * 4;
-                    const float2 zA = *reinterpret_cast<const float2*>(zt + cb * 8192 + rA * 128 + ((ch ^ (rA & 7)) << 4) + sub);
-                    const float2 zB = *reinterpret_cast<const float2*>(zt + cb * 8192 + (rA + 8) * 128 +
-                                                                       ((ch ^ ((rA + 8) & 7)) << 4) + sub);
-                    float2 wA = make_float2(rA_inv, rA_inv), wB = make_float2(rB_inv, rB_inv);
-                    if (a.w) {
-                        const float2 wv = __ldg(reinterpret_cast<const float2*>(a.w + col));
-                        wA = make_float2(wv.x * rA_inv, wv.y * rA_inv);
-                        wB = make_float2(wv.x * rB_inv, wv.y * rB_inv);
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 8 * j + cp, cb = col >> 5, ch = (col & 31) >> 2, sub = (col & 3) * 4;
+                        const float2 zA = *reinterpret_cast<const float2*>(zt + cb * 8192 + rA * 128 + ((ch ^ (rA & 7)) << 4) + sub);
+                        const float2 zB = *reinterpret_cast<const float2*>(zt + cb * 8192 + (rA + 8) * 128 +
+                                                                           ((ch ^ ((rA + 8) & 7)) << 4) + sub);
+                        float2 wA = make_float2(rA_inv, rA_inv), wB = make_float2(rB_inv, rB_inv);
+                        if (a.w) {
+                            const float2 wv = __ldg(reinterpret_cast<const float2*>(a.w + col));
+                            wA = make_float2(wv.x * rA_inv, wv.y * rA_inv);
+                            wB = make_float2(wv.x * rB_inv, wv.y * rB_inv);
+                        }
+                        const float2 sA = silu2(zA), sB = silu2(zB);
+                        o[4 * j] *= wA.x * sA.x;
+                        o[4 * j + 1] *= wA.y * sA.y;
+                        o[4 * j + 2] *= wB.x * sB.x;
+                        o[4 * j + 3] *= wB.y * sB.y;
                     }
-                    const float2 sA = fast_silu2(zA.x, zA.y), sB = fast_silu2(zB.x, zB.y);
-                    o[4 * j] *= wA.x * sA.x;
-                    o[4 * j + 1] *= wA.y * sA.y;
-                    o[4 * j + 2] *= wB.x * sB.x;
-                    o[4 * j + 3] *= wB.y * sB.y;
-                }
+                };
+                if (bf16_out)
+                    gate([](float2 x) { return fast_silu2(x.x, x.y); });
+                else
+                    gate([](float2 x) { return make_float2(x.x * sigmoidf_(x.x), x.y * sigmoidf_(x.y)); });
             }
             if (bf16_out && L == kC) {
                 // a full chunk: stage the bf16 rows as two 128-byte-swizzled [64 x 64] boxes in the
@@ -1680,15 +1688,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     }
 
     // the fused cooperative kernel serves calls with few (sequence, head) units: at most half the SMs
-    // run serial passes, the rest prepare chunks; GDN_PREFILL_FUSED=0 in the environment turns it off
+    // run serial passes, the rest prepare chunks; gdn_set_kernel_forms can turn it off
     int units = p.num_seqs * p.H, sms = 0, coop = 0, dev = 0, resident = 0;
     auto fused_fn = p.g_per_channel ? chunk_fused_kernel<true> : chunk_fused_kernel<false>;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
-    const char* env = getenv("GDN_PREFILL_FUSED");
-    bool fused = coop && units <= sms / 2 && !(env && env[0] == '0');
+    const int form = prefill_fused_form();
+    bool fused = coop && form != GDN_FORM_OFF && units <= (form == GDN_FORM_ON ? sms - 1 : sms / 2);
     if (fused) {
         e = cudaFuncSetAttribute(fused_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fz::kSmem);
         if (e != cudaSuccess) return e;

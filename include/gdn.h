@@ -105,9 +105,9 @@ typedef enum {
  *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte
  *                 aligned; may be NULL when that size is 0.
  * With bf16 q/k/v and d = 128, calls with at most (number of SMs) / 2 (sequence, head) pairs run the
- * chunk preparation and the serial pass as one cooperative launch that occupies every SM; setting
- * the environment variable GDN_PREFILL_FUSED=0 selects the two-kernel form (same results, bit for
- * bit).
+ * chunk preparation and the serial pass as one cooperative launch that occupies every SM; otherwise
+ * a chunk-preparation kernel and a serial-pass kernel run in turn.  gdn_set_kernel_forms can force
+ * either form; both give the same results, bit for bit.
  */
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int num_seqs, int total_T, int H, int H_k,
@@ -210,6 +210,9 @@ int gdn_decay_from_logits(const float* a, const float* A_log, const float* dt_bi
  * Arguments, layouts and results are those of gdn_chunk_fwd, without the workspace.  The scratch
  * lives in a fixed array of GDN_NOALLOC_SCRATCH_BYTES inside the library's device image, which
  * every GPU that loads libgdn.so holds until the process exits; nothing is allocated or freed.
+ * Under lazy module loading (CUDA_MODULE_LOADING=LAZY, the CUDA 12+ default) the array may be
+ * placed on a device only at this entry point's first call there; a device without room for it
+ * then makes that call return GDN_ERR_CUDA, with nothing launched.
  *   - Sizes whose workspace need (gdn_chunk_fwd_workspace_size) exceeds GDN_NOALLOC_SCRATCH_BYTES
  *     are rejected with GDN_ERR_WORKSPACE before anything is launched.
  *   - All calls share the one array per device and it keeps the last call's contents (the call
@@ -234,6 +237,22 @@ int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
  * since the last call.  Returns GDN_OK, or GDN_ERR_CUDA if the synchronisation itself failed.
  */
 int gdn_get_device_error(void* stream, int* device_status);
+
+/*
+ * gdn_set_kernel_forms -- process-wide choice between equivalent kernel forms, for comparisons
+ * and tests (the pages have no counterpart).  Every later call on any thread uses it; the default
+ * is GDN_FORM_AUTO for both.
+ *   prefill_fused  GDN_FORM_AUTO: gdn_chunk_fwd (tensor-core path) fuses chunk preparation and the
+ *                  serial pass into one cooperative launch when the (sequence, head) pairs number
+ *                  at most half the SMs; GDN_FORM_OFF: always the two-kernel form; GDN_FORM_ON:
+ *                  fused whenever the pairs number fewer than the SMs.  Results are bit-identical.
+ *   decode_blocks  GDN_FORM_AUTO: gdn_recurrent_multi_step takes the four-token block form when the
+ *                  tokens fill the blocks to within one token or T >= 10; GDN_FORM_OFF: token by
+ *                  token; GDN_FORM_ON: blocks for every T >= 2.  Results agree to fp32 rounding.
+ * Returns GDN_OK, or GDN_ERR_ARG for a value outside gdn_form (nothing is changed then).
+ */
+typedef enum { GDN_FORM_AUTO = 0, GDN_FORM_OFF = 1, GDN_FORM_ON = 2 } gdn_form;
+int gdn_set_kernel_forms(int prefill_fused, int decode_blocks);
 
 /* Human-readable name of a gdn_status value (static string). */
 const char* gdn_status_string(int status);

@@ -87,7 +87,7 @@ def test_multi_step_bad_index_is_reported():
 
 
 @pytest.mark.parametrize("T", [2, 3, 4, 6, 9])
-def test_block_and_token_forms_agree(T, monkeypatch):
+def test_block_and_token_forms_agree(T, kernel_forms):
     """The block form (the chunked update over blocks of four tokens, padded at the end) and the
     token-by-token form compute the same recurrence: outputs and states agree to fp32 rounding,
     gate included, with skipped sequences."""
@@ -96,7 +96,7 @@ def test_block_and_token_forms_agree(T, monkeypatch):
     dev = "cuda"
     res = {}
     for mode in ("1", "0"):
-        monkeypatch.setenv("GDN_DECODE_BLOCKS", mode)
+        gdn.gdn_set_kernel_forms(decode_blocks=gdn.GDN_FORM_ON if mode == "1" else gdn.GDN_FORM_OFF)
         p = pool.to(dev)
         y = gdn.gdn_recurrent_multi_step(q.to(dev), k.to(dev), v.to(dev), g.to(dev), beta.to(dev), p,
                                          state_indices=idx.to(dev), gate_z=z.to(dev), out_dtype=torch.float32)
