@@ -548,39 +548,27 @@ def bench_variants(args, dev):
     return res
 
 
-def serial_pass_share(call, dev):
-    """Share of the serial state pass in one gdn_chunk_fwd call in the two-kernel form (chunk
-    preparation, then the serial pass), from the device times of the launches recorded by
-    torch.profiler (CUPTI) around one call; the fused form overlaps the two, so it is split only
-    here.  None when the profiler records no device kernels."""
+def two_kernel_time(call, flush, steps=3):
+    """Mean CUDA-event time of one gdn_chunk_fwd call in the two-kernel form (chunk preparation,
+    then the serial pass), L2 flushed before each call."""
     import gated_deltanet_recurrence_gb300 as gdn
-    from torch.profiler import ProfilerActivity, profile
+    stream = torch.cuda.current_stream()
     gdn.gdn_set_kernel_forms(prefill_fused=gdn.GDN_FORM_OFF)
     try:
         call()
         torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
             call()
-            torch.cuda.synchronize()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
     finally:
         gdn.gdn_set_kernel_forms()
-    times = {}
-    for e in prof.key_averages():
-        dt = 0.0
-        for attr in ("self_device_time_total", "self_cuda_time_total", "device_time_total", "cuda_time_total"):
-            v_ = getattr(e, attr, None)
-            if v_:
-                dt = float(v_)
-                break
-        if dt > 0 and ("chunk_" in e.key or "gate_prep" in e.key):
-            times[e.key] = times.get(e.key, 0.0) + dt
-    total = sum(times.values())
-    if total <= 0:
-        return {"error": "no device kernels recorded", "events": [e.key[:60] for e in prof.key_averages()][:8]}
-    state = sum(t for n_, t in times.items() if "state" in n_)
-    return {"serial_pass_share": state / total, "two_kernel_ms": total / 1e3,
-            "kernels_ms": {n_.split("(")[0].split("<")[0].split(" ")[-1]: t / 1e3 for n_, t in times.items()},
-            "how": "two-kernel form, one call under torch.profiler (CUPTI device times)"}
+    return statistics.mean(x.elapsed_time(y) for x, y in ts)
 
 
 def bench_workloads(args, dev, names):
@@ -646,13 +634,16 @@ def bench_workloads(args, dev, names):
                                 "traffic": traffic_record(f"gdn_chunk_fwd[{wl}]"),
                                 "peak_source": f"{peak_src} hbm_gbs", "timed": "whole step"}}
         if wl == "long" and tc:
+            # the serial state pass's share: the two-kernel form (preparation, then the serial pass)
+            # timed live, split by the committed ncu launch list of the same call (digest-keyed)
             def call():
                 gdn.gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens=cu, num_seqs=n, initial_state=S0, gate_z=z,
                                   out=out, final_state=Sf, workspace=ws)
-            try:
-                res[wl]["serial_pass"] = serial_pass_share(call, dev)
-            except Exception as ex:  # the profiler is diagnostic only
-                res[wl]["serial_pass"] = {"error": str(ex)[:200]}
+            rec = profile_record("gdn_chunk_fwd[long]") or {}
+            res[wl]["serial_pass"] = {"two_kernel_call_ms": two_kernel_time(call, flush),
+                                      "share_of_two_kernel_call": rec.get("serial_pass_share"),
+                                      "kernel_us_ncu": rec.get("kernel_us"),
+                                      "source": "ncu launch list in profiles/traffic.json (null once the sources change)"}
         del q, k, v, a, b, z, S0, out, ws, g, beta, Sf
         torch.cuda.empty_cache()
     return res
@@ -661,6 +652,9 @@ def bench_workloads(args, dev, names):
 def run_gdn(args):
     dev = torch.device("cuda", args.local)
     torch.cuda.set_device(dev)
+    if args.prefill_form != "auto":
+        import gated_deltanet_recurrence_gb300 as gdn
+        gdn.gdn_set_kernel_forms(prefill_fused=gdn.GDN_FORM_ON if args.prefill_form == "fused" else gdn.GDN_FORM_OFF)
     peaks, peak_src = load_peaks()
     if args.workloads:
         res = bench_workloads(args, dev, [w for w in args.workloads.split(",") if w])
@@ -793,6 +787,8 @@ def main():
                     help="comma list of prefill workloads to time alone instead (tiny, varlen, long)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the tiny / varlen / long workload lines of the default run")
+    ap.add_argument("--prefill-form", choices=["auto", "fused", "two-kernel"], default="auto",
+                    help="force one prefill kernel form (profiling runs); the driver uses the default")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: warm-up raised to 3 steps", file=sys.stderr)
