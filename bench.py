@@ -452,8 +452,9 @@ def bench_decode(args, dev):
 
 def bench_variants(args, dev):
     """The prefill options on the prefill workload's sizes (B=2 x T=4096, H=16, d=128, bf16, fused
-    gate): 4 query/key heads shared by 16 value heads, a decay per key channel, and the fused short
-    convolution; plus one decode step with the convolution and its history updated in place.  Each
+    gate): 4 query/key heads shared by 16 value heads, a decay per key channel, the fused short
+    convolution, and head size 64; plus one decode step with the convolution and its history updated
+    in place.  Each
     timed region is one gdn_chunk_fwd (or gdn_recurrent_step) call, L2 flushed before every call."""
     import gated_deltanet_recurrence_gb300 as gdn
     from gated_deltanet_recurrence_gb300 import synthetic
@@ -462,7 +463,7 @@ def bench_variants(args, dev):
     peaks, _ = load_peaks()
     res = {}
     steps = max(3, min(args.steps, 10))
-    for name in ("prefill_gva", "prefill_kda", "prefill_conv"):
+    for name in ("prefill_gva", "prefill_kda", "prefill_conv", "prefill_d64"):
         inp = synthetic.prefill_inputs(name)
         cfg = inp["cfg"]
         total_T, H, d, n = inp["total_T"], cfg["H"], cfg["d"], inp["num_seqs"]

@@ -103,11 +103,12 @@ int gdn_get_device_error(void* stream, int* device_status) {
     return GDN_OK;
 }
 
-// The tensor-core path (bf16, d = 128) keeps per-chunk intermediates (W, U^T, the decayed Q K^T,
-// Q~, K~ and decay factors, about 42 KB per chunk and head) in the caller's workspace; the fp32
-// CUDA-core path needs none.
+// The tensor-core path (bf16 q/k/v; d = 128, or d = 64 run as 128-wide tiles whose extra columns
+// are zeros) keeps per-chunk intermediates (W, U^T, the decayed Q K^T, Q~, K~ and decay factors,
+// about 75 KB per chunk and head) in the caller's workspace; the fp32 CUDA-core path needs none.
 static bool uses_tc_path(int num_seqs, int total_T, int H, int d_k, int d_v, int qkv_dtype) {
-    return qkv_dtype == GDN_BF16 && d_k == 128 && d_v == 128 && total_T > 0 && num_seqs > 0 && H > 0;
+    return qkv_dtype == GDN_BF16 && d_k == d_v && (d_k == 128 || d_k == 64) && total_T > 0 &&
+           num_seqs > 0 && H > 0;
 }
 
 size_t gdn_chunk_fwd_workspace_size(int num_seqs, int total_T, int H, int d_k, int d_v,

@@ -89,6 +89,8 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
 struct TcArgs {
     const int32_t* cu;   // may be null: fixed length
     int num_seqs, total_T, H, Hk;
+    int d;               // head size of the caller's tensors (64 or 128); tiles are 128 wide, the
+                         // columns past d are zeros (TMA fills them) and stay zero throughout
     const __nv_bfloat16* q;  // raw q, k [total_T, Hk, 128] and v [total_T, H, 128]: convolution history
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
@@ -394,10 +396,11 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
     const int x0 = half * 64 + c8 * 8;
     // ten 0: Q, 1: K, 2: V (V occupies Q's rows once Q is no longer needed)
     uint8_t* tile = sm + oKQ + half * 16384 + (ten == 1 ? 0 : 8192);
-    const __nv_bfloat16* src = ten == 0 ? a.q + hk * kD + x0 : (ten == 1 ? a.k + hk * kD + x0 : a.v + (long)h * kD + x0);
-    const long stride = ten == 2 ? (long)a.H * kD : (long)a.Hk * kD;
-    const int chan = ten == 0 ? hk * kD + x0 : (ten == 1 ? a.Hk * kD + hk * kD + x0 : 2 * a.Hk * kD + h * kD + x0);
-    const bool live = r0 < L;
+    const int d = a.d;
+    const __nv_bfloat16* src = ten == 0 ? a.q + hk * d + x0 : (ten == 1 ? a.k + hk * d + x0 : a.v + (long)h * d + x0);
+    const long stride = ten == 2 ? (long)a.H * d : (long)a.Hk * d;
+    const int chan = ten == 0 ? hk * d + x0 : (ten == 1 ? a.Hk * d + hk * d + x0 : 2 * a.Hk * d + h * d + x0);
+    const bool live = r0 < L && x0 < d;  // columns past the head size hold zeros and stay so
     float hist[3][8];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
@@ -521,11 +524,12 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
     for (int hf = 0; hf < 2; ++hf) {
         // (a) per-channel inclusive sums, in log2 units; e^(G_last) for the state pass
         if (tid < 64) {  // all 64 loads of a channel in flight at once, then the running sum
-            const float* gp = a.g + (t0 * a.H + h) * (long)kD + hf * 64 + tid;
-            const long gs = (long)a.H * kD;
+            const bool chan_in = hf * 64 + tid < a.d;  // padded channels: no decay
+            const float* gp = a.g + (t0 * a.H + h) * (long)a.d + hf * 64 + tid;
+            const long gs = (long)a.H * a.d;
             float gv[kC];
 #pragma unroll
-            for (int i = 0; i < kC; ++i) gv[i] = i < L ? __ldg(gp + i * gs) : 0.f;
+            for (int i = 0; i < kC; ++i) gv[i] = (i < L && chan_in) ? __ldg(gp + i * gs) : 0.f;
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < kC; ++i) {
@@ -1150,8 +1154,9 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
         uint8_t* Sb = sm + oS;
         // initial state: S_bf16 <- S0, TMEM S <- gamma_0 S0 (32 columns at a time)
         {
-            const float* src = a.initial_state ? a.initial_state + ((long)unit * kD + r) * kD : nullptr;
-            float* dst = (nck == 0 && a.final_state) ? a.final_state + ((long)unit * kD + r) * kD : nullptr;
+            const bool row_in = r < a.d;  // rows (and columns) past the head size are zero
+            const float* src = (a.initial_state && row_in) ? a.initial_state + ((long)unit * a.d + r) * a.d : nullptr;
+            float* dst = (nck == 0 && a.final_state && row_in) ? a.final_state + ((long)unit * a.d + r) * a.d : nullptr;
             bool ready0 = true;
             if (nck > 0 && a.ready) ready0 = wait_ready(a.ready + (long)first * a.H + h);
             if (!ready0) fail();
@@ -1161,11 +1166,12 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 float f[32];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    float4 t = src ? *reinterpret_cast<const float4*>(src + blk * 32 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 t = (src && blk * 32 < a.d) ? *reinterpret_cast<const float4*>(src + blk * 32 + j)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                     f[j] = t.x; f[j + 1] = t.y; f[j + 2] = t.z; f[j + 3] = t.w;
                 }
                 if (nck == 0) {
-                    if (dst)
+                    if (dst && blk * 32 < a.d)
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
                             *reinterpret_cast<float4*>(dst + blk * 32 + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
@@ -1270,10 +1276,11 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             for (int blk = 0; blk < 4; ++blk) tmem_ld32(tS + lrow + blk * 32, v[blk]);
             tmem_wait_ld();
             if (last) {
-                if (ok && a.final_state) {
+                if (ok && a.final_state && r < a.d) {
 #pragma unroll
                     for (int blk = 0; blk < 4; ++blk) {
-                        float* dst = a.final_state + ((long)unit * kD + r) * kD + blk * 32;
+                        if (blk * 32 >= a.d) break;
+                        float* dst = a.final_state + ((long)unit * a.d + r) * a.d + blk * 32;
 #pragma unroll
                         for (int j = 0; j < 32; j += 4)
                             *reinterpret_cast<uint4*>(dst + j) = make_uint4(v[blk][j], v[blk][j + 1], v[blk][j + 2], v[blk][j + 3]);
@@ -1322,7 +1329,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
         const int cp = 2 * (lane & 3);
         const uint32_t lrow = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t gbar = 4u + (uint32_t)og;
-        const long tok_stride = (long)a.H * kD;
+        const long tok_stride = (long)a.H * a.d;
         const bool leader = (q4 == 0 && lane == 0);
         const bool bf16_out = a.out_dtype == GDN_BF16;
         // z of chunk c goes to buffer c & 1 (this group's); it is requested two chunks ahead
@@ -1384,7 +1391,8 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             if (a.z) {
                 ok = mbar_wait(&bars[ZFULL0 + b], (c >> 1) & 1, kPolls);
                 if (!ok) fail();
-                const float rA_inv = rsqrtf(ssA / kD + a.eps), rB_inv = rsqrtf(ssB / kD + a.eps);
+                // the mean over the head's d_v outputs (the padded columns are zeros)
+                const float rA_inv = rsqrtf(ssA / a.d + a.eps), rB_inv = rsqrtf(ssB / a.d + a.eps);
                 // bf16 output: SiLU with the packed half-precision tanh (error near 1e-3, below the
                 // output's 2^-9 rounding); fp32 output: SiLU at fp32 accuracy.  The choice is taken
                 // once, outside the loop, so that only one of the two is evaluated per element.
@@ -1396,7 +1404,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                         const float2 zB = *reinterpret_cast<const float2*>(zt + cb * 8192 + (rA + 8) * 128 +
                                                                            ((ch ^ ((rA + 8) & 7)) << 4) + sub);
                         float2 wA = make_float2(rA_inv, rA_inv), wB = make_float2(rB_inv, rB_inv);
-                        if (a.w) {
+                        if (a.w && col < a.d) {
                             const float2 wv = __ldg(reinterpret_cast<const float2*>(a.w + col));
                             wA = make_float2(wv.x * rA_inv, wv.y * rA_inv);
                             wB = make_float2(wv.x * rB_inv, wv.y * rB_inv);
@@ -1431,7 +1439,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 bar_sync(gbar, 128);
                 if (leader && ok) {
                     tma_store_3d(mOut, zt, 0, h, (int)t0);
-                    tma_store_3d(mOut, zt + 8192, 64, h, (int)t0);
+                    if (a.d > 64) tma_store_3d(mOut, zt + 8192, 64, h, (int)t0);
                     bulk_commit();
                 }
             } else if (ok) {
@@ -1441,9 +1449,10 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 for (int hr = 0; hr < 2; ++hr) {
                     const int r = rA + 8 * hr;
                     if (r < L) {
-                        const long base = (t0 + r) * tok_stride + (long)h * kD + cp;
+                        const long base = (t0 + r) * tok_stride + (long)h * a.d + cp;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
+                            if (8 * j >= a.d) break;
                             const float x0 = o[4 * j + 2 * hr], x1 = o[4 * j + 2 * hr + 1];
                             if (bf16_out)
                                 *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + base + 8 * j) =
@@ -1604,10 +1613,11 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-bool map_tokens(CUtensorMap* m, const void* base, int total_T, int H) {
-    // [total_T, H, 128] bf16 -> dims (128, H, total_T), box (64, 1, 64), 128-byte swizzle
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_T};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+bool map_tokens(CUtensorMap* m, const void* base, int total_T, int H, int d) {
+    // [total_T, H, d] bf16 -> dims (d, H, total_T), box (64, 1, 64), 128-byte swizzle; with d = 64 the
+    // boxes at column 64 lie past the tensor and load as zeros
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     cuuint32_t box[3] = {64, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return get_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -1615,10 +1625,10 @@ bool map_tokens(CUtensorMap* m, const void* base, int total_T, int H) {
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool map_z(CUtensorMap* m, const float* base, int total_T, int H) {
-    // gate input z [total_T, H, 128] fp32 -> dims (128, H, total_T), box (32, 1, 64), 128-byte swizzle
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)total_T};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)H * kD * 4};
+bool map_z(CUtensorMap* m, const float* base, int total_T, int H, int d) {
+    // gate input z [total_T, H, d] fp32 -> dims (d, H, total_T), box (32, 1, 64), 128-byte swizzle
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
     cuuint32_t box[3] = {32, 1, 64};
     cuuint32_t es[3] = {1, 1, 1};
     return get_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, es,
@@ -1643,14 +1653,14 @@ size_t prefill_tc_workspace_bytes(int num_seqs, int total_T, int H) {
 }
 
 bool prefill_tc_supported(const PrefillArgs& a) {
-    return a.d == 128 && a.qkv_dtype == GDN_BF16 && get_encoder() != nullptr && a.total_T > 0;
+    return (a.d == 128 || a.d == 64) && a.qkv_dtype == GDN_BF16 && get_encoder() != nullptr && a.total_T > 0;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     const WsLayout L = ws_layout(p.num_seqs, p.total_T, p.H);
     uint8_t* ws = static_cast<uint8_t*>(p.workspace);
     TcArgs a{};
-    a.cu = p.cu_seqlens; a.num_seqs = p.num_seqs; a.total_T = p.total_T; a.H = p.H; a.Hk = p.Hk;
+    a.cu = p.cu_seqlens; a.num_seqs = p.num_seqs; a.total_T = p.total_T; a.H = p.H; a.Hk = p.Hk; a.d = p.d;
     a.q = static_cast<const __nv_bfloat16*>(p.q);
     a.k = static_cast<const __nv_bfloat16*>(p.k);
     a.v = static_cast<const __nv_bfloat16*>(p.v);
@@ -1671,18 +1681,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.z = p.z; a.w = p.w; a.eps = p.eps; a.out = p.out; a.out_dtype = p.out_dtype; a.err = p.err;
 
     CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ, mOut;
-    if (!map_tokens(&mQ, p.q, p.total_T, p.Hk) || !map_tokens(&mK, p.k, p.total_T, p.Hk) ||
-        !map_tokens(&mV, p.v, p.total_T, p.H) || !map_rows(&mW, a.W, L.nch * kC, kD, 64) ||
+    if (!map_tokens(&mQ, p.q, p.total_T, p.Hk, p.d) || !map_tokens(&mK, p.k, p.total_T, p.Hk, p.d) ||
+        !map_tokens(&mV, p.v, p.total_T, p.H, p.d) || !map_rows(&mW, a.W, L.nch * kC, kD, 64) ||
         !map_rows(&mAqk, a.Aqk, L.nch * kC, kC, 64) || !map_rows(&mQt, a.Qt, L.nch * kC, kD, 64) ||
         !map_rows(&mKt, a.Kt, L.nch * kC, kD, 64))
         return cudaErrorInvalidValue;
     if (p.z) {
-        if (!map_z(&mZ, p.z, p.total_T, p.H)) return cudaErrorInvalidValue;
+        if (!map_z(&mZ, p.z, p.total_T, p.H, p.d)) return cudaErrorInvalidValue;
     } else {
         mZ = mQ;  // never dereferenced without a gate
     }
     if (p.out_dtype == GDN_BF16) {
-        if (!map_tokens(&mOut, p.out, p.total_T, p.H)) return cudaErrorInvalidValue;
+        if (!map_tokens(&mOut, p.out, p.total_T, p.H, p.d)) return cudaErrorInvalidValue;
     } else {
         mOut = mQ;  // never dereferenced with an fp32 output
     }

@@ -17,6 +17,7 @@ Workloads (named by what they are):
   prefill_conv  the prefill workload with the short convolution fused (raw q, k, v drawn; taps
                 per channel ~ U(-1/2, 1/2), the default uniform bound 1/sqrt(fan_in) of a
                 depthwise kernel of 4 taps; zero history, i.e. sequences that start here).
+  prefill_d64   the prefill workload with head size d_k = d_v = 64.
 Distributions common to all: q, k, v ~ N(0, 1); a ~ N(-1, 1) unless stated; A = exp(A_log) with
 A_log ~ U[0, ln 8] per head; b ~ N(0, 1) (beta = sigmoid(b)); z ~ N(0, 1).
 Options (any workload): Hk (query/key heads, default H), per_channel (a drawn [T, H, d] so that
@@ -47,6 +48,8 @@ WORKLOADS = {
                         a_mean=-1.0, gate=True, init_state=False, per_channel=True),
     "prefill_conv": dict(kind="prefill", seed=7, num_seqs=2, T=4096, H=16, d=128, dtype=torch.bfloat16,
                          a_mean=-1.0, gate=True, init_state=False, conv=True),
+    "prefill_d64": dict(kind="prefill", seed=8, num_seqs=2, T=4096, H=16, d=64, dtype=torch.bfloat16,
+                        a_mean=-1.0, gate=True, init_state=False),
 }
 
 

@@ -104,7 +104,8 @@ typedef enum {
  *   out           [total_T, H, d_v], element type out_dtype.
  *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size(...) bytes, 256-byte
  *                 aligned; may be NULL when that size is 0.
- * With bf16 q/k/v and d = 128, calls with at most (number of SMs) / 2 (sequence, head) pairs run the
+ * With bf16 q/k/v (d = 64 or 128; d = 64 runs the same kernels on tiles whose columns past 64 are
+ * zeros), calls with at most (number of SMs) / 2 (sequence, head) pairs run the
  * chunk preparation and the serial pass as one cooperative launch that occupies every SM; otherwise
  * a chunk-preparation kernel and a serial-pass kernel run in turn.  gdn_set_kernel_forms can force
  * either form; both give the same results, bit for bit.

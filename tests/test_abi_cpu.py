@@ -82,9 +82,11 @@ def test_workspace_size_is_consistent():
         assert ws > 0                               # bf16, d = 128: tensor-core path
         assert _chunk(num_seqs=n, total_T=T, H=H, dt=1, odt=1, ws=NUL, wsb=0) == -4
         assert _chunk(num_seqs=n, total_T=T, H=H, dt=1, odt=1, ws=P, wsb=ws - 1) == -4
-        # fp32 inputs and d = 64 run the CUDA-core path, which needs none
+        # fp32 inputs run the CUDA-core path, which needs none; bf16 with d = 64 runs the
+        # tensor-core path on 128-wide tiles and needs the same workspace as d = 128
         assert L.gdn_chunk_fwd_workspace_size(n, T, H, 128, 128, 0) == 0
-        assert L.gdn_chunk_fwd_workspace_size(n, T, H, 64, 64, 1) == 0
+        assert L.gdn_chunk_fwd_workspace_size(n, T, H, 64, 64, 1) == ws
+        assert L.gdn_chunk_fwd_workspace_size(n, T, H, 64, 64, 0) == 0
 
 
 def test_recurrent_step_rejects_bad_arguments():
