@@ -50,13 +50,14 @@ int main(void)
     }
     CHECK(gdn_status_string(12345) != NULL);
 
-    /* workspace sizing is host arithmetic: positive on the tensor-core path (bf16, d = 128),
-     * zero on the CUDA-core path (fp32 or d = 64), and growing with the number of tokens */
+    /* workspace sizing is host arithmetic: positive on the tensor-core path (bf16, d = 128 or 64,
+     * the same for both), zero on the CUDA-core path (fp32), and growing with the number of tokens */
     size_t w1 = gdn_chunk_fwd_workspace_size(2, 8192, 16, 128, 128, GDN_BF16);
     size_t w2 = gdn_chunk_fwd_workspace_size(2, 16384, 16, 128, 128, GDN_BF16);
     CHECK(w1 > 0 && w2 > w1);
     CHECK(gdn_chunk_fwd_workspace_size(2, 8192, 16, 128, 128, GDN_F32) == 0);
-    CHECK(gdn_chunk_fwd_workspace_size(2, 8192, 16, 64, 64, GDN_BF16) == 0);
+    CHECK(gdn_chunk_fwd_workspace_size(2, 8192, 16, 64, 64, GDN_BF16) == w1);
+    CHECK(gdn_chunk_fwd_workspace_size(2, 8192, 16, 64, 64, GDN_F32) == 0);
 
     /* argument errors come back before any launch */
     CHECK(chunk(NULL, 1, 64, 2, 2, 128, GDN_F32, NULL, 0, DP) == GDN_ERR_ARG);
