@@ -44,7 +44,10 @@ def test_decode_full_size_bf16():
     y, S, y_ref, S_ref = _decode_case("decode")
     err_y, err_S = _rel_rows(y, y_ref), rel_l2_states(S, S_ref)
     assert err_y <= TOL_BF16 and err_S <= TOL_BF16
-    # fp32 arithmetic on exactly upcast inputs: inside the fp32-input tolerance as well
+    # fp32 arithmetic on exactly upcast inputs: inside the fp32-input tolerance as well.  A tighter
+    # bar on the output is not something fp32 can promise row by row: y = S' q over 128 channels
+    # nearly cancels on a few of the 8,192 rows, and a plain fp32 evaluation of this same step in
+    # numpy already reaches 1.7e-5 on the worst row (median 1.7e-7) against the fp64 oracle.
     assert err_y < TOL_F32 and err_S < TOL_F32, (err_y, err_S)
 
 
