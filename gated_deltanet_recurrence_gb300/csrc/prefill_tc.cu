@@ -314,8 +314,9 @@ __device__ __forceinline__ bool wait_ready(const int32_t* flag) {
 // one warpgroup, so that two chunks proceed independently in one CTA.
 struct GroupBar {
     uint32_t id;
-    __device__ __forceinline__ void sync() const { bar_sync(id, 128); }
-    __device__ __forceinline__ bool sync_or(bool p) const { return bar_sync_or(id, 128, p); }
+    uint32_t n = 128;  // threads of the group
+    __device__ __forceinline__ void sync() const { bar_sync(id, n); }
+    __device__ __forceinline__ bool sync_or(bool p) const { return bar_sync_or(id, n, p); }
 };
 
 __device__ void unit_lower_inverse(const float* Af, float* Tf, int tid, GroupBar gb) {
@@ -383,19 +384,22 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 p, float* f) {
 }
 
 // Short convolution + SiLU ("因果卷积") of one loaded tile (ten 0: Q, 1: K, 2: V; 128B-swizzled
-// bf16), in place, rows 0..L-1 of the chunk starting at token t0.  Thread tid owns 8 consecutive
-// channels (one 16-byte chunk: c8 = tid % 8 of column half (tid / 8) % 2) and 8 rows (segment
-// tid / 16), so a quarter-warp reads or writes one whole 128-byte row.  Every thread first captures the
-// three raw rows before its segment (from the tile, or, for the first segment, from the sequence
-// in global memory or the carried state); after a barrier it reads its 8 raw rows, convolves
-// them and writes them back, so no thread reads a row that another one has overwritten.
+// bf16), in place, rows 0..L-1 of the chunk starting at token t0, by kT threads.  Thread tid owns 8
+// consecutive channels (one 16-byte chunk: c8 = tid % 8 of column half (tid / 8) % 2) and
+// kR = 1024 / kT rows (segment tid / 16), so a quarter-warp reads or writes one whole 128-byte row.
+// Every thread first captures the three raw rows before its segment (from the tile, or, for the
+// first segment, from the sequence in global memory or the carried state); after a barrier it
+// reads its raw rows, convolves them and writes them back, so no thread reads a row that another
+// one has overwritten.  K and Q sit in the two atom columns of the K / Q region (K rows first);
+// V's two atom columns start at kVOff, kVAtom bytes apart.
+template <int kT, uint32_t kVOff, uint32_t kVAtom>
 __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, int h, int hk, long bos,
                                            long t0, int L, int tid, GroupBar gb, int ten) {
-    using namespace prep;
-    const int c8 = tid & 7, half = (tid >> 3) & 1, r0 = (tid >> 4) * 8;
+    constexpr int kR = 1024 / kT;
+    const int c8 = tid & 7, half = (tid >> 3) & 1, r0 = (tid >> 4) * kR;
     const int x0 = half * 64 + c8 * 8;
-    // ten 0: Q, 1: K, 2: V (V occupies Q's rows once Q is no longer needed)
-    uint8_t* tile = sm + oKQ + half * 16384 + (ten == 1 ? 0 : 8192);
+    // ten 0: Q, 1: K, 2: V
+    uint8_t* tile = ten == 2 ? sm + kVOff + half * kVAtom : sm + prep::oKQ + half * 16384 + (ten == 1 ? 0 : 8192);
     const int d = a.d;
     const __nv_bfloat16* src = ten == 0 ? a.q + hk * d + x0 : (ten == 1 ? a.k + hk * d + x0 : a.v + (long)h * d + x0);
     const long stride = ten == 2 ? (long)a.H * d : (long)a.Hk * d;
@@ -424,9 +428,9 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
     }
     gb.sync();
     if (!live) return;
-    uint4 raw[8];
+    uint4 raw[kR];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kR; ++i)
         raw[i] = r0 + i < L ? *reinterpret_cast<const uint4*>(tile + sw128_offset(r0 + i, c8 * 8)) : make_uint4(0, 0, 0, 0);
     float4 w[8];
     const float4* w4 = reinterpret_cast<const float4*>(a.conv.w) + chan;
@@ -436,7 +440,7 @@ __device__ __forceinline__ void conv_tiles(uint8_t* sm, const TcArgs& a, int n, 
     float* h1 = hist[1];
     float* h2 = hist[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kR; ++i) {
         float x[8];
         unpack_bf16x8(raw[i], x);
         uint32_t o[4];
@@ -723,8 +727,8 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
     bool ok = mbar_wait(&bars[0], tma_parity, kPolls);
     if (a.conv.w) {  // fused short convolution of the loaded rows (group-uniform: has barriers)
         if (!gb.sync_or(!ok)) {
-            conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb, 0);
-            conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb, 1);
+            conv_tiles<prep::kThreads, prep::oV, 16384>(sm, a, n, h, hk, bos, t0, L, tid, gb, 0);
+            conv_tiles<prep::kThreads, prep::oV, 16384>(sm, a, n, h, hk, bos, t0, L, tid, gb, 1);
         }
     }
     if (ok && L < kC) {  // rows past the end of the sequence hold other tokens: zero them
@@ -876,7 +880,7 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
         }
         // V: landed, convolved, rows past the sequence zeroed
         const bool okv = mbar_wait(&bars[2], tma_parity, kPolls);
-        if (a.conv.w && !gb.sync_or(!okv)) conv_tiles(sm, a, n, h, hk, bos, t0, L, tid, gb, 2);
+        if (a.conv.w && !gb.sync_or(!okv)) conv_tiles<prep::kThreads, prep::oV, 16384>(sm, a, n, h, hk, bos, t0, L, tid, gb, 2);
         if (okv && L < kC) {
             for (int e = tid; e < (kC - L) * 8 * 2; e += kThreads) {
                 const int r = L + e / 16, part = e % 16;
@@ -984,6 +988,433 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant_
     tc_fence_after();
     const uint32_t tm = *tbase;
     prep_chunk<PC>(sm, tm, bars, 0, GroupBar{1}, tid, gh, &mQ, &mK, &mV, a);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tm, kTmemCols);
+    }
+}
+
+// ---- 2b. chunk preparation by eight warps (decay per head) -------------------------------------
+//
+// The same entries as prep_chunk, computed by 256 threads so that every phase's work per thread
+// halves and two chunks in flight keep 16 warps busy on an SM:
+//  - the K, Q and V tiles are requested together as the chunk starts;
+//  - the norms are summed from the loaded tiles while the Gram product [K; Q] K^T runs (N = 64:
+//    only the key columns of the Gram matrix are used);
+//  - the decays enter in the log domain: A_ij = 2^(cA_i - dK_j) (K K^T)_ij with
+//    cA_i = gc_i log2(e) + log2(beta_i kinv_i) and dK_j = gc_j log2(e) - log2(kinv_j), and
+//    Aqk_ij = 2^(cQ_i - dK_j) (Q K^T)_ij with cQ_i = gc_i log2(e) + log2(qs_i): one exponential and
+//    one product per element.  Where an element is kept (j < i, or j <= i) gc_i <= gc_j, so the
+//    exponent is at most log2 of the norm factors and nothing overflows;
+//  - T = (I + A)^-1 by block doubling.  Warps 0 and 1 each invert two 16 x 16 diagonal blocks by
+//    forward substitution and merge them, T_10 = -t_11 A_10 t_00 and T_32 = -t_33 A_32 t_22,
+//    synchronising only within the warp, while warps 2-7 write the state pass's scaled operand
+//    rows; then all eight warps take the 64 x 64 merge T_hl = -T_hh A_hl T_ll in 8 x 16 pieces.
+//    Every piece of T is written at once in fp32 (for the later merges) and as bf16 entries of the
+//    operand tiles T' = T diag(beta e^gc kinv) and T'' = T diag(beta), whose upper triangles are
+//    zeroed once per CTA and never written;
+//  - Aqk, W and U^T are staged in shared memory and leave in whole 512-byte rows per warp.
+namespace p2 {
+constexpr int kThreads = 256;
+constexpr int LDA = kC + 1;                    // A (fp32 64 x 64), odd row stride
+constexpr int LD = kC + 4;                     // T (fp32 64 x 64); its rows 0-31, columns 32-63 lie
+                                               // above the diagonal and serve the solve as scratch
+constexpr uint32_t oKQ = 0;                    // K rows 0-63 and Q rows 64-127 in two atom columns
+constexpr uint32_t oV = 32768;                 // V: two atom columns of 64 rows, 8 KB apart
+constexpr uint32_t oAf = 49152;                // A; after the products the W staging (64 x 256 B)
+constexpr uint32_t oTf = oAf + 16896;          // T; after the products the U^T staging (128 x 128 B)
+constexpr uint32_t oTP = 83968;                // T' and T'' (bf16 SW128 64 x 64, 8 KB each)
+constexpr uint32_t oAqk = oTP + 16384;         // Aqk staging (64 x 128 B, 16-byte pieces swizzled)
+constexpr uint32_t oSc = oAqk + 8192;          // per-token scalars: 10 rows of 64 fp32
+constexpr uint32_t oBar = oSc + 10 * 4 * kC;   // mbarriers (K and Q, products, V), then the TMEM base
+constexpr uint32_t kBytes = oBar + 64;
+constexpr uint32_t kSmem = kBytes + 1024;      // + alignment slack
+constexpr uint32_t kTmemCols = 128;            // the Gram product (64 columns), then W^T and U^T
+static_assert(oTf + 4 * kC * LD <= oTP && (oTP & 1023u) == 0, "layout");
+static_assert(2 * (kSmem + 1024) <= 233472, "two chunks per SM");
+enum { S_GC = 0, S_BETA, S_KINV, S_QS, S_CA, S_CQ, S_DK, S_KF, S_QF, S_TP };  // scalar rows
+}  // namespace p2
+
+// C[8 x 16] (+)= P[8 x 16] Q[16 x 16] for one warp: lane l owns row l / 4 and columns
+// 4 (l % 4) .. 4 (l % 4) + 3 of C.  P and Q are fp32 in shared memory with row strides LDP and LDQ
+// (LDQ a multiple of 4).
+template <int LDP, int LDQ>
+__device__ __forceinline__ void warp_mm8(const float* P, const float* Q, float (&c)[4], int lane) {
+    const int ii = lane >> 2, c0 = (lane & 3) * 4;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const float p = P[ii * LDP + k];
+        const float4 q = *reinterpret_cast<const float4*>(Q + k * LDQ + c0);
+        c[0] = fmaf(p, q.x, c[0]); c[1] = fmaf(p, q.y, c[1]); c[2] = fmaf(p, q.z, c[2]); c[3] = fmaf(p, q.w, c[3]);
+    }
+}
+
+// Row `row`, columns col .. col + 3 of T (fp32, negated when `neg`) into T and, scaled, into the
+// bf16 operand tiles T' and T''.
+__device__ __forceinline__ void put_t4(uint8_t* sm, float* Tf, const float* sc, int row, int col, const float (&c)[4],
+                                       bool neg) {
+    using namespace p2;
+    const float4 t = neg ? make_float4(-c[0], -c[1], -c[2], -c[3]) : make_float4(c[0], c[1], c[2], c[3]);
+    *reinterpret_cast<float4*>(Tf + row * LD + col) = t;
+    const float4 f = *reinterpret_cast<const float4*>(sc + S_TP * kC + col);
+    const float4 b = *reinterpret_cast<const float4*>(sc + S_BETA * kC + col);
+    const uint32_t off = sw128_offset(row, col);
+    *reinterpret_cast<uint2*>(sm + oTP + off) = make_uint2(pack_bf16x2(t.x * f.x, t.y * f.y), pack_bf16x2(t.z * f.z, t.w * f.w));
+    *reinterpret_cast<uint2*>(sm + oTP + 8192 + off) =
+        make_uint2(pack_bf16x2(t.x * b.x, t.y * b.y), pack_bf16x2(t.z * b.z, t.w * b.w));
+}
+
+// Inverse of the unit lower-triangular 16 x 16 diagonal block at (b0, b0) of I + A by forward
+// substitution; lane jj (0..15) computes column jj (entries above the diagonal come out zero) and
+// writes it to T, T' and T''.
+__device__ __forceinline__ void diag_inverse16(uint8_t* sm, const float* Af, float* Tf, const float* sc, int b0, int jj) {
+    using namespace p2;
+    float t[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+        // t[m] is zero for m < jj, so the sum may run over every m < ii
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < ii; ++m) {
+            if (m & 1) acc1 = fmaf(Af[(b0 + ii) * LDA + b0 + m], t[m], acc1);
+            else acc0 = fmaf(Af[(b0 + ii) * LDA + b0 + m], t[m], acc0);
+        }
+        t[ii] = ii < jj ? 0.f : (ii == jj ? 1.f : -(acc0 + acc1));
+    }
+    const int j = b0 + jj;
+    const float fj = sc[S_TP * kC + j], bj = sc[S_BETA * kC + j];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) {
+        Tf[(b0 + ii) * LD + j] = t[ii];
+        const uint32_t off = sw128_offset(b0 + ii, j);
+        *reinterpret_cast<__nv_bfloat16*>(sm + oTP + off) = __float2bfloat16_rn(t[ii] * fj);
+        *reinterpret_cast<__nv_bfloat16*>(sm + oTP + 8192 + off) = __float2bfloat16_rn(t[ii] * bj);
+    }
+}
+
+// Zero the operand tiles T' and T'' (their upper triangles are never written afterwards); run by
+// every thread of a preparation group before its first chunk.
+__device__ __forceinline__ void prep2_init_tiles(uint8_t* sm, int tid) {
+    for (int e = tid; e < 16384 / 16; e += p2::kThreads)
+        reinterpret_cast<uint4*>(sm + p2::oTP)[e] = make_uint4(0, 0, 0, 0);
+}
+
+// One chunk of one head by 256 threads (tid 0..255, synchronised by `gb`): everything the state
+// pass needs from it, written to the workspace.  `sm` is the chunk's 1024-aligned shared region,
+// `tm` its 128 TMEM columns, `bars` its three mbarriers; the tile barriers complete with parity
+// `tma_parity`.  Returns false after a timed-out wait (recorded in the error word); the tile
+// copies in flight have then landed or timed out too.
+__device__ __forceinline__ bool prep2_chunk(uint8_t* sm, uint32_t tm, uint64_t* bars, uint32_t tma_parity,
+                                            GroupBar gb, int tid, long gh, const CUtensorMap* mQ,
+                                            const CUtensorMap* mK, const CUtensorMap* mV, const TcArgs& a) {
+    using namespace p2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    float* Af = reinterpret_cast<float*>(sm + oAf);
+    float* Tf = reinterpret_cast<float*>(sm + oTf);
+    float* sc = reinterpret_cast<float*>(sm + oSc);
+    const int warp = tid >> 5, lane = tid & 31;
+    const int chunk = (int)(gh / a.H), h = (int)(gh % a.H);  // gh = chunk * H + head
+    const int hk = h / (a.H / a.Hk);                         // query/key head read by value head h
+    const int n = a.chunk_seq[chunk];
+    long bos, eos;
+    seq_bounds(a, n, bos, eos);
+    const long t0 = bos + (long)(chunk - a.chunk_first[n]) * kC;
+    const int L = (eos - t0 < kC) ? (int)(eos - t0) : kC;
+    auto fail = [&]() {
+        if (tid == 0) {
+            record_error(a.err, GDN_ERR_TIMEOUT);
+            mbar_wait(&bars[0], tma_parity, kPolls);  // no tile copy may still be in flight
+            mbar_wait(&bars[2], tma_parity, kPolls);
+        }
+        return false;
+    };
+
+    if (tid == 0) {
+        fence_async_smem();  // the previous chunk's generic accesses to the tiles come first
+        mbar_arrive_expect_tx(&bars[0], 32768);
+        for (int c = 0; c < 2; ++c) {
+            tma_load_3d(sm + oKQ + c * 16384, mK, &bars[0], c * 64, hk, (int)t0);
+            tma_load_3d(sm + oKQ + c * 16384 + 8192, mQ, &bars[0], c * 64, hk, (int)t0);
+        }
+        mbar_arrive_expect_tx(&bars[2], 16384);
+        for (int c = 0; c < 2; ++c) tma_load_3d(sm + oV + c * 8192, mV, &bars[2], c * 64, h, (int)t0);
+    }
+    if (warp == 0) {  // gc: inclusive sums of g down the chunk, two tokens per lane
+        const int i0 = 2 * lane;
+        const float g0 = i0 < L ? a.g[(t0 + i0) * a.H + h] : 0.f;
+        const float g1 = i0 + 1 < L ? a.g[(t0 + i0 + 1) * a.H + h] : 0.f;
+        float s = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += t;
+        }
+        sc[S_GC * kC + i0] = s - g1;
+        sc[S_GC * kC + i0 + 1] = s;
+    } else if (warp == 1) {
+        const int i0 = 2 * lane;
+        sc[S_BETA * kC + i0] = i0 < L ? a.beta[(t0 + i0) * a.H + h] : 0.f;
+        sc[S_BETA * kC + i0 + 1] = i0 + 1 < L ? a.beta[(t0 + i0 + 1) * a.H + h] : 0.f;
+    }
+    const bool ok = mbar_wait(&bars[0], tma_parity, kPolls);
+    if (gb.sync_or(!ok)) return fail();
+    if (a.conv.w) {  // fused short convolution of the loaded rows
+        conv_tiles<kThreads, oV, 8192>(sm, a, n, h, hk, bos, t0, L, tid, gb, 0);
+        conv_tiles<kThreads, oV, 8192>(sm, a, n, h, hk, bos, t0, L, tid, gb, 1);
+    }
+    if (L < kC) {  // rows past the end of the sequence hold other tokens: zero them
+        for (int e = tid; e < (kC - L) * 8 * 4; e += kThreads) {
+            const int r = L + e / 32, part = e % 32;  // 4 tiles (K, Q x 2 atom columns) x 8 pieces of 16 B
+            const int tile = part / 8, ch = part % 8;
+            *reinterpret_cast<uint4*>(sm + oKQ + (tile & 1) * 16384 + (tile >> 1) * 8192 + r * 128 + ch * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (a.conv.w || L < kC) fence_async_smem();  // generic writes to the tiles, read next by the tensor cores
+    gb.sync();
+    if (tid == 0) {  // Gram product: rows [K; Q] (M = 128) against the key rows (N = 64)
+        tc_fence_after();
+        const uint32_t kq = smem_u32(sm + oKQ);
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_bf16_ss(tm, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024),
+                        idesc_bf16(128, 64, 0, 0), k > 0);
+        }
+        mma_commit(&bars[1]);
+    }
+    {   // norms from the tiles: a quarter-warp takes 8 rows (8 distinct swizzle phases) of one atom
+        // column, the partner lane (lane ^ 8) the other column of the same rows
+        const int r = warp * 16 + (lane & 7) + ((lane >> 4) << 3);  // K rows 0-63, then Q rows
+        const int hc = (lane >> 3) & 1;
+        const uint8_t* rowp = sm + oKQ + hc * 16384 + (r >> 6) * 8192 + (r & 63) * 128;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float f[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s4[e & 3] = fmaf(f[e], f[e], s4[e & 3]);
+        }
+        float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        if (hc == 0) {
+            const float inv = a.use_l2 ? rsqrtf(ss + kL2Eps) : 1.0f;
+            if (r < kC) sc[S_KINV * kC + r] = inv;
+            else sc[S_QS * kC + r - kC] = a.scale * inv;
+        }
+    }
+    gb.sync();
+    if (tid < kC) {  // per-token factors
+        const int i = tid;
+        const float gi = sc[S_GC * kC + i], glast = sc[S_GC * kC + kC - 1];
+        const float bt = sc[S_BETA * kC + i], ki = sc[S_KINV * kC + i], qs = sc[S_QS * kC + i];
+        const float egi = __expf(gi);
+        sc[S_CA * kC + i] = gi * kLog2e + __log2f(bt * ki);
+        sc[S_CQ * kC + i] = gi * kLog2e + __log2f(qs);
+        sc[S_DK * kC + i] = gi * kLog2e - __log2f(ki);
+        sc[S_KF * kC + i] = __expf(glast - gi) * ki;   // K~ rows
+        sc[S_QF * kC + i] = egi * qs;                  // Q~ rows
+        sc[S_TP * kC + i] = bt * egi * ki;             // columns of T' = T diag(beta e^gc kinv)
+        if (i == 0) a.scal[gh * 4 * kC + 3 * kC] = __expf(glast);  // the chunk's decay gamma
+    }
+    const bool okg = mbar_wait(&bars[1], 0, kPolls);
+    tc_fence_after();
+    if (gb.sync_or(!okg)) return fail();
+    {   // ---- E1: Gram rows -> A (fp32, shared) and Aqk (bf16, staged) ----
+        // warp: TMEM lanes 32 q4 .. 32 q4 + 31 (Gram rows: K rows for q4 < 2, Q rows above),
+        // columns j0 .. j0 + 31
+        const int q4 = warp & 3, j0 = 32 * (warp >> 2);
+        const bool isq = q4 >= 2;
+        const int i = 32 * (q4 & 1) + lane;              // token of the row
+        const int lim = isq ? i + 1 : i;                 // kept columns: j < lim
+        const bool empty = j0 == 32 && (q4 & 1) == 0;    // every column of the warp lies past its rows
+        uint4* stage = reinterpret_cast<uint4*>(sm + oAqk + i * 128);  // Aqk row i: piece c at c ^ (i & 7)
+        if (!empty) {
+            uint32_t r[32];
+            tmem_ld32(tm + (static_cast<uint32_t>(32 * q4) << 16) + (uint32_t)j0, r);
+            tmem_wait_ld();
+            const float ci = sc[(isq ? S_CQ : S_CA) * kC + i];
+            const float* dk = sc + S_DK * kC + j0;
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float x = ex2_approx(ci - dk[e]) * __uint_as_float(r[e]);
+                v[e] = j0 + e < lim ? x : 0.f;
+            }
+            if (!isq) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) Af[i * LDA + j0 + e] = v[e];
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) stage[((j0 >> 3) + c) ^ (i & 7)] = pack_bf16x8(v + 8 * c);
+            }
+        } else if (isq) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) stage[((j0 >> 3) + c) ^ (i & 7)] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    tc_fence_before();
+    gb.sync();
+    if (warp < 2) {
+        // ---- warp w: diagonal blocks 2w (lanes 0-15) and 2w + 1 (lanes 16-31), then their merge
+        //      T_{b,b-1} = -t_b (A_{b,b-1} t_{b-1}), b = 2w + 1 ----
+        diag_inverse16(sm, Af, Tf, sc, 32 * warp + 16 * (lane >> 4), lane & 15);
+        __syncwarp();
+        const int b = 2 * warp + 1;
+        float* Y = Tf + 32 + 16 * warp;  // scratch: rows 0-15 of T, columns 32 + 16 w ..
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+            warp_mm8<LDA, LD>(Af + (16 * b + 8 * hh) * LDA + 16 * (b - 1), Tf + 16 * (b - 1) * LD + 16 * (b - 1), c[hh], lane);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+            *reinterpret_cast<float4*>(Y + (8 * hh + (lane >> 2)) * LD + (lane & 3) * 4) =
+                make_float4(c[hh][0], c[hh][1], c[hh][2], c[hh][3]);
+        __syncwarp();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            warp_mm8<LD, LD>(Tf + (16 * b + 8 * hh) * LD + 16 * b, Y, d, lane);
+            put_t4(sm, Tf, sc, 16 * b + 8 * hh + (lane >> 2), 16 * (b - 1) + (lane & 3) * 4, d, true);
+        }
+    } else {
+        // ---- meanwhile: the operand rows K~ = diag(kf) K and Q~ = diag(qf) Q (2 tensors x 64 rows
+        //      x 16 pieces of 16 B over 192 threads; a warp writes 2 whole rows), then Aqk ----
+#pragma unroll
+        for (int it = 0; it < 11; ++it) {
+            const int flat = it * (kThreads - 64) + tid - 64;
+            if (flat < 2048) {
+                const int isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + oKQ + (c16 >> 3) * 16384 + (isq ? 8192 : 0) +
+                                                                  sw128_offset(r, (c16 & 7) * 8));
+                const float fr = sc[(isq ? S_QF : S_KF) * kC + r];
+                float v[8];
+                unpack_bf16x8(raw, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= fr;
+                *reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)r * kD + c16 * 8) = pack_bf16x8(v);
+            }
+        }
+        uint4* adst = reinterpret_cast<uint4*>(a.Aqk + gh * kC * kC);
+#pragma unroll
+        for (int it = 0; it < 3; ++it) {  // 64 rows x 8 pieces
+            const int flat = it * (kThreads - 64) + tid - 64;
+            if (flat < 512) {
+                const int r = flat >> 3, c8 = flat & 7;
+                adst[flat] = reinterpret_cast<const uint4*>(sm + oAqk + r * 128)[c8 ^ (r & 7)];
+            }
+        }
+    }
+    gb.sync();
+    {   // ---- the 64 x 64 merge: X = A_hl T_ll, then T_hl = -T_hh X, as 2 x 2 blocks of 16 ----
+        // warp: output block (p, q) of the 32 x 32 result, rows r8 .. r8 + 7 of it
+        float* X = Tf + 32;  // scratch: rows 0-31, columns 32-63 of T
+        const int p = warp >> 2, q = (warp >> 1) & 1, r8 = (warp & 1) * 8;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k = q; k < 2; ++k)  // T_ll is lower triangular: block (k, q) vanishes for k < q
+            warp_mm8<LDA, LD>(Af + (32 + 16 * p + r8) * LDA + 16 * k, Tf + 16 * k * LD + 16 * q, c, lane);
+        *reinterpret_cast<float4*>(X + (16 * p + r8 + (lane >> 2)) * LD + 16 * q + (lane & 3) * 4) =
+            make_float4(c[0], c[1], c[2], c[3]);
+        gb.sync();
+        c[0] = c[1] = c[2] = c[3] = 0.f;
+        for (int k = 0; k <= p; ++k)  // T_hh is lower triangular: block (p, k) vanishes for k > p
+            warp_mm8<LD, LD>(Tf + (32 + 16 * p + r8) * LD + 32 + 16 * k, X + 16 * k * LD + 16 * q, c, lane);
+        put_t4(sm, Tf, sc, 32 + 16 * p + r8 + (lane >> 2), 16 * q + (lane & 3) * 4, c, true);
+    }
+    // V: landed, convolved, rows past the sequence zeroed
+    const bool okv = mbar_wait(&bars[2], tma_parity, kPolls);
+    if (gb.sync_or(!okv)) return fail();
+    if (a.conv.w) conv_tiles<kThreads, oV, 8192>(sm, a, n, h, hk, bos, t0, L, tid, gb, 2);
+    if (L < kC) {
+        for (int e = tid; e < (kC - L) * 16; e += kThreads) {
+            const int r = L + e / 16, part = e % 16;
+            *reinterpret_cast<uint4*>(sm + oV + (part >> 3) * 8192 + r * 128 + (part & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    fence_async_smem();  // T', T'' and any rewritten V rows, read next by the tensor cores
+    gb.sync();
+    if (tid == 0) {  // W^T = K^T T'^T and U^T = V^T T''^T (K and V as MN-major operands)
+        tc_fence_after();
+        const uint32_t kq = smem_u32(sm + oKQ), vv = smem_u32(sm + oV);
+        const uint32_t tp = smem_u32(sm + oTP), tpp = tp + 8192;
+        for (int k = 0; k < 4; ++k)
+            mma_bf16_ss(tm + 0, sdesc_sw128(kq + k * 2048, 16384, 1024), sdesc_sw128(tp + k * 32, 16, 1024),
+                        idesc_bf16(128, 64, 1, 0), k > 0);
+        for (int k = 0; k < 4; ++k)
+            mma_bf16_ss(tm + 64, sdesc_sw128(vv + k * 2048, 8192, 1024), sdesc_sw128(tpp + k * 32, 16, 1024),
+                        idesc_bf16(128, 64, 1, 0), k > 0);
+        mma_commit(&bars[1]);
+    }
+    const bool ok2 = mbar_wait(&bars[1], 1, kPolls);
+    tc_fence_after();
+    if (gb.sync_or(!ok2)) return fail();
+    {   // ---- E2: W (token-major) and U^T (row per value channel), staged over A and T ----
+        // thread: TMEM lane d = key channel (W^T) and value channel (U^T), tokens 32 th .. 32 th + 31
+        const int q4 = warp & 3, th = warp >> 2;
+        const int d = 32 * q4 + lane;
+        const uint32_t lrow = static_cast<uint32_t>(32 * q4) << 16;
+        uint32_t w[32], u[32];
+        tmem_ld32(tm + lrow + (uint32_t)(32 * th), w);
+        tmem_ld32(tm + lrow + 64u + (uint32_t)(32 * th), u);
+        tmem_wait_ld();
+        __nv_bfloat16* wst = reinterpret_cast<__nv_bfloat16*>(sm + oAf) + (32 * th) * kD + d;  // [64][128]
+#pragma unroll
+        for (int e = 0; e < 32; ++e) wst[e * kD] = __float2bfloat16_rn(__uint_as_float(w[e]));
+        uint4* ust = reinterpret_cast<uint4*>(sm + oTf + d * 128);  // U^T row d: piece c at c ^ (d & 7)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ust[(4 * th + c) ^ (d & 7)] = pack_bf16x8(reinterpret_cast<const float*>(u) + 8 * c);
+    }
+    tc_fence_before();
+    gb.sync();
+    {   // whole rows out: W 1024 pieces of 16 B, U^T 1024
+        uint4* wdst = reinterpret_cast<uint4*>(a.W + gh * kC * kD);
+        uint4* udst = reinterpret_cast<uint4*>(a.Ut + gh * kD * kC);
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = it * kThreads + tid;
+            wdst[e] = reinterpret_cast<const uint4*>(sm + oAf)[e];
+            const int r = e >> 3;
+            udst[e] = reinterpret_cast<const uint4*>(sm + oTf + r * 128)[(e & 7) ^ (r & 7)];
+        }
+    }
+    gb.sync();  // every read of this chunk's tiles, scalars and TMEM is done
+    return true;
+}
+
+__global__ void __launch_bounds__(p2::kThreads, 2)
+chunk_prep2_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                   const __grid_constant__ CUtensorMap mV, TcArgs a) {
+    using namespace p2;
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 32);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const long n_items = (long)a.n_chunks[0] * a.H;  // chunk-head pairs, item gh = chunk * H + head
+    if ((long)blockIdx.x >= n_items) return;
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        prefetch_tmap(&mQ);
+        prefetch_tmap(&mK);
+        prefetch_tmap(&mV);
+    }
+    if (warp == 0) {
+        tmem_alloc(tbase, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tbase;
+    prep2_init_tiles(sm, tid);
+    uint32_t parity = 0;
+    for (long gh = blockIdx.x; gh < n_items; gh += gridDim.x) {
+        if (!prep2_chunk(sm, tm, bars, parity, GroupBar{1, kThreads}, tid, gh, &mQ, &mK, &mV, a)) break;
+        parity ^= 1u;
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -1506,18 +1937,26 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
 // With few (sequence, head) units the serial pass occupies few SMs, yet it can only start after the
 // whole preparation kernel.  The fused kernel runs both in one cooperative launch (one CTA per SM,
 // all resident at once): CTAs 0 .. n_units-1 each run the serial pass of one unit; every other CTA
-// prepares three chunks at a time (one per warpgroup, each with its own shared region, 128 TMEM
-// columns and named barriers), taking chunks from a global counter position by position (the
-// first chunk of every unit, then the second, ...), so the serial passes find their next chunk
-// ready.  A prepared chunk is published by a release store of its flag, which the serial pass
-// acquires (bounded) before reading the chunk's entries.  Preparing CTAs never wait for serial ones.
+// prepares chunks, two at a time with a decay per head (two groups of eight warps, prep2_chunk) and
+// three at a time with a decay per key channel (one per warpgroup, prep_chunk), each with its own
+// shared region, 128 TMEM columns and named barriers.  They take chunks from a global counter
+// position by position (the first chunk of every unit, then the second, ...), so the serial passes
+// find their next chunk ready.  A prepared chunk is published by a release store of its flag, which
+// the serial pass acquires (bounded) before reading the chunk's entries.  Preparing CTAs never wait
+// for serial ones.
 namespace fz {
 constexpr uint32_t kPrepStride = (prep::kBytes + 1023u) & ~1023u;
 constexpr int kInst = 3;                          // chunk preparations per preparing CTA
 constexpr uint32_t oTmemBase = kInst * kPrepStride;  // prep role: TMEM base address
 constexpr uint32_t oItem = oTmemBase + 16;        // prep role: work item of each warpgroup
 constexpr uint32_t kPrepBytes = oItem + 8 * kInst;
-constexpr uint32_t kSmem = st::kSmem > kPrepBytes + 1024 ? st::kSmem : kPrepBytes + 1024;
+// decay per head: two eight-warp preparations
+constexpr uint32_t kPrepStride2 = (p2::kBytes + 1023u) & ~1023u;
+constexpr uint32_t oTmemBase2 = 2 * kPrepStride2;
+constexpr uint32_t oItem2 = oTmemBase2 + 16;
+constexpr uint32_t kPrepBytes2 = oItem2 + 16;
+constexpr uint32_t kPrepMax = kPrepBytes > kPrepBytes2 ? kPrepBytes : kPrepBytes2;
+constexpr uint32_t kSmem = st::kSmem > kPrepMax + 1024 ? st::kSmem : kPrepMax + 1024;
 static_assert(kSmem <= 232448, "fused kernel shared memory exceeds the per-block limit");
 // register split of the prep role (launched at 128 per thread, 512 x 128 = 65536):
 // three preparing warpgroups at 160 and the fourth at 24: 3 x 128 x 160 + 128 x 24 = 64512
@@ -1540,38 +1979,38 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
         return;
     }
     using namespace fz;
-    const int tid = threadIdx.x, warp = tid >> 5, wg = tid >> 7, ltid = tid & 127;
-    uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oTmemBase);
-    volatile long* item_slot = reinterpret_cast<volatile long*>(sm + oItem);
-    if (tid == 0) {
-        for (int i = 0; i < kInst; ++i) {
-            uint64_t* b = reinterpret_cast<uint64_t*>(sm + i * kPrepStride + prep::oBar);
-            for (int j = 0; j < 3; ++j) mbar_init(&b[j], 1);
+    if constexpr (!PC) {
+        const int tid = threadIdx.x, warp = tid >> 5, inst = tid >> 8, ltid = tid & 255;
+        uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oTmemBase2);
+        volatile long* item_slot = reinterpret_cast<volatile long*>(sm + oItem2);
+        if (tid == 0) {
+            for (int i = 0; i < 2; ++i) {
+                uint64_t* b = reinterpret_cast<uint64_t*>(sm + i * kPrepStride2 + p2::oBar);
+                for (int j = 0; j < 3; ++j) mbar_init(&b[j], 1);
+            }
+            fence_mbar_init();
+            prefetch_tmap(&mQ);
+            prefetch_tmap(&mK);
+            prefetch_tmap(&mV);
         }
-        fence_mbar_init();
-        prefetch_tmap(&mQ);
-        prefetch_tmap(&mK);
-        prefetch_tmap(&mV);
-    }
-    if (warp == 0) {
-        tmem_alloc(tbase, 512);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = *tbase;
-    if (wg < kInst) {
-        reg_alloc<kRegsPrep>();
-        uint8_t* smi = sm + wg * kPrepStride;
-        uint64_t* bars = reinterpret_cast<uint64_t*>(smi + prep::oBar);
-        const GroupBar gb{1u + 2u * (uint32_t)wg};
+        if (warp == 0) {
+            tmem_alloc(tbase, 2 * p2::kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tm = *tbase;
+        uint8_t* smi = sm + inst * kPrepStride2;
+        uint64_t* bars = reinterpret_cast<uint64_t*>(smi + p2::oBar);
+        const GroupBar gb{1u + (uint32_t)inst, (uint32_t)p2::kThreads};
+        prep2_init_tiles(smi, ltid);
         const long n_items = (long)a.n_chunks[1] * n_units;
         uint32_t parity = 0;
         for (;;) {
-            if (ltid == 0) item_slot[wg] = atomicAdd(&a.n_chunks[2], 1);
+            if (ltid == 0) item_slot[inst] = atomicAdd(&a.n_chunks[2], 1);
             gb.sync();
-            const long item = item_slot[wg];
+            const long item = item_slot[inst];
             gb.sync();  // the slot is rewritten only after every thread has read it
             if (item >= n_items) break;
             const int pos = (int)(item / n_units), unit = (int)(item % n_units);
@@ -1579,7 +2018,8 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
             const int first = a.chunk_first[nn];
             if (pos >= a.chunk_first[nn + 1] - first) continue;  // this sequence is shorter
             const long gh = (long)(first + pos) * a.H + hh;
-            prep_chunk<PC>(smi, tm + (uint32_t)wg * prep::kTmemCols, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a);
+            if (!prep2_chunk(smi, tm + (uint32_t)inst * p2::kTmemCols, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a))
+                break;
             parity ^= 1u;
             __threadfence();
             gb.sync();
@@ -1588,14 +2028,70 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 st_release_gpu(a.ready + gh, 1);
             }
         }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tm, 2 * p2::kTmemCols);
+        }
     } else {
-        reg_dealloc<kRegsIdle>();
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
+        const int tid = threadIdx.x, warp = tid >> 5, wg = tid >> 7, ltid = tid & 127;
+        uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oTmemBase);
+        volatile long* item_slot = reinterpret_cast<volatile long*>(sm + oItem);
+        if (tid == 0) {
+            for (int i = 0; i < kInst; ++i) {
+                uint64_t* b = reinterpret_cast<uint64_t*>(sm + i * kPrepStride + prep::oBar);
+                for (int j = 0; j < 3; ++j) mbar_init(&b[j], 1);
+            }
+            fence_mbar_init();
+            prefetch_tmap(&mQ);
+            prefetch_tmap(&mK);
+            prefetch_tmap(&mV);
+        }
+        if (warp == 0) {
+            tmem_alloc(tbase, 512);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
         tc_fence_after();
-        tmem_dealloc(tm, 512);
+        const uint32_t tm = *tbase;
+        if (wg < kInst) {
+            reg_alloc<kRegsPrep>();
+            uint8_t* smi = sm + wg * kPrepStride;
+            uint64_t* bars = reinterpret_cast<uint64_t*>(smi + prep::oBar);
+            const GroupBar gb{1u + 2u * (uint32_t)wg};
+            const long n_items = (long)a.n_chunks[1] * n_units;
+            uint32_t parity = 0;
+            for (;;) {
+                if (ltid == 0) item_slot[wg] = atomicAdd(&a.n_chunks[2], 1);
+                gb.sync();
+                const long item = item_slot[wg];
+                gb.sync();  // the slot is rewritten only after every thread has read it
+                if (item >= n_items) break;
+                const int pos = (int)(item / n_units), unit = (int)(item % n_units);
+                const int nn = unit / a.H, hh = unit % a.H;
+                const int first = a.chunk_first[nn];
+                if (pos >= a.chunk_first[nn + 1] - first) continue;  // this sequence is shorter
+                const long gh = (long)(first + pos) * a.H + hh;
+                prep_chunk<PC>(smi, tm + (uint32_t)wg * prep::kTmemCols, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a);
+                parity ^= 1u;
+                __threadfence();
+                gb.sync();
+                if (ltid == 0) {
+                    fence_proxy_async_global();
+                    st_release_gpu(a.ready + gh, 1);
+                }
+            }
+        } else {
+            reg_dealloc<kRegsIdle>();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(tm, 512);
+        }
     }
 }
 
@@ -1725,11 +2221,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
         return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_fn), dim3((unsigned)sms),
                                            dim3(st::kThreads), args, fz::kSmem, s);
     }
-    auto prep_fn = p.g_per_channel ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
     auto state_fn = p.g_per_channel ? chunk_state_kernel<true> : chunk_state_kernel<false>;
-    e = cudaFuncSetAttribute(prep_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep::kSmem);
-    if (e != cudaSuccess) return e;
-    prep_fn<<<(unsigned)L.nch, prep::kThreads, prep::kSmem, s>>>(mQ, mK, mV, a);
+    if (p.g_per_channel) {  // one CTA of four warps per chunk-head pair
+        e = cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep::kSmem);
+        if (e != cudaSuccess) return e;
+        chunk_prep_kernel<true><<<(unsigned)L.nch, prep::kThreads, prep::kSmem, s>>>(mQ, mK, mV, a);
+    } else {  // two resident CTAs of eight warps per SM, each walking the chunk-head pairs
+        e = cudaFuncSetAttribute(chunk_prep2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p2::kSmem);
+        if (e != cudaSuccess) return e;
+        const long grid = L.nch < 2L * sms ? L.nch : 2L * sms;
+        chunk_prep2_kernel<<<(unsigned)grid, p2::kThreads, p2::kSmem, s>>>(mQ, mK, mV, a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(state_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st::kSmem);
