@@ -1101,13 +1101,62 @@ __device__ __forceinline__ void prep2_init_tiles(uint8_t* sm, int tid) {
         reinterpret_cast<uint4*>(sm + p2::oTP)[e] = make_uint4(0, 0, 0, 0);
 }
 
+// Where chunk-head item gh = chunk * H + head lies in the packed tokens.
+struct ChunkPos {
+    long gh, t0, bos;
+    int n, h, hk, L;
+};
+__device__ __forceinline__ ChunkPos chunk_pos(const TcArgs& a, long gh) {
+    ChunkPos p;
+    p.gh = gh;
+    const int chunk = (int)(gh / a.H);
+    p.h = (int)(gh % a.H);
+    p.hk = p.h / (a.H / a.Hk);  // query/key head read by value head h
+    p.n = a.chunk_seq[chunk];
+    long eos;
+    seq_bounds(a, p.n, p.bos, eos);
+    p.t0 = p.bos + (long)(chunk - a.chunk_first[p.n]) * kC;
+    p.L = (eos - p.t0 < kC) ? (int)(eos - p.t0) : kC;
+    return p;
+}
+
+// Thread 0: request the K, Q (one barrier) and V (another) tiles of chunk p.
+__device__ __forceinline__ void prep2_issue(uint8_t* sm, uint64_t* bars, const ChunkPos& p, const CUtensorMap* mQ,
+                                            const CUtensorMap* mK, const CUtensorMap* mV) {
+    using namespace p2;
+    fence_async_smem();  // earlier generic accesses to the tiles come first
+    mbar_arrive_expect_tx(&bars[0], 32768);
+    for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sm + oKQ + c * 16384, mK, &bars[0], c * 64, p.hk, (int)p.t0);
+        tma_load_3d(sm + oKQ + c * 16384 + 8192, mQ, &bars[0], c * 64, p.hk, (int)p.t0);
+    }
+    mbar_arrive_expect_tx(&bars[2], 16384);
+    for (int c = 0; c < 2; ++c) tma_load_3d(sm + oV + c * 8192, mV, &bars[2], c * 64, p.h, (int)p.t0);
+}
+
+// Warp 0: g, warp 1: beta of tokens 2 lane and 2 lane + 1 of chunk p into x0, x1 (zero past the
+// sequence).  Other warps leave x0, x1 alone.  Only loads: the values are first used at the start
+// of the chunk, so a prefetch leaves them in flight meanwhile.
+__device__ __forceinline__ void prep2_load_gb(const TcArgs& a, const ChunkPos& p, int warp, int lane, float& x0, float& x1) {
+    const int i0 = 2 * lane;
+    if (warp < 2) {
+        const float* src = (warp == 0 ? a.g : a.beta) + p.t0 * a.H + p.h;
+        x0 = i0 < p.L ? src[(long)i0 * a.H] : 0.f;
+        x1 = i0 + 1 < p.L ? src[(long)(i0 + 1) * a.H] : 0.f;
+    }
+}
+
 // One chunk of one head by 256 threads (tid 0..255, synchronised by `gb`): everything the state
 // pass needs from it, written to the workspace.  `sm` is the chunk's 1024-aligned shared region,
 // `tm` its 128 TMEM columns, `bars` its three mbarriers; the tile barriers complete with parity
-// `tma_parity`.  Returns false after a timed-out wait (recorded in the error word); the tile
-// copies in flight have then landed or timed out too.
+// `tma_parity`.  When `loaded`, the chunk's tiles were requested and its g / beta values (x0, x1
+// of warps 0 and 1, see prep2_load_gb) loaded during the previous chunk.  With `more`, the next
+// chunk `nxt`'s tiles are requested as soon as this chunk's products have read the tiles, and its
+// g / beta go to x0, x1.  Returns false after a timed-out wait (recorded in the error word);
+// the tile copies in flight have then landed or timed out too.
 __device__ __forceinline__ bool prep2_chunk(uint8_t* sm, uint32_t tm, uint64_t* bars, uint32_t tma_parity,
-                                            GroupBar gb, int tid, long gh, const CUtensorMap* mQ,
+                                            GroupBar gb, int tid, const ChunkPos& cur, bool loaded,
+                                            const ChunkPos& nxt, bool more, float& x0, float& x1, const CUtensorMap* mQ,
                                             const CUtensorMap* mK, const CUtensorMap* mV, const TcArgs& a) {
     using namespace p2;
     constexpr float kLog2e = 1.4426950408889634f;
@@ -1115,13 +1164,8 @@ __device__ __forceinline__ bool prep2_chunk(uint8_t* sm, uint32_t tm, uint64_t* 
     float* Tf = reinterpret_cast<float*>(sm + oTf);
     float* sc = reinterpret_cast<float*>(sm + oSc);
     const int warp = tid >> 5, lane = tid & 31;
-    const int chunk = (int)(gh / a.H), h = (int)(gh % a.H);  // gh = chunk * H + head
-    const int hk = h / (a.H / a.Hk);                         // query/key head read by value head h
-    const int n = a.chunk_seq[chunk];
-    long bos, eos;
-    seq_bounds(a, n, bos, eos);
-    const long t0 = bos + (long)(chunk - a.chunk_first[n]) * kC;
-    const int L = (eos - t0 < kC) ? (int)(eos - t0) : kC;
+    const long gh = cur.gh, t0 = cur.t0, bos = cur.bos;
+    const int n = cur.n, h = cur.h, hk = cur.hk, L = cur.L;
     auto fail = [&]() {
         if (tid == 0) {
             record_error(a.err, GDN_ERR_TIMEOUT);
@@ -1131,32 +1175,22 @@ __device__ __forceinline__ bool prep2_chunk(uint8_t* sm, uint32_t tm, uint64_t* 
         return false;
     };
 
-    if (tid == 0) {
-        fence_async_smem();  // the previous chunk's generic accesses to the tiles come first
-        mbar_arrive_expect_tx(&bars[0], 32768);
-        for (int c = 0; c < 2; ++c) {
-            tma_load_3d(sm + oKQ + c * 16384, mK, &bars[0], c * 64, hk, (int)t0);
-            tma_load_3d(sm + oKQ + c * 16384 + 8192, mQ, &bars[0], c * 64, hk, (int)t0);
-        }
-        mbar_arrive_expect_tx(&bars[2], 16384);
-        for (int c = 0; c < 2; ++c) tma_load_3d(sm + oV + c * 8192, mV, &bars[2], c * 64, h, (int)t0);
+    if (!loaded) {
+        if (tid == 0) prep2_issue(sm, bars, cur, mQ, mK, mV);
+        prep2_load_gb(a, cur, warp, lane, x0, x1);
     }
     if (warp == 0) {  // gc: inclusive sums of g down the chunk, two tokens per lane
-        const int i0 = 2 * lane;
-        const float g0 = i0 < L ? a.g[(t0 + i0) * a.H + h] : 0.f;
-        const float g1 = i0 + 1 < L ? a.g[(t0 + i0 + 1) * a.H + h] : 0.f;
-        float s = g0 + g1;
+        float sum = x0 + x1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float t = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += t;
+            const float t = __shfl_up_sync(0xffffffffu, sum, o);
+            if (lane >= o) sum += t;
         }
-        sc[S_GC * kC + i0] = s - g1;
-        sc[S_GC * kC + i0 + 1] = s;
+        sc[S_GC * kC + 2 * lane] = sum - x1;
+        sc[S_GC * kC + 2 * lane + 1] = sum;
     } else if (warp == 1) {
-        const int i0 = 2 * lane;
-        sc[S_BETA * kC + i0] = i0 < L ? a.beta[(t0 + i0) * a.H + h] : 0.f;
-        sc[S_BETA * kC + i0 + 1] = i0 + 1 < L ? a.beta[(t0 + i0 + 1) * a.H + h] : 0.f;
+        sc[S_BETA * kC + 2 * lane] = x0;
+        sc[S_BETA * kC + 2 * lane + 1] = x1;
     }
     const bool ok = mbar_wait(&bars[0], tma_parity, kPolls);
     if (gb.sync_or(!ok)) return fail();
@@ -1350,6 +1384,10 @@ __device__ __forceinline__ bool prep2_chunk(uint8_t* sm, uint32_t tm, uint64_t* 
     const bool ok2 = mbar_wait(&bars[1], 1, kPolls);
     tc_fence_after();
     if (gb.sync_or(!ok2)) return fail();
+    if (more) {  // the products have read the tiles: the next chunk's tiles and scalars now
+        if (tid == 0) prep2_issue(sm, bars, nxt, mQ, mK, mV);
+        prep2_load_gb(a, nxt, warp, lane, x0, x1);
+    }
     {   // ---- E2: W (token-major) and U^T (row per value channel), staged over A and T ----
         // thread: TMEM lane d = key channel (W^T) and value channel (U^T), tokens 32 th .. 32 th + 31
         const int q4 = warp & 3, th = warp >> 2;
@@ -1411,9 +1449,18 @@ chunk_prep2_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     const uint32_t tm = *tbase;
     prep2_init_tiles(sm, tid);
     uint32_t parity = 0;
+    float x0 = 0.f, x1 = 0.f;
+    ChunkPos cur = chunk_pos(a, blockIdx.x);
+    bool loaded = false;
     for (long gh = blockIdx.x; gh < n_items; gh += gridDim.x) {
-        if (!prep2_chunk(sm, tm, bars, parity, GroupBar{1, kThreads}, tid, gh, &mQ, &mK, &mV, a)) break;
+        const bool more = gh + gridDim.x < n_items;
+        const ChunkPos nxt = more ? chunk_pos(a, gh + gridDim.x) : cur;
+        if (!prep2_chunk(sm, tm, bars, parity, GroupBar{1, kThreads}, tid, cur, loaded, nxt, more, x0, x1, &mQ, &mK,
+                         &mV, a))
+            break;
         parity ^= 1u;
+        cur = nxt;
+        loaded = more;
     }
     tc_fence_before();
     __syncthreads();
@@ -2007,6 +2054,9 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
         prep2_init_tiles(smi, ltid);
         const long n_items = (long)a.n_chunks[1] * n_units;
         uint32_t parity = 0;
+        float x0 = 0.f, x1 = 0.f;
+        // Chunks are taken one at a time, without requesting the next one's tiles early: taking an
+        // item ahead would hold back an early position that a serial pass is waiting for.
         for (;;) {
             if (ltid == 0) item_slot[inst] = atomicAdd(&a.n_chunks[2], 1);
             gb.sync();
@@ -2018,7 +2068,9 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
             const int first = a.chunk_first[nn];
             if (pos >= a.chunk_first[nn + 1] - first) continue;  // this sequence is shorter
             const long gh = (long)(first + pos) * a.H + hh;
-            if (!prep2_chunk(smi, tm + (uint32_t)inst * p2::kTmemCols, bars, parity, gb, ltid, gh, &mQ, &mK, &mV, a))
+            const ChunkPos cur = chunk_pos(a, gh);
+            if (!prep2_chunk(smi, tm + (uint32_t)inst * p2::kTmemCols, bars, parity, gb, ltid, cur, false, cur, false,
+                             x0, x1, &mQ, &mK, &mV, a))
                 break;
             parity ^= 1u;
             __threadfence();
