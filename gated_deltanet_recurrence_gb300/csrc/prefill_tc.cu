@@ -59,13 +59,15 @@ constexpr uint64_t kPolls = 2000000000ull;  // bound on any single mbarrier wait
 struct WsLayout {
     long nch;          // chunk-head slots = max_chunks * H
     size_t off_map, off_first, off_count, off_order, off_W, off_Ut, off_Aqk, off_scal, off_Qt, off_Kt, off_gam,
-        off_ready, total;
+        off_ready, off_Sx, off_Vx, off_oready, total;
+    bool exports;      // room for the fused kernel's exported state
 };
 
 __host__ __device__ inline long max_chunks(int num_seqs, int total_T) { return (long)total_T / kC + num_seqs; }
 
-inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
+inline WsLayout ws_layout(int num_seqs, int total_T, int H, bool exports) {
     WsLayout w{};
+    w.exports = exports;
     const long mc = max_chunks(num_seqs, total_T);
     w.nch = mc * H;
     auto al = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
@@ -82,6 +84,11 @@ inline WsLayout ws_layout(int num_seqs, int total_T, int H) {
     w.off_Kt = o;    o = al(o + sizeof(__nv_bfloat16) * w.nch * kC * kD);   // diag(e^(glast-gc) kinv) K
     w.off_gam = o;   o = al(o + sizeof(float) * w.nch * kD);                // per-channel e^(gc_last)
     w.off_ready = o; o = al(o + sizeof(int32_t) * w.nch);                  // fused kernel: chunk ready flags
+    if (exports) {  // fused kernel, export form: state tile, V_new^T, flag per chunk-head slot
+        w.off_Sx = o;     o = al(o + (size_t)32768 * w.nch);
+        w.off_Vx = o;     o = al(o + (size_t)16384 * w.nch);
+        w.off_oready = o; o = al(o + sizeof(int32_t) * w.nch);
+    }
     w.total = o;
     return w;
 }
@@ -111,6 +118,12 @@ struct TcArgs {
     __nv_bfloat16* Kt;
     float* gam;          // decay per key channel: e^(gc_last) per chunk and channel [nch][128]
     int32_t* ready;      // fused kernel only: per chunk-head slot, 1 once its entries are written
+    // fused kernel with exported state (null otherwise): per chunk-head slot the state at the chunk's
+    // start as the serial pass's bf16 operand tile (32 KB, swizzled as in shared memory), V_new^T
+    // (16 KB, likewise) and a flag set once both are written
+    uint8_t* Sx;
+    uint8_t* Vx;
+    int32_t* oready;
     long nch;            // chunk-head slots of the workspace
     const float* initial_state;
     float* final_state;
@@ -143,6 +156,8 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
     if (tid == 0) longest = 0;
     if (a.ready)  // fused kernel: no chunk is ready yet
         for (long i = tid; i < a.nch; i += 1024) a.ready[i] = 0;
+    if (a.oready)  // export form: no chunk's state is exported yet
+        for (long i = tid; i < a.nch; i += 1024) a.oready[i] = 0;
     // per-thread contiguous block of sequences
     const int per = (a.num_seqs + 1023) / 1024;
     const int s0 = tid * per, s1 = min(a.num_seqs, s0 + per);
@@ -179,6 +194,7 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(TcArgs a) {
         a.n_chunks[0] = part[1023];
         a.n_chunks[1] = longest;  // chunks of the longest sequence
         a.n_chunks[2] = 0;        // fused kernel: work counter of the preparing CTAs
+        a.n_chunks[3] = 0;        // fused kernel with exported state: output work counter
     }
     // the order in which the serial pass starts the sequences: most chunks first, so that the long
     // chains are not the last to begin (ties by index; more than 1024 sequences keep their order)
@@ -1470,6 +1486,149 @@ chunk_prep2_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     }
 }
 
+// Plain bulk copies (16-byte aligned addresses, a multiple of 16 bytes): shared -> global in this
+// thread's bulk group, and global -> shared completing on an mbarrier.
+__device__ __forceinline__ void bulk_store(void* dst_global, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_global),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_global, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst_smem)),
+                 "l"(src_global), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 64 columns of this thread's two rows of an M = 64 accumulator (16x256b shape, 16 repetitions)
+__device__ __forceinline__ void tmem_ld16x256b_x16(uint32_t taddr, uint32_t (&v)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+          "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
+          "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
+          "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+          "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+        : "r"(taddr));
+}
+
+// ---- the gated output of one chunk, shared by the serial pass and the output items ----------------
+//
+// O (M = 64, tokens as rows) comes out of TMEM with a 16x256b load: this thread holds rows
+// rA = 16 q + lane / 4 and rA + 8 and, in every group of 8 columns, the pair cp, cp + 1
+// (cp = 2 (lane % 4)); o[4 j + {0,1}] belong to row rA, o[4 j + {2,3}] to row rA + 8.
+
+// Each row's sum of squares over d_v: the four lanes of a row add their shares with two shuffles.
+__device__ __forceinline__ void out_sumsq(const float* o, float& ssA, float& ssB) {
+    float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        sA0 = fmaf(o[4 * j], o[4 * j], sA0);
+        sA1 = fmaf(o[4 * j + 1], o[4 * j + 1], sA1);
+        sB0 = fmaf(o[4 * j + 2], o[4 * j + 2], sB0);
+        sB1 = fmaf(o[4 * j + 3], o[4 * j + 3], sB1);
+    }
+    ssA = sA0 + sA1;
+    ssB = sB0 + sB1;
+    ssA += __shfl_xor_sync(0xffffffffu, ssA, 1);
+    ssB += __shfl_xor_sync(0xffffffffu, ssB, 1);
+    ssA += __shfl_xor_sync(0xffffffffu, ssA, 2);
+    ssB += __shfl_xor_sync(0xffffffffu, ssB, 2);
+}
+
+// The RMS norm and SiLU gate (when a.z is set; z of the chunk in the 128-byte-swizzled tile zt, four
+// boxes of [64 tokens][32 fp32]) and the stores of the chunk's rows t0 .. t0 + L - 1, by the 128
+// threads of named barrier gbar.  A full chunk with bf16 output is staged in zt as two [64 x 64]
+// boxes (after every row has read its z) and stored by the leader with the output's tensor map (the
+// caller commits nothing further and waits for the store before reusing zt); otherwise the rows
+// inside the sequence are written directly.  Nothing is stored unless ok.
+__device__ __forceinline__ void out_gate_store(float* o, float ssA, float ssB, int rA, int cp, uint8_t* zt, bool ok,
+                                               int L, long t0, int h, bool leader, uint32_t gbar,
+                                               const CUtensorMap* mOut, const TcArgs& a) {
+    const long tok_stride = (long)a.H * a.d;
+    const bool bf16_out = a.out_dtype == GDN_BF16;
+    if (a.z) {
+        // the mean over the head's d_v outputs (the padded columns are zeros)
+        const float rA_inv = rsqrtf(ssA / a.d + a.eps), rB_inv = rsqrtf(ssB / a.d + a.eps);
+        // bf16 output: SiLU with the packed half-precision tanh (error near 1e-3, below the
+        // output's 2^-9 rounding); fp32 output: SiLU at fp32 accuracy.  The choice is taken once,
+        // outside the loop, so that only one of the two is evaluated per element.
+        auto gate = [&](auto silu2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int col = 8 * j + cp, cb = col >> 5, ch = (col & 31) >> 2, sub = (col & 3) * 4;
+                const float2 zA = *reinterpret_cast<const float2*>(zt + cb * 8192 + rA * 128 + ((ch ^ (rA & 7)) << 4) + sub);
+                const float2 zB = *reinterpret_cast<const float2*>(zt + cb * 8192 + (rA + 8) * 128 +
+                                                                   ((ch ^ ((rA + 8) & 7)) << 4) + sub);
+                float2 wA = make_float2(rA_inv, rA_inv), wB = make_float2(rB_inv, rB_inv);
+                if (a.w && col < a.d) {
+                    const float2 wv = __ldg(reinterpret_cast<const float2*>(a.w + col));
+                    wA = make_float2(wv.x * rA_inv, wv.y * rA_inv);
+                    wB = make_float2(wv.x * rB_inv, wv.y * rB_inv);
+                }
+                const float2 sA = silu2(zA), sB = silu2(zB);
+                o[4 * j] *= wA.x * sA.x;
+                o[4 * j + 1] *= wA.y * sA.y;
+                o[4 * j + 2] *= wB.x * sB.x;
+                o[4 * j + 3] *= wB.y * sB.y;
+            }
+        };
+        if (bf16_out)
+            gate([](float2 x) { return fast_silu2(x.x, x.y); });
+        else
+            gate([](float2 x) { return make_float2(x.x * sigmoidf_(x.x), x.y * sigmoidf_(x.y)); });
+    }
+    if (bf16_out && L == kC) {
+        // a full chunk: stage the bf16 rows as two 128-byte-swizzled [64 x 64] boxes in the chunk's
+        // own z buffer (after every row has read its z) and let one thread store them with the
+        // tensor map of the output
+        if (a.z) bar_sync(gbar, 128);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            uint8_t* box = zt + (j >> 3) * 8192;
+            const int cj = j & 7;
+            *reinterpret_cast<uint32_t*>(box + rA * 128 + ((cj ^ (rA & 7)) << 4) + cp * 2) =
+                pack_bf16x2(o[4 * j], o[4 * j + 1]);
+            *reinterpret_cast<uint32_t*>(box + (rA + 8) * 128 + ((cj ^ ((rA + 8) & 7)) << 4) + cp * 2) =
+                pack_bf16x2(o[4 * j + 2], o[4 * j + 3]);
+        }
+        fence_async_smem();
+        bar_sync(gbar, 128);
+        if (leader && ok) {
+            tma_store_3d(mOut, zt, 0, h, (int)t0);
+            if (a.d > 64) tma_store_3d(mOut, zt + 8192, 64, h, (int)t0);
+            bulk_commit();
+        }
+    } else if (ok) {
+        // a partial chunk (the last of its sequence) or an fp32 output: the rows inside the
+        // sequence are written directly, two columns per store
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = rA + 8 * hr;
+            if (r < L) {
+                const long base = (t0 + r) * tok_stride + (long)h * a.d + cp;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    if (8 * j >= a.d) break;
+                    const float x0 = o[4 * j + 2 * hr], x1 = o[4 * j + 2 * hr + 1];
+                    if (bf16_out)
+                        *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + base + 8 * j) =
+                            pack_bf16x2(x0, x1);
+                    else
+                        *reinterpret_cast<float2*>(static_cast<float*>(a.out) + base + 8 * j) = make_float2(x0, x1);
+                }
+            }
+        }
+    }
+}
+
 // ---- 3. serial state pass ------------------------------------------------------------------------
 
 namespace st {
@@ -1496,7 +1655,11 @@ constexpr uint32_t kSmem = kBytes + 1024;
 static_assert(kSmem <= 232448, "state kernel shared memory exceeds the per-block limit");
 constexpr uint32_t kStageTx = 32768 + 16384 + 8192;
 // barriers
-enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF, DA1, A12, SFULL, DO_0, DO_1, DOE_0, DOE_1, ZFULL0, ZFULL1, NBAR };
+enum { FULL0 = 0, FULL1, EMPTY0, EMPTY1, SBF, DA1, A12, SFULL, DO_0, DO_1, DOE_0, DOE_1, ZFULL0, ZFULL1, SCP, VCP, NBAR };
+static_assert(8 * NBAR + 8 <= 256, "barrier block");
+// export form: the stage holds W, K~ and U^T (two boxes of 64 rows where the combined form keeps Q~),
+// and the chunk's decay gamma in a slot of the oGam row
+constexpr uint32_t kStageTxExport = 16384 + 16384 + 16384;
 constexpr uint32_t kTmemCols = 512;
 }  // namespace st
 
@@ -1508,10 +1671,16 @@ constexpr uint32_t kTmemCols = 512;
 // epilogue's read-only-path loads (__ldg) of those entries stay correct there: every entry is
 // first touched after its flag is acquired, each chunk's entries fill whole aligned slots (no
 // cache line holds two chunks), and the SM runs no other CTA, so no stale line can be cached.
+//
+// With a.Sx set (export form, fused kernel only) the serial pass forms no output: per chunk it copies
+// the state's operand tile and V_new^T to the workspace (warp 2, bulk copies) and flags them, and the
+// output of the chunk is formed elsewhere (out_chunk).  The chain then waits, before rewriting either
+// tile, for the copy to have read it (normally long done).
 template <bool PC>
 __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensorMap* mQt, const CUtensorMap* mKt,
                                            const CUtensorMap* mW, const CUtensorMap* mAqk,
-                                           const CUtensorMap* mZ, const CUtensorMap* mOut, const TcArgs& a) {
+                                           const CUtensorMap* mZ, const CUtensorMap* mOut, const CUtensorMap* mUt,
+                                           const TcArgs& a) {
     using namespace st;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tbase = reinterpret_cast<uint32_t*>(sm + oBar + 8 * NBAR);
@@ -1523,6 +1692,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
     if (!seq_bounds(a, n, bos, eos)) return;  // reported by the chunk map kernel
     const int nck = (int)((eos - bos + kC - 1) / kC);
     const int first = a.chunk_first[n];
+    const bool exp = a.Sx != nullptr;
 
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
@@ -1561,13 +1731,20 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 }
                 uint8_t* sp = stage_ptr(s);
                 const int row = (int)(ghc * kC);
-                mbar_arrive_expect_tx(&bars[FULL0 + s], kStageTx);
+                // export form: gamma into its slot before the arrive that releases it with the stage
+                if (exp) reinterpret_cast<float*>(sm + oGam)[s] = __ldg(a.scal + ghc * 4 * kC + 3 * kC);
+                mbar_arrive_expect_tx(&bars[FULL0 + s], exp ? kStageTxExport : kStageTx);
                 for (int ac = 0; ac < 2; ++ac) {
                     tma_load_2d(sp + sWQ + ac * 16384, mW, &bars[FULL0 + s], ac * 64, row);
-                    tma_load_2d(sp + sWQ + ac * 16384 + 8192, mQt, &bars[FULL0 + s], ac * 64, row);
+                    if (!exp) tma_load_2d(sp + sWQ + ac * 16384 + 8192, mQt, &bars[FULL0 + s], ac * 64, row);
                     tma_load_2d(sp + sK + ac * 8192, mKt, &bars[FULL0 + s], ac * 64, row);
                 }
-                tma_load_2d(sp + sAqk, mAqk, &bars[FULL0 + s], 0, row);
+                if (!exp) {
+                    tma_load_2d(sp + sAqk, mAqk, &bars[FULL0 + s], 0, row);
+                } else {  // U^T rows 0-63 and 64-127, and gamma, for the chain epilogue
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_2d(sp + sWQ + bx * 16384 + 8192, mUt, &bars[FULL0 + s], 0, (int)(ghc * kD) + 64 * bx);
+                }
             }
             // drain: wait until the last issued stages have landed before the CTA may exit
             for (int c = max(0, nck - 2); c < nck; ++c) mbar_wait(&bars[FULL0 + (c & 1)], (c >> 1) & 1, kPolls);
@@ -1601,12 +1778,14 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 mma_commit(&bars[DA1]);
                 // while the state epilogue forms V_new: O = Q~ S^T (tokens as rows, M = 64), once the
                 // output group has taken chunk c - 2's O out of this buffer
-                if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
-                tc_fence_after();
+                if (!exp) {
+                    if (c >= 2 && !mbar_wait(&bars[DOE_0 + b], ((c >> 1) - 1) & 1, kPolls)) { fail(); break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-                    mma_bf16_ss(tDO, dSt + (sWQ + 8192) / 16 + off, dS + off, kIdO, k > 0);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint64_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+                        mma_bf16_ss(tDO, dSt + (sWQ + 8192) / 16 + off, dS + off, kIdO, k > 0);
+                    }
                 }
                 if (!mbar_wait(&bars[A12], c & 1, kPolls)) { fail(); break; }
                 tc_fence_after();
@@ -1615,13 +1794,46 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 for (int k = 0; k < 4; ++k) mma_bf16_ss(tS, dA1 + k * 2, dK + k * 128, kIdS, 1);
                 mma_commit(&bars[SFULL]);
                 // O += Aqk V_new   (B = V_new^T rows, K-major)
+                if (!exp) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) mma_bf16_ss(tDO, dSt + sAqk / 16 + k * 2, dA1 + k * 2, kIdO, 1);
-                mma_commit(&bars[DO_0 + b]);
+                    for (int k = 0; k < 4; ++k) mma_bf16_ss(tDO, dSt + sAqk / 16 + k * 2, dA1 + k * 2, kIdO, 1);
+                    mma_commit(&bars[DO_0 + b]);
+                }
                 mma_commit(&bars[EMPTY0 + s]);
             }
         }
-    }  // warps 2-3: idle
+    } else if (warp == 2) {
+        // ================= export (export form only) =================
+        // Per chunk c: the state's operand tile once the chain has signalled it (SBF), V_new^T once
+        // it has (A12), each to the chunk's workspace slot.  Each tile is released to the chain as
+        // soon as its own copy has read it; chunk c's flag is released once both of its copies are
+        // written, checked after the next chunk's first copy is issued (at most one group newer).
+        if (exp && lane == 0) {
+            for (int c = 0; c < nck; ++c) {
+                const long gh = (long)(first + c) * a.H + h;
+                if (!mbar_wait(&bars[SBF], c & 1, kPolls)) { fail(); break; }
+                bulk_store(a.Sx + gh * 32768, sm + oS, 32768);
+                bulk_commit();
+                bulk_wait_read();
+                mbar_arrive(&bars[SCP]);
+                if (c >= 1) {  // chunk c - 1's two copies are all but the newest group
+                    asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+                    fence_proxy_async_global();
+                    st_release_gpu(a.oready + gh - a.H, 1);
+                }
+                if (!mbar_wait(&bars[A12], c & 1, kPolls)) { fail(); break; }
+                bulk_store(a.Vx + gh * 16384, sm + oA1, 16384);
+                bulk_commit();
+                bulk_wait_read();
+                mbar_arrive(&bars[VCP]);
+            }
+            bulk_wait_all();
+            if (nck > 0 && !*abort_flag) {
+                fence_proxy_async_global();
+                st_release_gpu(a.oready + (long)(first + nck - 1) * a.H + h, 1);
+            }
+        }
+    }  // warp 3: idle
     } else if (warp < 8) {
     reg_alloc<kRegsHigh>();
     {
@@ -1683,7 +1895,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             }
         }
         uint4 up_next[8];
-        if (nck > 0 && !*abort_flag) {
+        if (nck > 0 && !*abort_flag && !exp) {
             const uint4* src = reinterpret_cast<const uint4*>(a.Ut + ((long)first * a.H + h) * kD * kC + (long)r * kC);
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) up_next[c8] = __ldg(src + c8);
@@ -1697,10 +1909,11 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             uint4 up[8];
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) up[c8] = up_next[c8];
-            // the next chunk's entries (a failed wait skips them; the group leaves at its next barrier)
-            const bool nready = !last && (!a.ready || wait_ready(a.ready + gh + a.H));
-            if (!last && !nready) fail();
-            const float gnext = (!nready || PC) ? 1.0f : __ldg(a.scal + (gh + a.H) * 4 * kC + 3 * kC);
+            // the next chunk's entries (a failed wait skips them; the group leaves at its next barrier);
+            // the export form takes them from the stages instead, off the chain
+            const bool nready = !last && !exp && (!a.ready || wait_ready(a.ready + gh + a.H));
+            if (!last && !exp && !nready) fail();
+            float gnext = (!nready || PC) ? 1.0f : __ldg(a.scal + (gh + a.H) * 4 * kC + 3 * kC);
             float* gvec = reinterpret_cast<float*>(sm + oGam) + ((c + 1) & 1) * kD;
             if (PC && nready) gvec[r] = __ldg(a.gam + (gh + a.H) * kD + r);  // read after the next group barrier
             if (nready) {
@@ -1714,6 +1927,17 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             if (!ok) fail();
             tc_fence_after();
             // ---- V_new^T row r = U^T row r - (S W^T) row r ----
+            if (exp && c >= 1 && ok) {  // the previous chunk's V_new^T has been copied out
+                ok = mbar_wait(&bars[VCP], (c - 1) & 1, kPolls);
+                if (!ok) fail();
+            }
+            if (ok && exp) {  // U^T row r from this chunk's stage (its phase completes before the MMAs ran)
+                ok = mbar_wait(&bars[FULL0 + (c & 1)], (c >> 1) & 1, kPolls);
+                if (!ok) fail();
+                const uint8_t* ub = stage_ptr(c & 1) + sWQ + (r >> 6) * 16384 + 8192;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) up[c8] = *reinterpret_cast<const uint4*>(ub + sw128_offset(r & 63, c8 * 8));
+            }
             if (ok) {
                 uint32_t v[2][32];
                 tmem_ld32(tDA0 + b * 64 + lrow, v[0]);
@@ -1765,6 +1989,10 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                     }
                 }
             } else {
+                if (exp && ok) {  // this chunk's state tile has been copied out
+                    ok = mbar_wait(&bars[SCP], c & 1, kPolls);
+                    if (!ok) fail();
+                }
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
@@ -1778,6 +2006,11 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
                 tc_fence_before();
                 if (bar_sync_or(1, 128, *abort_flag != 0)) break;
                 if (r == 0) mbar_arrive(&bars[SBF]);
+                if (exp) {  // the next chunk's gamma, from its stage slot once the stage has landed
+                    const int sn = (c + 1) & 1;
+                    if (!mbar_wait(&bars[FULL0 + sn], ((c + 1) >> 1) & 1, kPolls)) fail();
+                    gnext = reinterpret_cast<const float*>(sm + oGam)[sn];
+                }
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
@@ -1793,7 +2026,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
     }
     } else {
     reg_dealloc<kRegsOut>();
-    {
+    if (!exp) {  // the export form leaves the output to out_chunk
         // ================= output epilogue (O and the gate) =================
         // Two groups of four warps take alternate chunks (group 0: warps 8-11, even chunks; group 1:
         // warps 12-15, odd chunks), each with its own O buffer, z buffer and named barrier, so a
@@ -1807,9 +2040,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
         const int cp = 2 * (lane & 3);
         const uint32_t lrow = static_cast<uint32_t>(q4 * 32) << 16;
         const uint32_t gbar = 4u + (uint32_t)og;
-        const long tok_stride = (long)a.H * a.d;
         const bool leader = (q4 == 0 && lane == 0);
-        const bool bf16_out = a.out_dtype == GDN_BF16;
         // z of chunk c goes to buffer c & 1 (this group's); it is requested two chunks ahead
         auto issue_z = [&](int cz) {
             const int t0z = (int)(bos + (long)cz * kC);
@@ -1829,118 +2060,23 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
             tc_fence_after();
             uint32_t v[64];
             if (ok) {
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.16x256b.x16.b32 "
-                    "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-                    "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-                    "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-                    "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-                      "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-                      "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
-                      "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]),
-                      "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]),
-                      "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
-                      "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
-                    : "r"(tDO0 + b * 128 + lrow));
+                tmem_ld16x256b_x16(tDO0 + b * 128 + lrow, v);
                 tmem_wait_ld();
             } else {
 #pragma unroll
                 for (int e = 0; e < 64; ++e) v[e] = 0u;
             }
             float* o = reinterpret_cast<float*>(v);   // o[4 j + {0,1}]: row rA, o[4 j + {2,3}]: row rA + 8
-            float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                sA0 = fmaf(o[4 * j], o[4 * j], sA0);
-                sA1 = fmaf(o[4 * j + 1], o[4 * j + 1], sA1);
-                sB0 = fmaf(o[4 * j + 2], o[4 * j + 2], sB0);
-                sB1 = fmaf(o[4 * j + 3], o[4 * j + 3], sB1);
-            }
-            float ssA = sA0 + sA1, ssB = sB0 + sB1;
-            ssA += __shfl_xor_sync(0xffffffffu, ssA, 1);
-            ssB += __shfl_xor_sync(0xffffffffu, ssB, 1);
-            ssA += __shfl_xor_sync(0xffffffffu, ssA, 2);
-            ssB += __shfl_xor_sync(0xffffffffu, ssB, 2);
+            float ssA, ssB;
+            out_sumsq(o, ssA, ssB);
             tc_fence_before();
             if (bar_sync_or(gbar, 128, *abort_flag != 0)) break;
             if (leader) mbar_arrive(&bars[DOE_0 + b]);
             if (a.z) {
                 ok = mbar_wait(&bars[ZFULL0 + b], (c >> 1) & 1, kPolls);
                 if (!ok) fail();
-                // the mean over the head's d_v outputs (the padded columns are zeros)
-                const float rA_inv = rsqrtf(ssA / a.d + a.eps), rB_inv = rsqrtf(ssB / a.d + a.eps);
-                // bf16 output: SiLU with the packed half-precision tanh (error near 1e-3, below the
-                // output's 2^-9 rounding); fp32 output: SiLU at fp32 accuracy.  The choice is taken
-                // once, outside the loop, so that only one of the two is evaluated per element.
-                auto gate = [&](auto silu2) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = 8 * j + cp, cb = col >> 5, ch = (col & 31) >> 2, sub = (col & 3) * 4;
-                        const float2 zA = *reinterpret_cast<const float2*>(zt + cb * 8192 + rA * 128 + ((ch ^ (rA & 7)) << 4) + sub);
-                        const float2 zB = *reinterpret_cast<const float2*>(zt + cb * 8192 + (rA + 8) * 128 +
-                                                                           ((ch ^ ((rA + 8) & 7)) << 4) + sub);
-                        float2 wA = make_float2(rA_inv, rA_inv), wB = make_float2(rB_inv, rB_inv);
-                        if (a.w && col < a.d) {
-                            const float2 wv = __ldg(reinterpret_cast<const float2*>(a.w + col));
-                            wA = make_float2(wv.x * rA_inv, wv.y * rA_inv);
-                            wB = make_float2(wv.x * rB_inv, wv.y * rB_inv);
-                        }
-                        const float2 sA = silu2(zA), sB = silu2(zB);
-                        o[4 * j] *= wA.x * sA.x;
-                        o[4 * j + 1] *= wA.y * sA.y;
-                        o[4 * j + 2] *= wB.x * sB.x;
-                        o[4 * j + 3] *= wB.y * sB.y;
-                    }
-                };
-                if (bf16_out)
-                    gate([](float2 x) { return fast_silu2(x.x, x.y); });
-                else
-                    gate([](float2 x) { return make_float2(x.x * sigmoidf_(x.x), x.y * sigmoidf_(x.y)); });
             }
-            if (bf16_out && L == kC) {
-                // a full chunk: stage the bf16 rows as two 128-byte-swizzled [64 x 64] boxes in the
-                // chunk's own z buffer (after every row has read its z) and let one thread store
-                // them with the tensor map of the output
-                if (a.z) bar_sync(gbar, 128);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    uint8_t* box = zt + (j >> 3) * 8192;
-                    const int cj = j & 7;
-                    *reinterpret_cast<uint32_t*>(box + rA * 128 + ((cj ^ (rA & 7)) << 4) + cp * 2) =
-                        pack_bf16x2(o[4 * j], o[4 * j + 1]);
-                    *reinterpret_cast<uint32_t*>(box + (rA + 8) * 128 + ((cj ^ ((rA + 8) & 7)) << 4) + cp * 2) =
-                        pack_bf16x2(o[4 * j + 2], o[4 * j + 3]);
-                }
-                fence_async_smem();
-                bar_sync(gbar, 128);
-                if (leader && ok) {
-                    tma_store_3d(mOut, zt, 0, h, (int)t0);
-                    if (a.d > 64) tma_store_3d(mOut, zt + 8192, 64, h, (int)t0);
-                    bulk_commit();
-                }
-            } else if (ok) {
-                // a partial chunk (the last of its sequence) or an fp32 output: the rows inside the
-                // sequence are written directly, two columns per store
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int r = rA + 8 * hr;
-                    if (r < L) {
-                        const long base = (t0 + r) * tok_stride + (long)h * a.d + cp;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if (8 * j >= a.d) break;
-                            const float x0 = o[4 * j + 2 * hr], x1 = o[4 * j + 2 * hr + 1];
-                            if (bf16_out)
-                                *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + base + 8 * j) =
-                                    pack_bf16x2(x0, x1);
-                            else
-                                *reinterpret_cast<float2*>(static_cast<float*>(a.out) + base + 8 * j) = make_float2(x0, x1);
-                        }
-                    }
-                }
-            }
+            out_gate_store(o, ssA, ssB, rA, cp, zt, ok, L, t0, h, leader, gbar, mOut, a);
             // every row has read its z and written its output: the buffers may be reused once the
             // tensor store issued from the z buffer has read it
             if (bar_sync_or(gbar, 128, *abort_flag != 0)) break;
@@ -1975,9 +2111,169 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
     // keeps the shared address space (plain shared loads and stores, not generic ones)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int unit = a.seq_order[blockIdx.x / a.H] * a.H + blockIdx.x % a.H;  // longest sequences first
-    state_unit<PC>(sm, unit, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, a);
+    state_unit<PC>(sm, unit, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mW, a);  // no export: mUt unused
 }
 
+
+// ---- 3b. the outputs from the exported state (fused kernel, export form) -------------------------
+//
+// O = Q~ S^T + Aqk V_new for every chunk, then the gate and the stores, by each preparing CTA once its
+// preparations are done, after the serial pass has exported the chunk's state tile and V_new^T
+// (workspace flag).  The products are the serial pass's own (same operands, same order) and the
+// epilogue is the same function, so both forms give the same bits.  The CTA's 16 warps form a
+// pipeline over two item buffers (tiles) and two TMEM accumulators: warp 0 lane 0 takes items
+// position by position and loads them, warp 1 lane 0 issues the products, warps 8-11 and 12-15 take
+// alternate items through the gate and the stores.
+namespace oc {
+constexpr uint32_t oS = 0, oV = 32768, oQ = 49152, oA = 65536, oZ = 73728;  // within one item buffer
+constexpr uint32_t kBuf = oZ + 32768;
+constexpr uint32_t kTx = 32768 + 16384 + 16384 + 8192;
+enum { FULL0 = 0, FULL1, ZF0, ZF1, OF0, OF1, OE0, OE1, EMPTY0, EMPTY1, NBAR };
+struct Slot {  // the item in a buffer: chunk-head pair (-1: no more), first token, tokens, head
+    long gh, t0;
+    int L, h;
+};
+constexpr uint32_t kEngBytes = 8 * NBAR + 2 * sizeof(Slot);  // barriers, then the two buffers' items
+}  // namespace oc
+
+// All 512 threads of a preparing CTA; `eng` holds the engine's barriers and item slots, `tm` the
+// CTA's 256 TMEM columns.  The preparing CTAs take the items in turn (CTA e of E takes items e,
+// e + E, ...; items are position-major).  The producer waits for an item's flags before it waits
+// for a free buffer, so that the two latencies overlap.  It marks the slot after the last item, and
+// the one after that, with -1, which ends the MMA thread and both epilogue groups.  Waits are
+// bounded; a timeout is recorded and ends the role.
+__device__ __forceinline__ void out_engine(uint8_t* sm, uint8_t* eng, uint32_t tm, int n_units, int e, int E,
+                                           const CUtensorMap* mQt, const CUtensorMap* mAqk, const CUtensorMap* mZ,
+                                           const CUtensorMap* mOut, const TcArgs& a) {
+    using namespace oc;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(eng);
+    volatile Slot* ring = reinterpret_cast<volatile Slot*>(eng + 8 * NBAR);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long n_items = (long)a.n_chunks[1] * n_units;
+    if (tid == 0) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) {  // ---- producer ----
+            long k = 0, j = e;
+            bool ok = true;
+            for (;; ++k) {
+                const int b = (int)(k & 1);
+                uint8_t* buf = sm + b * kBuf;
+                // the next item whose sequence reaches its position, and where it lies
+                Slot sl{-1, 0, 0, 0};
+                for (; j < n_items; j += E) {
+                    const int pos = (int)(j / n_units), unit = (int)(j % n_units);
+                    const int nn = unit / a.H;
+                    const int first = a.chunk_first[nn];
+                    if (pos < a.chunk_first[nn + 1] - first) {
+                        long bos, eos;
+                        seq_bounds(a, nn, bos, eos);
+                        sl.gh = (long)(first + pos) * a.H + unit % a.H;
+                        sl.t0 = bos + (long)pos * kC;
+                        sl.L = (eos - sl.t0 < kC) ? (int)(eos - sl.t0) : kC;
+                        sl.h = unit % a.H;
+                        j += E;
+                        break;
+                    }
+                }
+                if (sl.gh >= 0 && (!wait_ready(a.ready + sl.gh) || !wait_ready(a.oready + sl.gh))) { ok = false; break; }
+                if (k >= 2 && !mbar_wait(&bars[EMPTY0 + b], ((k >> 1) - 1) & 1, kPolls)) { ok = false; break; }
+                ring[b].gh = sl.gh;
+                ring[b].t0 = sl.t0;
+                ring[b].L = sl.L;
+                ring[b].h = sl.h;
+                if (sl.gh < 0) {
+                    mbar_arrive(&bars[FULL0 + b]);
+                    break;
+                }
+                fence_proxy_async_global();  // the entries and exports were written before their flags
+                if (a.z) {
+                    mbar_arrive_expect_tx(&bars[ZF0 + b], 32768);
+                    for (int cb = 0; cb < 4; ++cb) tma_load_3d(buf + oZ + cb * 8192, mZ, &bars[ZF0 + b], cb * 32, sl.h, (int)sl.t0);
+                }
+                mbar_arrive_expect_tx(&bars[FULL0 + b], kTx);
+                const int row = (int)(sl.gh * kC);
+                for (int ac = 0; ac < 2; ++ac) tma_load_2d(buf + oQ + ac * 8192, mQt, &bars[FULL0 + b], ac * 64, row);
+                tma_load_2d(buf + oA, mAqk, &bars[FULL0 + b], 0, row);
+                bulk_load(buf + oS, a.Sx + sl.gh * 32768, 32768, &bars[FULL0 + b]);
+                bulk_load(buf + oV, a.Vx + sl.gh * 16384, 16384, &bars[FULL0 + b]);
+            }
+            if (ok) {  // the slot after the last: its previous item must be done first
+                const int b = (int)((k + 1) & 1);
+                if (k >= 1 && !mbar_wait(&bars[EMPTY0 + b], ((k - 1) >> 1) & 1, kPolls)) ok = false;
+                ring[b].gh = -1;
+                mbar_arrive(&bars[FULL0 + b]);
+            }
+            if (!ok) record_error(a.err, GDN_ERR_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ---- products: O (tokens as rows, M = 64) = Q~ S^T + Aqk V_new ----
+            constexpr uint32_t kIdO = idesc_bf16(64, 128, 0, 0);
+            int ends = 0;
+            for (long k = 0; ends < 2; ++k) {
+                const int b = (int)(k & 1);
+                if (!mbar_wait(&bars[FULL0 + b], (k >> 1) & 1, kPolls)) { record_error(a.err, GDN_ERR_TIMEOUT); break; }
+                if (ring[b].gh < 0) {
+                    ++ends;
+                    continue;
+                }
+                if (k >= 2 && !mbar_wait(&bars[OE0 + b], ((k >> 1) - 1) & 1, kPolls)) {
+                    record_error(a.err, GDN_ERR_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                uint8_t* buf = sm + b * kBuf;
+                const uint64_t dS = sdesc_sw128(smem_u32(buf + oS), 16, 1024);
+                const uint64_t dV = sdesc_sw128(smem_u32(buf + oV), 16, 1024);
+                const uint64_t dQ = sdesc_sw128(smem_u32(buf + oQ), 16, 1024);
+                const uint64_t dA = sdesc_sw128(smem_u32(buf + oA), 16, 1024);
+                const uint32_t tO = tm + (uint32_t)b * 128;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ss(tO, dQ + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+                                dS + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), kIdO, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(tO, dA + kk * 2, dV + kk * 2, kIdO, 1);
+                mma_commit(&bars[OF0 + b]);
+            }
+        }
+    } else if (warp >= 8) {  // ---- epilogue groups: group g takes the items k = g, g + 2, ... ----
+        const int g = (warp - 8) >> 2, q4 = warp & 3;
+        const int rA = q4 * 16 + (lane >> 2), cp = 2 * (lane & 3);
+        const bool leader = q4 == 0 && lane == 0;
+        const uint32_t ebar = 5u + (uint32_t)g;
+        uint8_t* buf = sm + g * kBuf;
+        for (long k = g;; k += 2) {
+            bool ok = mbar_wait(&bars[FULL0 + g], (k >> 1) & 1, kPolls);
+            const long gh = ok ? ring[g].gh : -1;
+            if (!ok) record_error(a.err, GDN_ERR_TIMEOUT);
+            if (gh < 0) break;
+            const long t0 = ring[g].t0;
+            const int L = ring[g].L, h = ring[g].h;
+            ok = mbar_wait(&bars[OF0 + g], (k >> 1) & 1, kPolls);
+            tc_fence_after();
+            uint32_t v[64];
+            tmem_ld16x256b_x16(tm + (uint32_t)g * 128 + (static_cast<uint32_t>(q4 * 32) << 16), v);  // in bounds
+            tmem_wait_ld();
+            tc_fence_before();
+            bar_sync(ebar, 128);
+            if (leader) mbar_arrive(&bars[OE0 + g]);  // O is out of TMEM: the accumulator may take item k + 2
+            float* o = reinterpret_cast<float*>(v);
+            float ssA, ssB;
+            out_sumsq(o, ssA, ssB);
+            if (a.z) ok = mbar_wait(&bars[ZF0 + g], (k >> 1) & 1, kPolls) && ok;
+            if (!ok) record_error(a.err, GDN_ERR_TIMEOUT);
+            out_gate_store(o, ssA, ssB, rA, cp, buf + oZ, ok, L, t0, h, leader, ebar, mOut, a);
+            if (leader) bulk_wait_read();  // the staged rows have left the buffer
+            bar_sync(ebar, 128);           // every row has read its z
+            if (leader) mbar_arrive(&bars[EMPTY0 + g]);
+        }
+        if (leader) bulk_wait_all();  // output stores complete before the CTA exits
+    }
+}
 
 // ---- 4. fused preparation + serial pass (few units) ----------------------------------------------
 //
@@ -2001,7 +2297,9 @@ constexpr uint32_t kPrepBytes = oItem + 8 * kInst;
 constexpr uint32_t kPrepStride2 = (p2::kBytes + 1023u) & ~1023u;
 constexpr uint32_t oTmemBase2 = 2 * kPrepStride2;
 constexpr uint32_t oItem2 = oTmemBase2 + 16;
-constexpr uint32_t kPrepBytes2 = oItem2 + 16;
+constexpr uint32_t oEng = oItem2 + 16;            // export form: the output engine's barriers and items
+constexpr uint32_t kPrepBytes2 = oEng + oc::kEngBytes;
+static_assert(2 * oc::kBuf <= oTmemBase2, "the output engine's buffers within the preparations' regions");
 constexpr uint32_t kPrepMax = kPrepBytes > kPrepBytes2 ? kPrepBytes : kPrepBytes2;
 constexpr uint32_t kSmem = st::kSmem > kPrepMax + 1024 ? st::kSmem : kPrepMax + 1024;
 static_assert(kSmem <= 232448, "fused kernel shared memory exceeds the per-block limit");
@@ -2018,11 +2316,12 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mQt,
                    const __grid_constant__ CUtensorMap mKt, const __grid_constant__ CUtensorMap mW,
                    const __grid_constant__ CUtensorMap mAqk, const __grid_constant__ CUtensorMap mZ,
-                   const __grid_constant__ CUtensorMap mOut, TcArgs a, int n_units) {
+                   const __grid_constant__ CUtensorMap mOut, const __grid_constant__ CUtensorMap mUt, TcArgs a,
+                   int n_units) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     if ((int)blockIdx.x < n_units) {
-        state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, a);
+        state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mUt, a);
         return;
     }
     using namespace fz;
@@ -2079,6 +2378,13 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 fence_proxy_async_global();
                 st_release_gpu(a.ready + gh, 1);
             }
+        }
+        if (a.Sx) {  // export form: then the chunks' outputs, by the whole CTA
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            out_engine(sm, sm + oEng, tm, n_units, (int)blockIdx.x - n_units, (int)gridDim.x - n_units, &mQt, &mAqk,
+                       &mZ, &mOut, a);
         }
         tc_fence_before();
         __syncthreads();
@@ -2196,8 +2502,20 @@ bool map_rows(CUtensorMap* m, const void* base, long rows, int cols, int box_row
 
 }  // namespace
 
+// Whether a call with this many (sequence, head) units may take the fused kernel on the current
+// device (the kernel-form setting can only narrow it), and so needs room for its exported state.
+bool fused_possible(long units) {
+    int dev = 0, sms = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return coop && units <= sms - 1;
+}
+
 size_t prefill_tc_workspace_bytes(int num_seqs, int total_T, int H) {
-    return ws_layout(num_seqs, total_T, H).total;
+    return ws_layout(num_seqs, total_T, H, fused_possible((long)num_seqs * H)).total;
 }
 
 bool prefill_tc_supported(const PrefillArgs& a) {
@@ -2205,7 +2523,7 @@ bool prefill_tc_supported(const PrefillArgs& a) {
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
-    const WsLayout L = ws_layout(p.num_seqs, p.total_T, p.H);
+    const WsLayout L = ws_layout(p.num_seqs, p.total_T, p.H, fused_possible((long)p.num_seqs * p.H));
     uint8_t* ws = static_cast<uint8_t*>(p.workspace);
     TcArgs a{};
     a.cu = p.cu_seqlens; a.num_seqs = p.num_seqs; a.total_T = p.total_T; a.H = p.H; a.Hk = p.Hk; a.d = p.d;
@@ -2228,10 +2546,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     a.initial_state = p.initial_state; a.final_state = p.final_state;
     a.z = p.z; a.w = p.w; a.eps = p.eps; a.out = p.out; a.out_dtype = p.out_dtype; a.err = p.err;
 
-    CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ, mOut;
+    CUtensorMap mQ, mK, mV, mW, mAqk, mQt, mKt, mZ, mOut, mUt;
     if (!map_tokens(&mQ, p.q, p.total_T, p.Hk, p.d) || !map_tokens(&mK, p.k, p.total_T, p.Hk, p.d) ||
         !map_tokens(&mV, p.v, p.total_T, p.H, p.d) || !map_rows(&mW, a.W, L.nch * kC, kD, 64) ||
         !map_rows(&mAqk, a.Aqk, L.nch * kC, kC, 64) || !map_rows(&mQt, a.Qt, L.nch * kC, kD, 64) ||
+        !map_rows(&mUt, a.Ut, L.nch * kD, kC, 64) ||
         !map_rows(&mKt, a.Kt, L.nch * kC, kD, 64))
         return cudaErrorInvalidValue;
     if (p.z) {
@@ -2264,12 +2583,21 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     }
     a.nch = L.nch;
     a.ready = fused ? reinterpret_cast<int32_t*>(ws + L.off_ready) : nullptr;
+    // decay per head, no fused convolution: the fused kernel's serial passes export the state and
+    // the preparing CTAs form the outputs.  (With the convolution the preparations are heavier and
+    // the preparing CTAs would take longer than the serial passes; a decay per key channel keeps
+    // the four-warp preparations.)
+    if (fused && L.exports && !p.g_per_channel && !p.conv.w) {
+        a.Sx = ws + L.off_Sx;
+        a.Vx = ws + L.off_Vx;
+        a.oready = reinterpret_cast<int32_t*>(ws + L.off_oready);
+    }
 
     chunk_map_kernel<<<1, 1024, 0, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (fused) {  // one CTA per SM, all resident (cooperative launch)
-        void* args[] = {&mQ, &mK, &mV, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &a, &units};
+        void* args[] = {&mQ, &mK, &mV, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mUt, &a, &units};
         return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_fn), dim3((unsigned)sms),
                                            dim3(st::kThreads), args, fz::kSmem, s);
     }
