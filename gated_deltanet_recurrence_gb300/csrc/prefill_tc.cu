@@ -1672,11 +1672,11 @@ constexpr uint32_t kTmemCols = 512;
 // first touched after its flag is acquired, each chunk's entries fill whole aligned slots (no
 // cache line holds two chunks), and the SM runs no other CTA, so no stale line can be cached.
 //
-// With a.Sx set (export form, fused kernel only) the serial pass forms no output: per chunk it copies
+// With EXP (export form, fused kernel only, a.Sx set) the serial pass forms no output: per chunk it copies
 // the state's operand tile and V_new^T to the workspace (warp 2, bulk copies) and flags them, and the
 // output of the chunk is formed elsewhere (out_chunk).  The chain then waits, before rewriting either
 // tile, for the copy to have read it (normally long done).
-template <bool PC>
+template <bool PC, bool EXP>
 __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensorMap* mQt, const CUtensorMap* mKt,
                                            const CUtensorMap* mW, const CUtensorMap* mAqk,
                                            const CUtensorMap* mZ, const CUtensorMap* mOut, const CUtensorMap* mUt,
@@ -1692,7 +1692,7 @@ __device__ __forceinline__ void state_unit(uint8_t* sm, int unit, const CUtensor
     if (!seq_bounds(a, n, bos, eos)) return;  // reported by the chunk map kernel
     const int nck = (int)((eos - bos + kC - 1) / kC);
     const int first = a.chunk_first[n];
-    const bool exp = a.Sx != nullptr;
+    constexpr bool exp = EXP;
 
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
@@ -2111,7 +2111,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
     // keeps the shared address space (plain shared loads and stores, not generic ones)
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     const int unit = a.seq_order[blockIdx.x / a.H] * a.H + blockIdx.x % a.H;  // longest sequences first
-    state_unit<PC>(sm, unit, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mW, a);  // no export: mUt unused
+    state_unit<PC, false>(sm, unit, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mW, a);  // no export: mUt unused
 }
 
 
@@ -2310,7 +2310,7 @@ static_assert(kInst * 128 * kRegsPrep + (4 - kInst) * 128 * kRegsIdle <= st::kTh
               "register split above the launch total");
 }  // namespace fz
 
-template <bool PC>
+template <bool PC, bool EXP>
 __global__ void __launch_bounds__(st::kThreads, 1)
 chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mQt,
@@ -2321,7 +2321,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = smraw + ((1024u - (smem_u32(smraw) & 1023u)) & 1023u);
     if ((int)blockIdx.x < n_units) {
-        state_unit<PC>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mUt, a);
+        state_unit<PC, EXP>(sm, blockIdx.x, &mQt, &mKt, &mW, &mAqk, &mZ, &mOut, &mUt, a);
         return;
     }
     using namespace fz;
@@ -2379,7 +2379,7 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 st_release_gpu(a.ready + gh, 1);
             }
         }
-        if (a.Sx) {  // export form: then the chunks' outputs, by the whole CTA
+        if constexpr (EXP) {  // export form: then the chunks' outputs, by the whole CTA
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
@@ -2567,7 +2567,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     // the fused cooperative kernel serves calls with few (sequence, head) units: at most half the SMs
     // run serial passes, the rest prepare chunks; gdn_set_kernel_forms can turn it off
     int units = p.num_seqs * p.H, sms = 0, coop = 0, dev = 0, resident = 0;
-    auto fused_fn = p.g_per_channel ? chunk_fused_kernel<true> : chunk_fused_kernel<false>;
+    auto fused_fn = p.g_per_channel ? chunk_fused_kernel<true, false> : chunk_fused_kernel<false, false>;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -2583,14 +2583,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     }
     a.nch = L.nch;
     a.ready = fused ? reinterpret_cast<int32_t*>(ws + L.off_ready) : nullptr;
-    // decay per head, no fused convolution: the fused kernel's serial passes export the state and
-    // the preparing CTAs form the outputs.  (With the convolution the preparations are heavier and
-    // the preparing CTAs would take longer than the serial passes; a decay per key channel keeps
-    // the four-warp preparations.)
-    if (fused && L.exports && !p.g_per_channel && !p.conv.w) {
+    // The export form (decay per head, no fused convolution): the fused kernel's serial passes export
+    // the state and the preparing CTAs form the outputs.  It shortens the serial chain step but adds
+    // the exports' DRAM traffic and gives the preparing CTAs the output work, so it pays off only
+    // where the chain dominates: long sequences (on average 256 chunks or more), or always with
+    // GDN_FORM_ON.  (With the convolution the preparations are heavier, and a decay per key channel
+    // keeps the four-warp preparations.)
+    const bool long_seqs = (long)p.total_T >= 256L * kC * p.num_seqs;
+    if (fused && L.exports && !p.g_per_channel && !p.conv.w && (form == GDN_FORM_ON || long_seqs)) {
         a.Sx = ws + L.off_Sx;
         a.Vx = ws + L.off_Vx;
         a.oready = reinterpret_cast<int32_t*>(ws + L.off_oready);
+        fused_fn = chunk_fused_kernel<false, true>;
+        e = cudaFuncSetAttribute(fused_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fz::kSmem);
+        if (e != cudaSuccess) return e;
     }
 
     chunk_map_kernel<<<1, 1024, 0, s>>>(a);

@@ -101,8 +101,9 @@ def test_fused_and_two_kernel_forms_agree_bitwise(kernel_forms):
     inp = synthetic.prefill_inputs(_cfg([300, 64, 0, 1000, 65], 4, seed=85, gate=True, init_state=True))
     g32, b32 = oracle_gates(inp)
     outs = []
-    for form in (gdn.GDN_FORM_AUTO, gdn.GDN_FORM_OFF):
+    for form in (gdn.GDN_FORM_AUTO, gdn.GDN_FORM_ON, gdn.GDN_FORM_OFF):  # fused, fused export form, two kernels
         kernel_forms.gdn_set_kernel_forms(prefill_fused=form)
         outs.append(_run(inp, g32, b32, out_dtype=torch.bfloat16))
-    assert torch.equal(outs[0][0], outs[1][0])
-    assert torch.equal(outs[0][1], outs[1][1])
+    for o in outs[:2]:
+        assert torch.equal(o[0], outs[2][0])
+        assert torch.equal(o[1], outs[2][1])
