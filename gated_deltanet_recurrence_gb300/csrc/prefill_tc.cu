@@ -2117,13 +2117,14 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap mQt, const __grid_constan
 
 // ---- 3b. the outputs from the exported state (fused kernel, export form) -------------------------
 //
-// O = Q~ S^T + Aqk V_new for every chunk, then the gate and the stores, by each preparing CTA once its
-// preparations are done, after the serial pass has exported the chunk's state tile and V_new^T
-// (workspace flag).  The products are the serial pass's own (same operands, same order) and the
-// epilogue is the same function, so both forms give the same bits.  The CTA's 16 warps form a
-// pipeline over two item buffers (tiles) and two TMEM accumulators: warp 0 lane 0 takes items
-// position by position and loads them, warp 1 lane 0 issues the products, warps 8-11 and 12-15 take
-// alternate items through the gate and the stores.
+// O = Q~ S^T + Aqk V_new for every chunk, then the gate and the stores, by a set of output CTAs (as
+// many as serial passes), each chunk after its serial pass has exported the chunk's state tile and
+// V_new^T (workspace flag), so that the outputs trail the serial passes while the exports are still
+// in L2.  The products are the serial pass's own (same operands, same order) and the epilogue is the
+// same function, so both forms give the same bits.  An output CTA's 16 warps form a pipeline over
+// two item buffers (tiles) and two TMEM accumulators: warp 0 lane 0 takes items position by position
+// and loads them, warp 1 lane 0 issues the products, warps 8-11 and 12-15 take alternate items
+// through the gate and the stores.
 namespace oc {
 constexpr uint32_t oS = 0, oV = 32768, oQ = 49152, oA = 65536, oZ = 73728;  // within one item buffer
 constexpr uint32_t kBuf = oZ + 32768;
@@ -2136,8 +2137,8 @@ struct Slot {  // the item in a buffer: chunk-head pair (-1: no more), first tok
 constexpr uint32_t kEngBytes = 8 * NBAR + 2 * sizeof(Slot);  // barriers, then the two buffers' items
 }  // namespace oc
 
-// All 512 threads of a preparing CTA; `eng` holds the engine's barriers and item slots, `tm` the
-// CTA's 256 TMEM columns.  The preparing CTAs take the items in turn (CTA e of E takes items e,
+// All 512 threads of an output CTA; `eng` holds the engine's barriers and item slots, `tm` the
+// CTA's 256 TMEM columns.  The output CTAs take the items in turn (CTA e of E takes items e,
 // e + E, ...; items are position-major).  The producer waits for an item's flags before it waits
 // for a free buffer, so that the two latencies overlap.  It marks the slot after the last item, and
 // the one after that, with -1, which ends the MMA thread and both epilogue groups.  Waits are
@@ -2347,6 +2348,20 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
         __syncthreads();
         tc_fence_after();
         const uint32_t tm = *tbase;
+        if constexpr (EXP) {
+            // export form: CTAs n_units .. 2 n_units - 1 form the chunks' outputs from the start, so
+            // that they trail the serial passes while the exports are still in L2; the rest prepare
+            if ((int)blockIdx.x < 2 * n_units) {
+                out_engine(sm, sm + oEng, tm, n_units, (int)blockIdx.x - n_units, n_units, &mQt, &mAqk, &mZ, &mOut, a);
+                tc_fence_before();
+                __syncthreads();
+                if (warp == 0) {
+                    tc_fence_after();
+                    tmem_dealloc(tm, 2 * p2::kTmemCols);
+                }
+                return;
+            }
+        }
         uint8_t* smi = sm + inst * kPrepStride2;
         uint64_t* bars = reinterpret_cast<uint64_t*>(smi + p2::oBar);
         const GroupBar gb{1u + (uint32_t)inst, (uint32_t)p2::kThreads};
@@ -2378,13 +2393,6 @@ chunk_fused_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
                 fence_proxy_async_global();
                 st_release_gpu(a.ready + gh, 1);
             }
-        }
-        if constexpr (EXP) {  // export form: then the chunks' outputs, by the whole CTA
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            out_engine(sm, sm + oEng, tm, n_units, (int)blockIdx.x - n_units, (int)gridDim.x - n_units, &mQt, &mAqk,
-                       &mZ, &mOut, a);
         }
         tc_fence_before();
         __syncthreads();
@@ -2583,14 +2591,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, cudaStream_t s) {
     }
     a.nch = L.nch;
     a.ready = fused ? reinterpret_cast<int32_t*>(ws + L.off_ready) : nullptr;
-    // The export form (decay per head, no fused convolution): the fused kernel's serial passes export
-    // the state and the preparing CTAs form the outputs.  It shortens the serial chain step but adds
-    // the exports' DRAM traffic and gives the preparing CTAs the output work, so it pays off only
-    // where the chain dominates: long sequences (on average 256 chunks or more), or always with
-    // GDN_FORM_ON.  (With the convolution the preparations are heavier, and a decay per key channel
-    // keeps the four-warp preparations.)
-    const bool long_seqs = (long)p.total_T >= 256L * kC * p.num_seqs;
-    if (fused && L.exports && !p.g_per_channel && !p.conv.w && (form == GDN_FORM_ON || long_seqs)) {
+    // The export form (decay per head, no fused convolution, at most a third of the SMs in serial
+    // passes): the fused kernel's serial passes export the state and as many other CTAs form the
+    // outputs while the rest prepare.  The serial chain step shortens (no output work beside it),
+    // the exports are read back from L2, and the preparing CTAs keep up.  (With the convolution the
+    // preparations are heavier, and a decay per key channel keeps the four-warp preparations.)
+    if (fused && L.exports && !p.g_per_channel && !p.conv.w && 3 * units <= sms) {
         a.Sx = ws + L.off_Sx;
         a.Vx = ws + L.off_Vx;
         a.oready = reinterpret_cast<int32_t*>(ws + L.off_oready);

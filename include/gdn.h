@@ -245,11 +245,11 @@ int gdn_get_device_error(void* stream, int* device_status);
  * is GDN_FORM_AUTO for both.
  *   prefill_fused  GDN_FORM_AUTO: gdn_chunk_fwd (tensor-core path) fuses chunk preparation and the
  *                  serial pass into one cooperative launch when the (sequence, head) pairs number
- *                  at most half the SMs; with a decay per head, no fused convolution and sequences
- *                  of 256 chunks or more on average, the serial passes of that launch leave the
- *                  chunk outputs to the preparing CTAs (export form).  GDN_FORM_OFF: always the
+ *                  at most half the SMs; with a decay per head, no fused convolution and pairs
+ *                  numbering at most a third of the SMs, the serial passes of that launch leave the
+ *                  chunk outputs to as many other CTAs (export form).  GDN_FORM_OFF: always the
  *                  two-kernel form; GDN_FORM_ON: fused whenever the pairs number fewer than the
- *                  SMs, in the export form wherever it applies.  Results are bit-identical.
+ *                  SMs.  Results are bit-identical.
  *   decode_blocks  GDN_FORM_AUTO: gdn_recurrent_multi_step takes the four-token block form when the
  *                  tokens fill the blocks to within one token or T >= 10; GDN_FORM_OFF: token by
  *                  token; GDN_FORM_ON: blocks for every T >= 2.  Results agree to fp32 rounding.

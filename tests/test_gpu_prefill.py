@@ -202,7 +202,7 @@ def test_gate_prep_then_prefill_end_to_end():
                                      ("varlen", dict(lengths=[300, 64, 0, 1000, 65], num_seqs=5, H=4))])
 def test_fused_and_two_kernel_paths_agree_bitwise(name, kw, kernel_forms):
     """Few (sequence, head) units run the fused cooperative kernel (preparation and serial pass at
-    once; with GDN_FORM_ON in the export form, whose outputs the preparing CTAs form);
+    once; with few pairs in the export form, whose outputs other CTAs form);
     gdn_set_kernel_forms(GDN_FORM_OFF) selects the two-kernel path.  All run the same arithmetic in
     the same order, so outputs and final states must be identical bit for bit."""
     cfg = synthetic.workload(name if name != "varlen" else "varlen", **kw) if kw else synthetic.workload(name)
@@ -216,8 +216,8 @@ def test_fused_and_two_kernel_paths_agree_bitwise(name, kw, kernel_forms):
                   conv_weight=inp["conv_weight"].to(dev) if inp.get("conv_weight") is not None else None,
                   gate_z=inp["z"].to(dev) if inp["z"] is not None else None)
     outs = {}
-    # AUTO: fused; ON: fused, in the export form where it applies (decay per head, no convolution);
-    # OFF: two kernels
+    # AUTO: fused (in the export form where it applies: decay per head, no convolution, few pairs);
+    # ON: fused whenever the pairs number fewer than the SMs; OFF: two kernels
     for mode, form in (("1", gdn.GDN_FORM_AUTO), ("2", gdn.GDN_FORM_ON), ("0", gdn.GDN_FORM_OFF)):
         gdn.gdn_set_kernel_forms(prefill_fused=form)
         out, Sf = gdn.gdn_chunk_fwd(*args, **kwargs)

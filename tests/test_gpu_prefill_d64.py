@@ -101,7 +101,7 @@ def test_fused_and_two_kernel_forms_agree_bitwise(kernel_forms):
     inp = synthetic.prefill_inputs(_cfg([300, 64, 0, 1000, 65], 4, seed=85, gate=True, init_state=True))
     g32, b32 = oracle_gates(inp)
     outs = []
-    for form in (gdn.GDN_FORM_AUTO, gdn.GDN_FORM_ON, gdn.GDN_FORM_OFF):  # fused, fused export form, two kernels
+    for form in (gdn.GDN_FORM_AUTO, gdn.GDN_FORM_ON, gdn.GDN_FORM_OFF):  # fused (export form), fused, two kernels
         kernel_forms.gdn_set_kernel_forms(prefill_fused=form)
         outs.append(_run(inp, g32, b32, out_dtype=torch.bfloat16))
     for o in outs[:2]:
