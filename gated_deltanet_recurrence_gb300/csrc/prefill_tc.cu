@@ -690,8 +690,8 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
     }
 }
 
-// One chunk of one head: everything the state pass needs from it, written to the workspace.  The
-// 128 threads (tid 0..127) synchronise with `gb`; `sm` is this chunk's 1024-aligned shared region,
+// One chunk of one head with a decay per key channel (prep2_chunk handles a decay per head):
+// everything the state pass needs from it, written to the workspace.  The 128 threads (tid 0..127) synchronise with `gb`; `sm` is this chunk's 1024-aligned shared region,
 // `tm` its 256 TMEM columns, `bars` its two mbarriers, the TMA barrier expected at `tma_parity`.
 template <bool PC>
 __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* bars, uint32_t tma_parity,
@@ -799,76 +799,7 @@ __device__ __forceinline__ void prep_chunk(uint8_t* sm, uint32_t tm, uint64_t* b
         }
         tc_fence_before();
         gb.sync();
-        if constexpr (PC) {
-            pc_products(sm, a, gh, h, t0, L, tid, kinv, qsv, bts, Af, Tf, gb);
-        } else {
-        // every element is formed in registers first (the loop has no stores, so its shared loads
-        // pipeline), then the row is stored
-        if (tid < kC) {
-            const int i = tid;
-            const float gi = gcs[i], f = bts[i] * kinv[i];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) row[j] = j < i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) Af[i * LDA + j] = row[j];
-            // per-token factors for the state pass
-            float* sc = a.scal + gh * 4 * kC;
-            const float glast = gcs[kC - 1];
-            sc[i] = __expf(gi) * qsv[i];
-            sc[kC + i] = __expf(glast - gi) * kinv[i];
-            sc[2 * kC + i] = gi;
-            if (i == 0) sc[3 * kC] = __expf(glast);
-        } else {  // decayed Q K^T row, bf16, staged (in the T tile, free until the solve)
-            const int i = tid - kC;
-            const float gi = gcs[i], f = qsv[i];
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(Tf) + i * 128);
-#pragma unroll
-            for (int j = 0; j < 64; ++j) row[j] = j <= i ? f * __expf(gi - gcs[j]) * row[j] * kinv[j] : 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                dst[c8 ^ (i & 7)] = make_uint4(pack_bf16x2(row[8 * c8], row[8 * c8 + 1]), pack_bf16x2(row[8 * c8 + 2], row[8 * c8 + 3]),
-                                               pack_bf16x2(row[8 * c8 + 4], row[8 * c8 + 5]), pack_bf16x2(row[8 * c8 + 6], row[8 * c8 + 7]));
-        }
-        // ---- scaled operand rows for the state pass: K~ = diag(e^(glast-gc) kinv) K,
-        //      Q~ = diag(e^gc qs) Q; per-row factors first, then every warp writes whole rows ----
-        float* rowf = Tf + 2048;  // [K~ factors 64 | Q~ factors 64], after the 8 KB staged rows
-        {
-            const int i = tid & 63;
-            rowf[tid] = tid >= kC ? __expf(gcs[i]) * qsv[i] : __expf(gcs[kC - 1] - gcs[i]) * kinv[i];
-        }
-        gb.sync();
-        // 2 tensors x 64 rows x 16 chunks of 16 B; a warp covers 2 whole rows.  Four chunks are
-        // read from the tiles before any of them is written to the workspace.
-#pragma unroll 1
-        for (int it0 = 0; it0 < 16; it0 += 4) {
-            uint4 raw[4];
-            float fr[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int flat = (it0 + u) * kThreads + tid, isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
-                raw[u] = *reinterpret_cast<const uint4*>(sm + oKQ + (isq ? 8192 : 0) + (c16 >> 3) * 16384 +
-                                                         sw128_offset(r, (c16 & 7) * 8));
-                fr[u] = rowf[isq * kC + r];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int flat = (it0 + u) * kThreads + tid, isq = flat >> 10, r = (flat >> 4) & 63, c16 = flat & 15;
-                float v[8];
-                unpack_bf16x8(raw[u], v);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= fr[u];
-                *reinterpret_cast<uint4*>((isq ? a.Qt : a.Kt) + gh * kC * kD + (long)r * kD + c16 * 8) =
-                    make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                               pack_bf16x2(v[6], v[7]));
-            }
-        }
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {   // the staged Q K^T rows: 64 rows x 8 chunks; a warp: 4 rows
-            const int flat = it * kThreads + tid, r = flat >> 3, c8 = flat & 7;
-            reinterpret_cast<uint4*>(a.Aqk + gh * kC * kC + (long)r * kC)[c8] =
-                reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(Tf) + r * 128)[c8 ^ (r & 7)];
-        }
-        }  // per-head decay
+        pc_products(sm, a, gh, h, t0, L, tid, kinv, qsv, bts, Af, Tf, gb);
         fence_async_smem();  // the K tile may have been rewritten (K . e^G) for the W product
         gb.sync();
         // Q is no longer read: V comes into its rows while the triangular solve runs
