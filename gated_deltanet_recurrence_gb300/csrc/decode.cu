@@ -1,7 +1,7 @@
 // decode.cu -- gated delta rule decode on kept fp32 states (gdn_recurrent_step and
 // gdn_recurrent_multi_step: T tokens per sequence from a state pool, token by token in
-// decode_kernel or, for several tokens, in blocks of four in the chunked form in
-// decode_block_kernel).
+// decode_kernel or, for several tokens or with the convolution, in decode_stream_kernel: blocks
+// of four tokens in the chunked form, states staged through shared memory by bulk copies).
 //
 // "6.6 Gated DeltaNet" 6.6.8 and "[LLM Algorithms-2] Gated DeltaNet" section 4: per (sequence,
 // head) and per state row r (d_k contiguous), with alpha one value or one per key channel,
@@ -22,6 +22,7 @@
 #include <stdlib.h>
 
 #include "gdn_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -302,10 +303,10 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
     for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::store(S + (long)i * D, s[i]);
 }
 
-// ---- several tokens per unit: blocks of kBlk tokens in the chunked form ------------------------
+// ---- several tokens per unit, and the convolution: the streamed form ---------------------------
 //
 // "[LLM Algorithms-2] Gated DeltaNet" section 4 (the chunk form of the same recurrence) applied to
-// a block of kBlk tokens of one unit, with S_0 the state before the block and, per key channel c,
+// a block of NB tokens of one unit, with S_0 the state before the block and, per key channel c,
 // G_t[c] the block's cumulative log decay up to token t (one value for all channels when the decay
 // is per head):
 //     A[i][j] = beta_i sum_c k_i[c] k_j[c] e^(G_i - G_j)[c]   (j < i),   T = (I + A)^-1
@@ -315,305 +316,294 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
 //              M[i][j] = sum_c q_i[c] k_j[c] e^(G_i - G_j)[c]
 //     s_r <- e^G_last . s_r + sum_j V_new[j][r] (e^(G_last - G_j) . k_j)
 // which is the token-by-token update (prediction from the decayed state, write, read) regrouped,
-// so a unit's tokens share one pass over its state: the 2 kBlk dot products of a state row are
-// independent, and the update costs kBlk + 1 operations per element instead of 2 kBlk.  Every
+// so a unit's tokens share one pass over its state: the 2 NB dot products of a state row are
+// independent, and the update costs NB + 1 operations per element instead of 2 NB.  Every
 // exponent is <= 0.  A block past the last token is padded with tokens that change nothing
-// (k = q = v = 0, beta = 0, no decay), so any T works.
-constexpr int kBlk = 4;
+// (k = q = v = 0, beta = 0, no decay), so any T works.  With NB = 1 the formulas are the
+// single-token step itself (W = beta alpha k, U = beta v, M = q . k).
+//
+// Layout of the work.  Persistent CTAs (one per SM for d = 128, two for d = 64) take the (sequence,
+// head) units with the grid as stride.  Each unit's state (64 KB at d = 128) is requested from HBM
+// by bulk copies into a shared-memory stage kStages units ahead, so later units' reads are in
+// flight while the current one computes.  The state warps (16 rows each, lanes over the columns as
+// in decode_kernel) take the rows into registers, which frees the stage for the next request, run
+// the unit's blocks and write the rows back to HBM from registers.  The block operands (W, U,
+// e^G q, e^(G_last - G) k, e^G_last, M) depend on the inputs alone, so four preparing warps form
+// them ahead of the state warps: block number b of the CTA (counted over its units) goes to
+// preparing warp b mod 4, which writes it into a shared-memory slot of its own and so is never
+// more than one use of that slot ahead.  Every wait is bounded; on a timeout the kernel records
+// GDN_ERR_TIMEOUT, the state warps agree at the next unit to stop, and the requests still in
+// flight are waited for (bounded) before the CTA exits.
+constexpr int kBlk = 4;                      // tokens per block when a unit has several tokens
+constexpr int kPrepWarps = 4;
+constexpr uint64_t kWaitNs = 2000000000ull;  // bound on one mbarrier wait: 2 s
 
-template <int D, typename TIn, bool GATE, bool CONV>
-__global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
-    constexpr int EPT = D / 32, NW = D / kRowsPerWarp;
-    static_assert(NW >= kBlk, "one warp per token of a block");
-    __shared__ __align__(16) float kn[kBlk][D];   // normalised k (then unused rows of W scratch)
-    __shared__ __align__(16) float qn[kBlk][D];   // scaled, normalised q
-    __shared__ __align__(16) float vv[kBlk][D];   // v
-    __shared__ __align__(16) float Gs[kBlk][D];   // log decay, then its cumulative sum over the block
-    __shared__ __align__(16) float Wm[kBlk][D];   // e^G_j . k_j, then W_i
-    __shared__ __align__(16) float Qd[kBlk][D];   // e^G_i . q_i
-    __shared__ __align__(16) float Kd[kBlk][D];   // e^(G_last - G_j) . k_j
-    __shared__ __align__(16) float gL[D];         // e^G_last
-    __shared__ __align__(16) float zz[GATE ? kBlk : 1][GATE ? D : 1];
-    __shared__ float part[GATE ? kBlk : 1][NW];  // per warp: sum of y^2 over its 16 rows
-    __shared__ float bet[kBlk], Am[kBlk][kBlk], Mm[kBlk][kBlk], Uc[kBlk][kBlk];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int unit = blockIdx.x;  // n * H + h
-    const int n = unit / a.H, h = unit % a.H;
-    const int grp = a.H / a.Hk, hk = h / grp;
-    const int slot = a.idx ? a.idx[n] : n;
-    if (slot < 0) return;
-    if (slot >= a.num_slots) {
-        if (tid == 0) record_error(a.err, GDN_ERR_ARG);
-        return;
+template <int D, int NB, bool GATE>
+struct StreamShape {
+    static constexpr int EPT = D / 32;
+    static constexpr int kStateWarps = D / kRowsPerWarp;
+    static constexpr int kThreads = (kStateWarps + kPrepWarps) * 32;
+    static constexpr int kCtasPerSm = D == 128 ? 1 : 2;
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr uint32_t kState = D * D * 4;
+    static constexpr uint32_t kCopy = kState < 16384 ? kState : 16384;  // bytes per bulk copy
+    // a preparing warp's slot: W, e^G q, e^(G_last - G) k, U ([NB][D] each), e^G_last [D], the
+    // gate input z [NB][D], M [NB][NB]
+    static constexpr uint32_t kRows = NB * D * 4;
+    static constexpr uint32_t oW = 0, oQd = kRows, oKd = 2 * kRows, oU = 3 * kRows, oGL = 4 * kRows;
+    static constexpr uint32_t oZ = oGL + D * 4, oM = oZ + (GATE ? kRows : 0);
+    static constexpr uint32_t kSlot = (oM + NB * NB * 4 + 15) / 16 * 16;
+    // shared memory: state stages, slots, the gate's per-warp sums of squares [2][NB][warps], barriers
+    static constexpr uint32_t oSlots = kStages * kState;
+    static constexpr uint32_t oPart = oSlots + kPrepWarps * kSlot;
+    static constexpr uint32_t oBar = oPart + 2 * NB * kStateWarps * 4;
+    static constexpr uint32_t kBytes = oBar + (kStages + 2 * kPrepWarps) * 8;
+    static_assert(oBar % 8 == 0 && kState % kCopy == 0, "layout");
+};
+
+template <int EPT>
+__device__ __forceinline__ void lds_vec(const float* p, float* o) {
+    if constexpr (EPT == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        o[0] = t.x; o[1] = t.y;
     }
-    const int r0 = warp * kRowsPerWarp;
-    float* S = a.state + ((long)slot * a.H + h) * D * D + (long)r0 * D + lane * EPT;
-    float s[kRowsPerWarp][EPT];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::load(S + (long)i * D, s[i]);
+}
+template <int EPT>
+__device__ __forceinline__ void sts_vec(float* p, const float* o) {
+    if constexpr (EPT == 4) *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
+    else *reinterpret_cast<float2*>(p) = make_float2(o[0], o[1]);
+}
 
-    const int c0 = lane * EPT;                       // this lane's key / value channels
+// After this, lanes j and j + 16 hold the warp-wide sum of x[j] (16 values per lane in, 1 out).
+// After this, lane l holds the sum over its half-warp (the 16 lanes with the same l >> 4) of
+// x[l & 15] (16 values per lane in, 1 out).
+__device__ __forceinline__ float transpose_reduce_half(float (&x)[16], int lane) {
+#pragma unroll
+    for (int width = 8; width >= 1; width >>= 1) {
+        const bool upper = (lane & width) != 0;
+#pragma unroll
+        for (int j = 0; j < width; ++j) {
+            float send = upper ? x[j] : x[j + width];
+            float keep = upper ? x[j + width] : x[j];
+            x[j] = keep + __shfl_xor_sync(0xffffffffu, send, width);
+        }
+    }
+    return x[0];
+}
+// After this, lanes j and j + 16 hold the warp-wide sum of x[j].
+__device__ __forceinline__ float transpose_reduce16(float (&x)[16], int lane) {
+    const float h = transpose_reduce_half(x, lane);
+    return h + __shfl_xor_sync(0xffffffffu, h, 16);
+}
+
+// Pool slot of unit j's sequence, or -1 when the unit is skipped: a padding entry, or an index
+// past the pool (recorded in `err` when given, so that one role reports it).
+__device__ __forceinline__ int unit_slot(const DecodeArgs& a, int j, int* err) {
+    const int n = j / a.H;
+    const int s = a.idx ? a.idx[n] : n;
+    if (s >= a.num_slots) {
+        if (err) record_error(err, GDN_ERR_ARG);
+        return -1;
+    }
+    return s;
+}
+// The first unit at or after j, in steps of the grid, that is not skipped; `units` when none is left.
+__device__ __forceinline__ int next_unit(const DecodeArgs& a, int j, int units, int* slot, int* err) {
+    for (; j < units; j += gridDim.x)
+        if ((*slot = unit_slot(a, j, err)) >= 0) return j;
+    return units;
+}
+
+// Forms block t0 .. t0 + NB - 1 of unit (n, h) in slot `sl` (one warp; lane holds key and value
+// channels c0 .. c0 + EPT - 1).  With the convolution, the block at t0 = 0 also writes the unit's
+// final history: only that block reads the input history (NB >= 3, or T = 1), and the lane that
+// reads a channel's history is the one that writes it, after its reads, so the history may be
+// updated in place.
+template <int D, typename TIn, bool GATE, bool CONV, int NB>
+__device__ __forceinline__ void prep_block(const DecodeArgs& a, uint8_t* sl, int n, int h, int slot, int t0,
+                                           int lane) {
+    using L = StreamShape<D, NB, GATE>;
+    constexpr int EPT = L::EPT;
+    const int grp = a.H / a.Hk, hk = h / grp, c0 = lane * EPT;
     const int cq = hk * D + c0, ck = a.Hk * D + cq, cv = 2 * a.Hk * D + h * D + c0;  // conv channels
     const float* cs_in = CONV && a.conv.state_in ? a.conv.state_in + (long)slot * a.conv.dim * 3 : nullptr;
-    const int vrow = r0 + (lane & (kRowsPerWarp - 1));
-
-    for (int t0 = 0; t0 < a.T; t0 += kBlk) {
-        // ---- per token (warp w <- token t0 + w): inputs, convolution, norms ----
-        if (warp < kBlk) {
-            const int t = t0 + warp;
-            float qv[EPT], kv[EPT], vx[EPT], gv[EPT], zv[EPT];
-            float bt = 0.f;
+    float qv[NB][EPT], kv[NB][EPT], vx[NB][EPT], G[NB][EPT], bt[NB];
+    if constexpr (CONV) {
+        // raw inputs of tokens t0 - 3 .. t0 + NB - 1: this call's, the history before it, zero after it
+        float rq[NB + 3][EPT], rk[NB + 3][EPT], rv[NB + 3][EPT];
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) { qv[e] = kv[e] = vx[e] = gv[e] = zv[e] = 0.f; }
-            if (t < a.T) {
-                const long tok = (long)n * a.T + t, vt = tok * a.H + h, qt = tok * a.Hk + hk;
-                load_vec<EPT>(static_cast<const TIn*>(a.q) + qt * D + c0, qv);
-                load_vec<EPT>(static_cast<const TIn*>(a.k) + qt * D + c0, kv);
-                load_vec<EPT>(static_cast<const TIn*>(a.v) + vt * D + c0, vx);
-                if constexpr (CONV) {
-                    // raw inputs of tokens t-3 .. t-1: earlier tokens of this call, else the history
-                    const float4* w4 = reinterpret_cast<const float4*>(a.conv.w);
-                    float hq[3][EPT], hkk[3][EPT], hv[3][EPT];
-#pragma unroll
-                    for (int j = 0; j < 3; ++j) {
-                        const int tau = t - 3 + j;
-                        if (tau >= 0) {
-                            const long tk = (long)n * a.T + tau;
-                            load_vec<EPT>(static_cast<const TIn*>(a.q) + (tk * a.Hk + hk) * D + c0, hq[j]);
-                            load_vec<EPT>(static_cast<const TIn*>(a.k) + (tk * a.Hk + hk) * D + c0, hkk[j]);
-                            load_vec<EPT>(static_cast<const TIn*>(a.v) + (tk * a.H + h) * D + c0, hv[j]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < EPT; ++e) {
-                                hq[j][e] = cs_in ? cs_in[(long)(cq + e) * 3 + 3 + tau] : 0.f;
-                                hkk[j][e] = cs_in ? cs_in[(long)(ck + e) * 3 + 3 + tau] : 0.f;
-                                hv[j][e] = cs_in ? cs_in[(long)(cv + e) * 3 + 3 + tau] : 0.f;
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < EPT; ++e) {
-                        qv[e] = round_to<TIn>(conv4_silu(__ldg(w4 + cq + e), hq[0][e], hq[1][e], hq[2][e], qv[e]));
-                        kv[e] = round_to<TIn>(conv4_silu(__ldg(w4 + ck + e), hkk[0][e], hkk[1][e], hkk[2][e], kv[e]));
-                        vx[e] = round_to<TIn>(conv4_silu(__ldg(w4 + cv + e), hv[0][e], hv[1][e], hv[2][e], vx[e]));
-                    }
-                }
-                if (a.g_per_channel) {
-                    load_vec<EPT>(a.g + vt * D + c0, gv);
-                } else {
-                    const float g0 = a.g[vt];
-#pragma unroll
-                    for (int e = 0; e < EPT; ++e) gv[e] = g0;
-                }
-                bt = a.beta[vt];
-                if constexpr (GATE) load_vec<EPT>(a.z + vt * D + c0, zv);
-                float ssq = 0.f, ssk = 0.f;
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) { ssq += qv[e] * qv[e]; ssk += kv[e] * kv[e]; }
-                ssq = warp_sum(ssq);
-                ssk = warp_sum(ssk);
-                const float qf = a.use_l2 ? a.scale * rsqrtf(ssq + kL2Eps) : a.scale;
-                const float kf = a.use_l2 ? rsqrtf(ssk + kL2Eps) : 1.0f;
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) { qv[e] *= qf; kv[e] *= kf; }
-            }
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) {
-                qn[warp][c0 + e] = qv[e];
-                kn[warp][c0 + e] = kv[e];
-                vv[warp][c0 + e] = vx[e];
-                Gs[warp][c0 + e] = gv[e];
-                if constexpr (GATE) zz[warp][c0 + e] = zv[e];
-            }
-            if (lane == 0) bet[warp] = bt;
-        }
-        __syncthreads();
-        // ---- cumulative log decay and the decayed operand rows (one thread per channel) ----
-        if (tid < D) {
-            const int c = tid;
-            float G[kBlk];
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < kBlk; ++j) { acc += Gs[j][c]; G[j] = acc; Gs[j][c] = acc; }
-            gL[c] = __expf(G[kBlk - 1]);  // every exponent here is <= 0
-#pragma unroll
-            for (int j = 0; j < kBlk; ++j) {
-                const float eg = __expf(G[j]);
-                Wm[j][c] = eg * kn[j][c];
-                Qd[j][c] = eg * qn[j][c];
-                Kd[j][c] = __expf(G[kBlk - 1] - G[j]) * kn[j][c];
-            }
-        }
-        __syncthreads();
-        // ---- A (strictly lower) and M (lower with diagonal): 16 dot products over the channels ----
-        for (int p = warp; p < kBlk * (kBlk + 1) / 2 + kBlk * (kBlk - 1) / 2; p += NW) {
-            // p < 10: M[i][j], j <= i; else A[i][j], j < i
-            const bool isM = p < kBlk * (kBlk + 1) / 2;
-            int q_ = isM ? p : p - kBlk * (kBlk + 1) / 2, i = 0;
-            const int off = isM ? 0 : 1;
-            while (q_ >= i + 1 - off) { q_ -= i + 1 - off; ++i; }
-            const int j = q_;
-            const float* x = isM ? qn[i] : kn[i];
-            float part = 0.f;
-            if (a.g_per_channel) {
+        for (int m = 0; m < NB + 3; ++m) {
+            const int tau = t0 - 3 + m;
+            if (tau >= 0 && tau < a.T) {
+                const long tk = (long)n * a.T + tau;
+                load_vec<EPT>(static_cast<const TIn*>(a.q) + (tk * a.Hk + hk) * D + c0, rq[m]);
+                load_vec<EPT>(static_cast<const TIn*>(a.k) + (tk * a.Hk + hk) * D + c0, rk[m]);
+                load_vec<EPT>(static_cast<const TIn*>(a.v) + (tk * a.H + h) * D + c0, rv[m]);
+            } else {
+                const bool hist = tau < 0 && cs_in;
 #pragma unroll
                 for (int e = 0; e < EPT; ++e) {
-                    const int c = c0 + e;
-                    part += x[c] * kn[j][c] * __expf(Gs[i][c] - Gs[j][c]);
+                    rq[m][e] = hist ? cs_in[(long)(cq + e) * 3 + 3 + tau] : 0.f;
+                    rk[m][e] = hist ? cs_in[(long)(ck + e) * 3 + 3 + tau] : 0.f;
+                    rv[m][e] = hist ? cs_in[(long)(cv + e) * 3 + 3 + tau] : 0.f;
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) part += x[c0 + e] * kn[j][c0 + e];
-            }
-            part = warp_sum(part);
-            if (!a.g_per_channel) part *= __expf(Gs[i][0] - Gs[j][0]);
-            if (lane == 0) {
-                if (isM) Mm[i][j] = part;
-                else Am[i][j] = bet[i] * part;
             }
         }
-        __syncthreads();
-        // ---- T = (I + A)^-1 (unit lower, forward substitution) and the U coefficients T diag(beta) ----
-        if (tid == 0) {
-            float T[kBlk][kBlk];
+        const float4* w4 = reinterpret_cast<const float4*>(a.conv.w);
 #pragma unroll
-            for (int i = 0; i < kBlk; ++i)
+        for (int e = 0; e < EPT; ++e) {
+            const float4 wq = __ldg(w4 + cq + e), wk = __ldg(w4 + ck + e), wv = __ldg(w4 + cv + e);
 #pragma unroll
-                for (int j = 0; j < kBlk; ++j) T[i][j] = i == j ? 1.f : 0.f;
-#pragma unroll
-            for (int i = 1; i < kBlk; ++i)
-#pragma unroll
-                for (int j = 0; j < i; ++j) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = j; m < i; ++m) acc += Am[i][m] * T[m][j];
-                    T[i][j] = -acc;
-                }
-#pragma unroll
-            for (int i = 0; i < kBlk; ++i)
-#pragma unroll
-                for (int j = 0; j < kBlk; ++j) Uc[i][j] = T[i][j] * bet[j];
-        }
-        __syncthreads();
-        if (tid < D) {  // W_i = sum_j T[i][j] beta_j (e^G_j . k_j), in place per channel
-            const int c = tid;
-            float kg[kBlk];
-#pragma unroll
-            for (int j = 0; j < kBlk; ++j) kg[j] = Wm[j][c];
-#pragma unroll
-            for (int i = 0; i < kBlk; ++i) {
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 0; j <= i; ++j) acc += Uc[i][j] * kg[j];
-                Wm[i][c] = acc;
+            for (int i = 0; i < NB; ++i) {
+                const bool live = t0 + i < a.T;
+                qv[i][e] = live ? round_to<TIn>(conv4_silu(wq, rq[i][e], rq[i + 1][e], rq[i + 2][e], rq[i + 3][e])) : 0.f;
+                kv[i][e] = live ? round_to<TIn>(conv4_silu(wk, rk[i][e], rk[i + 1][e], rk[i + 2][e], rk[i + 3][e])) : 0.f;
+                vx[i][e] = live ? round_to<TIn>(conv4_silu(wv, rv[i][e], rv[i + 1][e], rv[i + 2][e], rv[i + 3][e])) : 0.f;
             }
         }
-        __syncthreads();
-        // ---- the unit's state rows: s_r . W_i and s_r . (e^G_i . q_i) for the block's tokens ----
-        float dd[kBlk];
+    } else {
 #pragma unroll
-        for (int i = 0; i < kBlk; ++i) {
-            float wv[EPT], qd[EPT];
-#pragma unroll
-            for (int e = 0; e < EPT; ++e) { wv[e] = Wm[i][c0 + e]; qd[e] = Qd[i][c0 + e]; }
-            float x[32];
-#pragma unroll
-            for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-                float2 pk = make_float2(0.f, 0.f), pq = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < EPT; e += 2) {
-                    const float2 sv = make_float2(s[rr][e], s[rr][e + 1]);
-                    pk = __ffma2_rn(sv, make_float2(wv[e], wv[e + 1]), pk);
-                    pq = __ffma2_rn(sv, make_float2(qd[e], qd[e + 1]), pq);
-                }
-                x[rr] = pk.x + pk.y;
-                x[kRowsPerWarp + rr] = pq.x + pq.y;
-            }
-            dd[i] = transpose_reduce32(x, lane);  // lane < 16: s_r . W_i; lane >= 16: s_r . Qd_i (r = vrow)
-        }
-        // both halves of the warp get both products of row vrow, then V_new and y of that row
-        float vn[kBlk], yv[kBlk];
-#pragma unroll
-        for (int i = 0; i < kBlk; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, dd[i], kRowsPerWarp);
-            const float sw = lane < kRowsPerWarp ? dd[i] : other;   // s_r . W_i
-            const float sq = lane < kRowsPerWarp ? other : dd[i];   // s_r . Qd_i
-            float u = 0.f;
-#pragma unroll
-            for (int j = 0; j <= i; ++j) u += Uc[i][j] * vv[j][vrow];
-            vn[i] = u - sw;
-            float y = sq;
-#pragma unroll
-            for (int j = 0; j <= i; ++j) y += Mm[i][j] * vn[j];
-            yv[i] = y;
-        }
-        // outputs, or for the gate each warp's sum of y^2 over its 16 rows (lanes < 16)
-#pragma unroll
-        for (int i = 0; i < kBlk; ++i) {
+        for (int i = 0; i < NB; ++i) {
             const int t = t0 + i;
-            const long vt = ((long)n * a.T + t) * a.H + h;
-            if constexpr (GATE) {
-                float sq = lane < kRowsPerWarp ? yv[i] * yv[i] : 0.f;
-#pragma unroll
-                for (int o = kRowsPerWarp / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                if (lane == 0) part[i][warp] = sq;
+            if (t < a.T) {
+                const long tok = (long)n * a.T + t;
+                load_vec<EPT>(static_cast<const TIn*>(a.q) + (tok * a.Hk + hk) * D + c0, qv[i]);
+                load_vec<EPT>(static_cast<const TIn*>(a.k) + (tok * a.Hk + hk) * D + c0, kv[i]);
+                load_vec<EPT>(static_cast<const TIn*>(a.v) + (tok * a.H + h) * D + c0, vx[i]);
             } else {
-                if (t < a.T && (lane >> 4) == (i & 1)) store_out(a.out, vt * D + vrow, a.out_dtype, yv[i]);
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) qv[i][e] = kv[i][e] = vx[i][e] = 0.f;
             }
         }
-        // ---- state update: s_r <- e^G_last . s_r + sum_j V_new[j][r] (e^(G_last - G_j) . k_j) ----
-        {
-            float gl[EPT], kd[kBlk][EPT];
+    }
+    // decay, beta, gate input; normalised k, scaled normalised q
 #pragma unroll
-            for (int e = 0; e < EPT; ++e) {
-                gl[e] = gL[c0 + e];
+    for (int i = 0; i < NB; ++i) {
+        const int t = t0 + i;
+        const long vt = ((long)n * a.T + t) * a.H + h;
+        if (t < a.T) {
+            if (a.g_per_channel) {
+                load_vec<EPT>(a.g + vt * D + c0, G[i]);
+            } else {
+                const float g0 = a.g[vt];
 #pragma unroll
-                for (int j = 0; j < kBlk; ++j) kd[j][e] = Kd[j][c0 + e];
+                for (int e = 0; e < EPT; ++e) G[i][e] = g0;
             }
+            bt[i] = a.beta[vt];
+        } else {
 #pragma unroll
-            for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-                float vj[kBlk];
-#pragma unroll
-                for (int j = 0; j < kBlk; ++j) vj[j] = __shfl_sync(0xffffffffu, vn[j], rr);
-#pragma unroll
-                for (int e = 0; e < EPT; e += 2) {
-                    float2 acc = __fmul2_rn(make_float2(gl[e], gl[e + 1]), make_float2(s[rr][e], s[rr][e + 1]));
-#pragma unroll
-                    for (int j = 0; j < kBlk; ++j)
-                        acc = __ffma2_rn(make_float2(vj[j], vj[j]), make_float2(kd[j][e], kd[j][e + 1]), acc);
-                    s[rr][e] = acc.x;
-                    s[rr][e + 1] = acc.y;
-                }
-            }
+            for (int e = 0; e < EPT; ++e) G[i][e] = 0.f;
+            bt[i] = 0.f;
         }
         if constexpr (GATE) {
-            __syncthreads();  // every warp's partial sums are in
-            if (lane < kRowsPerWarp) {
-                const float w = a.w ? a.w[vrow] : 1.0f;
+            float zv[EPT];
+            if (t < a.T) {
+                load_vec<EPT>(a.z + vt * D + c0, zv);
+            } else {
 #pragma unroll
-                for (int i = 0; i < kBlk; ++i) {
-                    const int t = t0 + i;
-                    if (t < a.T) {
-                        float ss = 0.f;
-#pragma unroll
-                        for (int ww = 0; ww < NW; ++ww) ss += part[i][ww];
-                        const long vt = ((long)n * a.T + t) * a.H + h;
-                        const float z = zz[i][vrow];
-                        store_out(a.out, vt * D + vrow, a.out_dtype,
-                                  w * yv[i] * rsqrtf(ss / D + a.eps) * z * sigmoidf_(z));
-                    }
-                }
+                for (int e = 0; e < EPT; ++e) zv[e] = 0.f;
             }
+            sts_vec<EPT>(reinterpret_cast<float*>(sl + L::oZ) + i * D + c0, zv);
         }
-        __syncthreads();  // the block's shared rows are rewritten by the next block
-    }
+        float ssq = 0.f, ssk = 0.f;
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) StateVec<EPT>::store(S + (long)i * D, s[i]);
+        for (int e = 0; e < EPT; ++e) { ssq += qv[i][e] * qv[i][e]; ssk += kv[i][e] * kv[i][e]; }
+        ssq = warp_sum(ssq);
+        ssk = warp_sum(ssk);
+        const float qf = a.use_l2 ? a.scale * rsqrtf(ssq + kL2Eps) : a.scale;
+        const float kf = a.use_l2 ? rsqrtf(ssk + kL2Eps) : 1.0f;
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) { qv[i][e] *= qf; kv[i][e] *= kf; }
+    }
+    // cumulative log decay over the block
+#pragma unroll
+    for (int i = 1; i < NB; ++i)
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) G[i][e] += G[i - 1][e];
+    // P[i][j] = q_i . k_j e^(G_i - G_j) (j <= i: M[i][j]) and k_j . k_i e^(G_j - G_i) (j > i:
+    // A[j][i] / beta_j), over the channels; every exponent is <= 0
+    float P[NB == 1 ? 1 : 16];
+    static_assert(NB == 1 || NB == 4, "blocks of one or four tokens");
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                if (j <= i) acc += qv[i][e] * kv[j][e] * __expf(G[i][e] - G[j][e]);
+                else acc += kv[j][e] * kv[i][e] * __expf(G[j][e] - G[i][e]);
+            }
+            P[i * NB + j] = acc;
+        }
+    float* Ms = reinterpret_cast<float*>(sl + L::oM);
+    float Am[NB][NB];  // A[i][m], m < i, on every lane
+    if constexpr (NB == 1) {
+        const float m00 = warp_sum(P[0]);
+        if (lane == 0) Ms[0] = m00;
+    } else {
+        const float red = transpose_reduce16(P, lane);  // lane l: P[l & 15]
+        if (lane < NB * NB) Ms[lane] = (lane % NB <= lane / NB) ? red : 0.f;
+#pragma unroll
+        for (int i = 1; i < NB; ++i)
+#pragma unroll
+            for (int m = 0; m < i; ++m) Am[i][m] = bt[i] * __shfl_sync(0xffffffffu, red, m * NB + i);
+    }
+    // T = (I + A)^-1 (unit lower, forward substitution), then the coefficients T diag(beta)
+    float Tm[NB][NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+#pragma unroll
+        for (int j = 0; j < NB; ++j) Tm[i][j] = i == j ? 1.f : 0.f;
+#pragma unroll
+    for (int i = 1; i < NB; ++i)
+#pragma unroll
+        for (int j = 0; j < i; ++j) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = j; m < i; ++m) acc += Am[i][m] * Tm[m][j];
+            Tm[i][j] = -acc;
+        }
+    // W_i, U_i, e^G_i q_i, e^(G_last - G_i) k_i, e^G_last
+    float* Ws = reinterpret_cast<float*>(sl + L::oW);
+    float* Qs = reinterpret_cast<float*>(sl + L::oQd);
+    float* Ks = reinterpret_cast<float*>(sl + L::oKd);
+    float* Us = reinterpret_cast<float*>(sl + L::oU);
+    float eG[NB][EPT];
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) eG[i][e] = __expf(G[i][e]);
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+        float wr[EPT], ur[EPT], qd[EPT], kd[EPT];
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+            float aw = 0.f, au = 0.f;
+#pragma unroll
+            for (int j = 0; j <= i; ++j) {
+                const float c = Tm[i][j] * bt[j];
+                aw += c * (eG[j][e] * kv[j][e]);
+                au += c * vx[j][e];
+            }
+            wr[e] = aw;
+            ur[e] = au;
+            qd[e] = eG[i][e] * qv[i][e];
+            kd[e] = __expf(G[NB - 1][e] - G[i][e]) * kv[i][e];
+        }
+        sts_vec<EPT>(Ws + i * D + c0, wr);
+        sts_vec<EPT>(Us + i * D + c0, ur);
+        sts_vec<EPT>(Qs + i * D + c0, qd);
+        sts_vec<EPT>(Ks + i * D + c0, kd);
+    }
+    sts_vec<EPT>(reinterpret_cast<float*>(sl + L::oGL) + c0, eG[NB - 1]);
 
     if constexpr (CONV) {
-        // final history: raw inputs of tokens T-3 .. T-1 (from the history when T < 3); every read
-        // of the input history happened before the barrier that ended the first block
-        if (a.conv.state_out && warp == 0) {
+        // final history: raw inputs of tokens T-3 .. T-1 (from the history when T < 3); all reads first
+        if (t0 == 0 && a.conv.state_out) {
             float* so = a.conv.state_out + (long)slot * a.conv.dim * 3;
             float hq[3][EPT], hkk[3][EPT], hv[3][EPT];
 #pragma unroll
@@ -647,30 +637,259 @@ __global__ void __launch_bounds__(D * 2, 2) decode_block_kernel(DecodeArgs a) {
     }
 }
 
-template <int D, typename TIn, bool GATE, bool CONV>
-cudaError_t launch_variant(const DecodeArgs& a, cudaStream_t s, bool blocks) {
-    const unsigned units = (unsigned)((long)a.N * a.H);
-    if (blocks) decode_block_kernel<D, TIn, GATE, CONV><<<units, D * 2, 0, s>>>(a);
-    else decode_kernel<D, TIn, GATE, CONV><<<units, D * 2, 0, s>>>(a);
+template <int D, typename TIn, bool GATE, bool CONV, int NB>
+__global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShape<D, NB, GATE>::kCtasPerSm)
+    decode_stream_kernel(DecodeArgs a) {
+    using L = StreamShape<D, NB, GATE>;
+    constexpr int EPT = L::EPT, WS = L::kStateWarps;
+    extern __shared__ __align__(128) uint8_t sm[];
+    uint64_t* sfull = reinterpret_cast<uint64_t*>(sm + L::oBar);  // [kStages] state copies landed
+    uint64_t* pfull = sfull + L::kStages;                          // [4] a preparing warp's slot written
+    uint64_t* pempty = pfull + kPrepWarps;                         // [4] the slot read by every state warp
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int units = a.N * a.H, nb = (a.T + NB - 1) / NB, grid = gridDim.x;
+    if (tid == 0) {
+        for (int s = 0; s < L::kStages; ++s) ptx::mbar_init(&sfull[s], 1);
+        for (int p = 0; p < kPrepWarps; ++p) {
+            ptx::mbar_init(&pfull[p], 32);
+            ptx::mbar_init(&pempty[p], WS);
+        }
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp >= WS) {
+        // ---- preparing warps: block b of the CTA's sequence of blocks by warp b mod 4 ----
+        const int pw = warp - WS;
+        int b = 0;
+        for (int j = blockIdx.x, slot; (j = next_unit(a, j, units, &slot, nullptr)) < units; j += grid) {
+            for (int blk = 0; blk < nb; ++blk, ++b) {
+                if (b % kPrepWarps != pw) continue;
+                const int use = b / kPrepWarps;
+                if (use > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&pempty[pw], (use - 1) & 1, kWaitNs))) {
+                    if (lane == 0) record_error(a.err, GDN_ERR_TIMEOUT);
+                    return;
+                }
+                prep_block<D, TIn, GATE, CONV, NB>(a, sm + L::oSlots + pw * L::kSlot, j / a.H, j % a.H, slot, blk * NB,
+                                                   lane);
+                ptx::mbar_arrive(&pfull[pw]);  // every lane: its slot writes are released
+            }
+        }
+        return;
+    }
+
+    // ---- state warps ----
+    // Warp w owns rows r0 .. r0 + 15; lane l holds rows r0 + 8 (l >> 4) + m (m < 8), and of each
+    // row the column chunks 64 k + 4 (l & 15) .. + 3 (k < D / 64), so a row's dot product is spread
+    // over the 16 lanes of a half-warp and every shared or global access of a half-warp to one row
+    // is 256 contiguous bytes.
+    constexpr int CH = D / 64, CPL = 4 * CH;  // float4 chunks and columns per lane and row
+    const int r0 = warp * kRowsPerWarp, hf = lane >> 4, cs = lane & 15;
+    const int rl = 8 * hf + (lane & 7);       // the row whose V_new and y this lane forms
+    float* part = reinterpret_cast<float*>(sm + L::oPart);
+    auto ld_cols = [&](const float* row, float* o) {  // this lane's columns of a row in shared memory
+#pragma unroll
+        for (int k = 0; k < CH; ++k) lds_vec<4>(row + 64 * k + 4 * cs, o + 4 * k);
+    };
+    // thread 0 requests the states: the k-th request goes to stage k mod kStages
+    int pj = blockIdx.x, issued = 0;
+    auto request = [&](int stage) {
+        int ps;
+        pj = next_unit(a, pj, units, &ps, a.err);
+        if (pj >= units) return;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.state + ((long)ps * a.H + pj % a.H) * D * D);
+        uint8_t* dst = sm + stage * L::kState;
+        ptx::mbar_arrive_expect_tx(&sfull[stage], L::kState);
+#pragma unroll
+        for (uint32_t o = 0; o < L::kState; o += L::kCopy) ptx::bulk_load(dst + o, src + o, L::kCopy, &sfull[stage]);
+        pj += grid;
+        ++issued;
+    };
+    if (tid == 0)
+        for (int st = 0; st < L::kStages; ++st) request(st);
+
+    int ui = 0, b = 0;
+    bool bad = false;
+    float s[8][CPL];
+    for (int j = blockIdx.x, slot; (j = next_unit(a, j, units, &slot, nullptr)) < units; j += grid, ++ui) {
+        const int n = j / a.H, h = j % a.H, st = ui % L::kStages;
+        const bool landed = !bad && ptx::mbar_wait(&sfull[st], (ui / L::kStages) & 1, kWaitNs);
+        if (landed) {
+            const float* src = reinterpret_cast<const float*>(sm + st * L::kState) + (r0 + 8 * hf) * D;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) ld_cols(src + m * D, s[m]);
+        }
+        // every state warp has its rows (the stage is free), or all stop together
+        if (ptx::bar_sync_or(1, WS * 32, !landed)) {
+            bad = true;
+            break;
+        }
+        if (tid == 0) request(st);
+
+        for (int blk = 0; blk < nb; ++blk, ++b) {
+            const int w = b % kPrepWarps, t0 = blk * NB;
+            const bool ready = !bad && __all_sync(0xffffffffu, ptx::mbar_wait(&pfull[w], (b / kPrepWarps) & 1, kWaitNs));
+            bad = !ready;
+            const uint8_t* sl = sm + L::oSlots + w * L::kSlot;
+            const float* Ms = reinterpret_cast<const float*>(sl + L::oM);
+            float yv[NB];
+            if (ready) {
+                // s_r . W_i and s_r . (e^G_i q_i) for the block's tokens
+                const float* Ws = reinterpret_cast<const float*>(sl + L::oW);
+                const float* Qs = reinterpret_cast<const float*>(sl + L::oQd);
+                const float* Us = reinterpret_cast<const float*>(sl + L::oU);
+                float dd[NB];
+#pragma unroll
+                for (int i = 0; i < NB; ++i) {
+                    float wv[CPL], qd[CPL];
+                    ld_cols(Ws + i * D, wv);
+                    ld_cols(Qs + i * D, qd);
+                    float x[16];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        float2 pk = make_float2(0.f, 0.f), pq = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < CPL; e += 2) {
+                            const float2 sv = make_float2(s[m][e], s[m][e + 1]);
+                            pk = __ffma2_rn(sv, make_float2(wv[e], wv[e + 1]), pk);
+                            pq = __ffma2_rn(sv, make_float2(qd[e], qd[e + 1]), pq);
+                        }
+                        x[m] = pk.x + pk.y;
+                        x[8 + m] = pq.x + pq.y;
+                    }
+                    // lane l: (l & 15) < 8: s_r . W_i, else s_r . Qd_i, of row r0 + 8 hf + (l & 7)
+                    dd[i] = transpose_reduce_half(x, lane);
+                }
+                // both lanes of a row get both of its products, then V_new and y of that row
+                float vn[NB];
+#pragma unroll
+                for (int i = 0; i < NB; ++i) {
+                    const float other = __shfl_xor_sync(0xffffffffu, dd[i], 8);
+                    const float sw = (lane & 8) ? other : dd[i];
+                    const float sq = (lane & 8) ? dd[i] : other;
+                    vn[i] = Us[i * D + r0 + rl] - sw;
+                    float y = sq;
+#pragma unroll
+                    for (int j2 = 0; j2 <= i; ++j2) y += Ms[i * NB + j2] * vn[j2];
+                    yv[i] = y;
+                }
+                // s_r <- e^G_last . s_r + sum_j V_new[j][r] (e^(G_last - G_j) . k_j)
+                const float* Ks = reinterpret_cast<const float*>(sl + L::oKd);
+                float gl[CPL], kd[NB][CPL];
+                ld_cols(reinterpret_cast<const float*>(sl + L::oGL), gl);
+#pragma unroll
+                for (int j2 = 0; j2 < NB; ++j2) ld_cols(Ks + j2 * D, kd[j2]);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    float vj[NB];
+#pragma unroll
+                    for (int j2 = 0; j2 < NB; ++j2) vj[j2] = __shfl_sync(0xffffffffu, vn[j2], (lane & 16) | m);
+#pragma unroll
+                    for (int e = 0; e < CPL; e += 2) {
+                        float2 acc = __fmul2_rn(make_float2(gl[e], gl[e + 1]), make_float2(s[m][e], s[m][e + 1]));
+#pragma unroll
+                        for (int j2 = 0; j2 < NB; ++j2)
+                            acc = __ffma2_rn(make_float2(vj[j2], vj[j2]), make_float2(kd[j2][e], kd[j2][e + 1]), acc);
+                        s[m][e] = acc.x;
+                        s[m][e + 1] = acc.y;
+                    }
+                }
+                if constexpr (!GATE) {  // lanes l and l ^ 8 hold the same row: each stores half the tokens
+#pragma unroll
+                    for (int i = 0; i < NB; ++i) {
+                        const int t = t0 + i;
+                        if (t < a.T && ((lane >> 3) & 1) == (i & 1))
+                            store_out(a.out, (((long)n * a.T + t) * a.H + h) * D + r0 + rl, a.out_dtype, yv[i]);
+                    }
+                }
+            }
+            if constexpr (GATE) {
+                // RMS over the d_v rows of each token: per-warp sums of squares, one barrier per block
+                // (two buffers, so a warp that runs ahead never overwrites sums still being read)
+                float* pp = part + (b & 1) * NB * WS;
+#pragma unroll
+                for (int i = 0; i < NB; ++i) {
+                    float sq = ready && !(lane & 8) ? yv[i] * yv[i] : 0.f;
+                    sq = warp_sum(sq);
+                    if (lane == 0) pp[i * WS + warp] = sq;
+                }
+                ptx::bar_sync(2, WS * 32);
+                if (ready && !(lane & 8)) {
+                    const float* Zs = reinterpret_cast<const float*>(sl + L::oZ);
+                    const int r = r0 + rl;
+                    const float wr = a.w ? a.w[r] : 1.0f;
+#pragma unroll
+                    for (int i = 0; i < NB; ++i) {
+                        const int t = t0 + i;
+                        if (t < a.T) {
+                            float ss = 0.f;
+#pragma unroll
+                            for (int ww = 0; ww < WS; ++ww) ss += pp[i * WS + ww];
+                            const float z = Zs[i * D + r];
+                            store_out(a.out, (((long)n * a.T + t) * a.H + h) * D + r, a.out_dtype,
+                                      wr * yv[i] * rsqrtf(ss / D + a.eps) * z * sigmoidf_(z));
+                        }
+                    }
+                }
+            }
+            if (ready) {
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&pempty[w]);
+            }
+        }
+        if (!bad) {
+            float* S = a.state + ((long)slot * a.H + h) * D * D + (long)(r0 + 8 * hf) * D + 4 * cs;
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int k = 0; k < CH; ++k) StateVec<4>::store(S + (long)m * D + 64 * k, s[m] + 4 * k);
+        }
+    }
+    if (bad && lane == 0) record_error(a.err, GDN_ERR_TIMEOUT);
+    // requests not consumed (only after a timeout) are waited for before the CTA exits
+    if (tid == 0)
+        for (int k = ui; k < issued; ++k) ptx::mbar_wait(&sfull[k % L::kStages], (k / L::kStages) & 1, kWaitNs);
+}
+
+template <int D, typename TIn, bool GATE, bool CONV, int NB>
+cudaError_t launch_stream(const DecodeArgs& a, cudaStream_t s) {
+    using L = StreamShape<D, NB, GATE>;
+    auto* fn = decode_stream_kernel<D, TIn, GATE, CONV, NB>;
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes)) != cudaSuccess)
+        return e;
+    const long units = (long)a.N * a.H, cap = (long)sms * L::kCtasPerSm;
+    fn<<<(unsigned)(units < cap ? units : cap), L::kThreads, L::kBytes, s>>>(a);
     return cudaGetLastError();
 }
 
-// The block form when a unit's tokens fill its blocks to within one token, or there are many of
-// them; otherwise token by token.  Measured (N = 256, H = 32, d = 128, bf16, gate; ms):
-// T = 2: 0.222 vs 0.265 (blocks), 3: 0.292 vs 0.270, 4: 0.347 vs 0.272, 5: 0.404 vs 0.448,
-// 8: 0.565 vs 0.467: a block costs about 0.19 ms here, a token about 0.06 ms.
-// gdn_set_kernel_forms can force either form (for comparisons and tests).
+template <int D, typename TIn, bool GATE, bool CONV>
+cudaError_t launch_variant(const DecodeArgs& a, cudaStream_t s, bool stream) {
+    if (!stream) {
+        decode_kernel<D, TIn, GATE, CONV><<<(unsigned)((long)a.N * a.H), D * 2, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    if (a.T == 1) return launch_stream<D, TIn, GATE, CONV, 1>(a, s);
+    return launch_stream<D, TIn, GATE, CONV, kBlk>(a, s);
+}
+
+// The streamed form for several tokens per unit and for the convolution; one token without the
+// convolution goes token by token (decode_kernel: load, one update, store, already at the copy
+// rate).  gdn_set_kernel_forms can force either form (for comparisons and tests).
 template <int D, typename TIn>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
-    bool blocks = a.T >= 3 && (a.T % kBlk == 0 || a.T % kBlk == kBlk - 1 || a.T >= 10);
+    bool stream = a.T >= 2 || a.conv.w;
     const int form = decode_blocks_form();
-    if (form != GDN_FORM_AUTO) blocks = form == GDN_FORM_ON && a.T >= 2;
+    if (form != GDN_FORM_AUTO) stream = form == GDN_FORM_ON;
     if (a.conv.w) {
-        if (a.z) return launch_variant<D, TIn, true, true>(a, s, blocks);
-        return launch_variant<D, TIn, false, true>(a, s, blocks);
+        if (a.z) return launch_variant<D, TIn, true, true>(a, s, stream);
+        return launch_variant<D, TIn, false, true>(a, s, stream);
     }
-    if (a.z) return launch_variant<D, TIn, true, false>(a, s, blocks);
-    return launch_variant<D, TIn, false, false>(a, s, blocks);
+    if (a.z) return launch_variant<D, TIn, true, false>(a, s, stream);
+    return launch_variant<D, TIn, false, false>(a, s, stream);
 }
 
 }  // namespace

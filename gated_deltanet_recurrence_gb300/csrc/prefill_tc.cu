@@ -1417,20 +1417,6 @@ chunk_prep2_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant
     }
 }
 
-// Plain bulk copies (16-byte aligned addresses, a multiple of 16 bytes): shared -> global in this
-// thread's bulk group, and global -> shared completing on an mbarrier.
-__device__ __forceinline__ void bulk_store(void* dst_global, const void* src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_global),
-                 "r"(smem_u32(src_smem)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_global, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst_smem)),
-                 "l"(src_global), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // 64 columns of this thread's two rows of an M = 64 accumulator (16x256b shape, 16 repetitions)
 __device__ __forceinline__ void tmem_ld16x256b_x16(uint32_t taddr, uint32_t (&v)[64]) {
     asm volatile(

@@ -250,9 +250,12 @@ int gdn_get_device_error(void* stream, int* device_status);
  *                  chunk outputs to as many other CTAs (export form).  GDN_FORM_OFF: always the
  *                  two-kernel form; GDN_FORM_ON: fused whenever the pairs number fewer than the
  *                  SMs.  Results are bit-identical.
- *   decode_blocks  GDN_FORM_AUTO: gdn_recurrent_multi_step takes the four-token block form when the
- *                  tokens fill the blocks to within one token or T >= 10; GDN_FORM_OFF: token by
- *                  token; GDN_FORM_ON: blocks for every T >= 2.  Results agree to fp32 rounding.
+ *   decode_blocks  GDN_FORM_AUTO: gdn_recurrent_step and gdn_recurrent_multi_step take the streamed
+ *                  form (persistent CTAs, states staged through shared memory, blocks of four
+ *                  tokens in the chunked form) for T >= 2 or with the fused convolution, and go
+ *                  token by token otherwise; GDN_FORM_OFF: token by token; GDN_FORM_ON: the
+ *                  streamed form for every T (one-token blocks at T = 1).  Results agree to fp32
+ *                  rounding; convolution histories are identical.
  * Returns GDN_OK, or GDN_ERR_ARG for a value outside gdn_form (nothing is changed then).
  */
 typedef enum { GDN_FORM_AUTO = 0, GDN_FORM_OFF = 1, GDN_FORM_ON = 2 } gdn_form;

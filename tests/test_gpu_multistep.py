@@ -86,22 +86,34 @@ def test_multi_step_bad_index_is_reported():
     assert torch.equal(p[[1, 3, 4, 5]].cpu(), pool[[1, 3, 4, 5]])
 
 
-@pytest.mark.parametrize("T", [2, 3, 4, 6, 9])
-def test_block_and_token_forms_agree(T, kernel_forms):
-    """The block form (the chunked update over blocks of four tokens, padded at the end) and the
-    token-by-token form compute the same recurrence: outputs and states agree to fp32 rounding,
-    gate included, with skipped sequences."""
+@pytest.mark.parametrize("T,conv", [(1, False), (2, False), (3, False), (4, False), (6, False), (9, False),
+                                    (1, True), (5, True)])
+def test_block_and_token_forms_agree(T, conv, kernel_forms):
+    """The streamed form (the chunked update over blocks of four tokens, padded at the end, or the
+    single-token step at T = 1, with the states staged through shared memory) and the token-by-token
+    form compute the same recurrence: outputs, states and convolution histories agree to fp32
+    rounding, gate included, with skipped sequences."""
     N, H, d, slots = 21, 4, 128, 30
     q, k, v, g, beta, pool, idx, z = _case(N, T, H, d, torch.bfloat16, slots, True, seed=300 + T)
     dev = "cuda"
+    cw = cs = None
+    if conv:
+        gen = torch.Generator().manual_seed(400 + T)
+        C = 3 * H * d
+        cw = (torch.rand(C, 4, generator=gen) - 0.5).to(dev)
+        cs = torch.randn(slots, C, 3, generator=gen).to(dev)
     res = {}
     for mode in ("1", "0"):
         gdn.gdn_set_kernel_forms(decode_blocks=gdn.GDN_FORM_ON if mode == "1" else gdn.GDN_FORM_OFF)
         p = pool.to(dev)
+        cout = torch.zeros_like(cs) if conv else None
         y = gdn.gdn_recurrent_multi_step(q.to(dev), k.to(dev), v.to(dev), g.to(dev), beta.to(dev), p,
-                                         state_indices=idx.to(dev), gate_z=z.to(dev), out_dtype=torch.float32)
+                                         state_indices=idx.to(dev), conv_weight=cw, conv_state=cs,
+                                         conv_state_out=cout, gate_z=z.to(dev), out_dtype=torch.float32)
         assert gdn.gdn_get_device_error() == 0
-        res[mode] = (y.cpu(), p.cpu())
+        res[mode] = (y.cpu(), p.cpu(), cout.cpu() if conv else None)
     live = idx >= 0
     torch.testing.assert_close(res["1"][0][live], res["0"][0][live], rtol=1e-5, atol=1e-5)
     torch.testing.assert_close(res["1"][1], res["0"][1], rtol=1e-5, atol=1e-7)
+    if conv:   # the histories are raw inputs: identical
+        assert torch.equal(res["1"][2], res["0"][2])

@@ -288,9 +288,9 @@ def test_conv_prefill_then_decode_continues_the_sequence():
 @pytest.mark.parametrize("T", [1, 2, 4, 7])
 def test_multi_step_conv_history_in_place(T):
     """With H_k == H the convolution history may be updated in place: every read of the input history
-    happens before the writes (token-by-token form at T = 1, 2; block form at T = 4, 7, where only
-    the first block reads it).  In place and out of place give the same outputs, states and
-    histories, bit for bit."""
+    happens before the writes (in the streamed form only the first block reads it, and the lane
+    that reads a channel's history writes it).  In place and out of place give the same outputs,
+    states and histories, bit for bit."""
     N, H, d, slots = 9, 4, 128, 12
     q, k, v, g, beta, S0, w, cs, z = _decode_case(N, T, H, H, d, torch.bfloat16, False, True, seed=120 + T)
     idx = torch.randperm(slots, generator=torch.Generator().manual_seed(7))[:N].to(torch.int32)
