@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
 // by bulk copies into a shared-memory stage kStages units ahead, so later units' reads are in
 // flight while the current one computes.  The state warps (16 rows each, lanes over the columns as
 // in decode_kernel) take the rows into registers, which frees the stage for the next request, run
-// the unit's blocks and write the rows back to HBM from registers.  The block operands (W, U,
+// the unit's blocks and write the rows back to HBM from registers (for one-token blocks through an
+// output buffer and bulk stores).  The block operands (W, U,
 // e^G q, e^(G_last - G) k, e^G_last, M) depend on the inputs alone, so four preparing warps form
 // them ahead of the state warps: block number b of the CTA (counted over its units) goes to
 // preparing warp b mod 4, which writes it into a shared-memory slot of its own and so is never
@@ -341,9 +342,23 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // bound on one mbarrier wait: 2 s
 template <int D, int NB, bool GATE>
 struct StreamShape {
     static constexpr int EPT = D / 32;
-    static constexpr int kStateWarps = D / kRowsPerWarp;
+    // d = 128 without the gate: 16 state warps of 8 rows (more warps to hide the reductions'
+    // latency); otherwise 16 rows a warp (the gate's per-block barrier over the state warps, and
+    // d = 64 with two CTAs an SM, favour fewer warps)
+    static constexpr bool kWide = D == 128 && !GATE;
+    static constexpr int kRowsPerStateWarp = kWide ? 8 : 16;
+    static constexpr int kStateWarps = D / kRowsPerStateWarp;
     static constexpr int kThreads = (kStateWarps + kPrepWarps) * 32;
     static constexpr int kCtasPerSm = D == 128 ? 1 : 2;
+    // single-token blocks leave the state warps little arithmetic: their rows go back through an
+    // output buffer by bulk stores, so the warps move on to the next unit at once
+    static constexpr bool kOutBuf = NB == 1;
+    // wide: launched at 96 registers a thread (640 threads); the state warpgroups give 8 back and
+    // the preparing warpgroup takes 32 more (4 x 128 x 88 + 128 x 128 = 640 x 96)
+    static constexpr bool kRegSplit = kWide;
+    static constexpr int kRegsState = 88, kRegsPrep = 128;
+    static_assert(!kRegSplit || (kStateWarps % 4 == 0 && 4 * 32 * (kStateWarps / 4) * kRegsState +
+                                 4 * 32 * kRegsPrep == kThreads * 96), "register split");
     static constexpr int kStages = D == 128 ? 2 : 4;
     static constexpr uint32_t kState = D * D * 4;
     static constexpr uint32_t kCopy = kState < 16384 ? kState : 16384;  // bytes per bulk copy
@@ -356,9 +371,10 @@ struct StreamShape {
     // shared memory: state stages, slots, the gate's per-warp sums of squares [2][NB][warps], barriers
     static constexpr uint32_t oSlots = kStages * kState;
     static constexpr uint32_t oPart = oSlots + kPrepWarps * kSlot;
-    static constexpr uint32_t oBar = oPart + 2 * NB * kStateWarps * 4;
+    static constexpr uint32_t oOut = oPart + 2 * NB * kStateWarps * 4;
+    static constexpr uint32_t oBar = oOut + (kOutBuf ? kState : 0);
     static constexpr uint32_t kBytes = oBar + (kStages + 2 * kPrepWarps) * 8;
-    static_assert(oBar % 8 == 0 && kState % kCopy == 0, "layout");
+    static_assert(oOut % 16 == 0 && kState % kCopy == 0 && kBytes <= 232448, "layout");
 };
 
 template <int EPT>
@@ -378,11 +394,12 @@ __device__ __forceinline__ void sts_vec(float* p, const float* o) {
 }
 
 // After this, lanes j and j + 16 hold the warp-wide sum of x[j] (16 values per lane in, 1 out).
-// After this, lane l holds the sum over its half-warp (the 16 lanes with the same l >> 4) of
-// x[l & 15] (16 values per lane in, 1 out).
-__device__ __forceinline__ float transpose_reduce_half(float (&x)[16], int lane) {
+// V values per lane in, 1 out: after this, lane l holds the sum over its half-warp (the 16 lanes
+// with the same l >> 4) of x[l & (V - 1)].
+template <int V>
+__device__ __forceinline__ float transpose_reduce_half(float (&x)[V], int lane) {
 #pragma unroll
-    for (int width = 8; width >= 1; width >>= 1) {
+    for (int width = V / 2; width >= 1; width >>= 1) {
         const bool upper = (lane & width) != 0;
 #pragma unroll
         for (int j = 0; j < width; ++j) {
@@ -391,11 +408,14 @@ __device__ __forceinline__ float transpose_reduce_half(float (&x)[16], int lane)
             x[j] = keep + __shfl_xor_sync(0xffffffffu, send, width);
         }
     }
-    return x[0];
+    float r = x[0];
+#pragma unroll
+    for (int o = V; o < 16; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
 }
 // After this, lanes j and j + 16 hold the warp-wide sum of x[j].
 __device__ __forceinline__ float transpose_reduce16(float (&x)[16], int lane) {
-    const float h = transpose_reduce_half(x, lane);
+    const float h = transpose_reduce_half<16>(x, lane);
     return h + __shfl_xor_sync(0xffffffffu, h, 16);
 }
 
@@ -641,7 +661,7 @@ template <int D, typename TIn, bool GATE, bool CONV, int NB>
 __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShape<D, NB, GATE>::kCtasPerSm)
     decode_stream_kernel(DecodeArgs a) {
     using L = StreamShape<D, NB, GATE>;
-    constexpr int EPT = L::EPT, WS = L::kStateWarps;
+    constexpr int WS = L::kStateWarps;
     extern __shared__ __align__(128) uint8_t sm[];
     uint64_t* sfull = reinterpret_cast<uint64_t*>(sm + L::oBar);  // [kStages] state copies landed
     uint64_t* pfull = sfull + L::kStages;                          // [4] a preparing warp's slot written
@@ -660,6 +680,7 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
 
     if (warp >= WS) {
         // ---- preparing warps: block b of the CTA's sequence of blocks by warp b mod 4 ----
+        if constexpr (L::kRegSplit) ptx::reg_alloc<L::kRegsPrep>();
         const int pw = warp - WS;
         int b = 0;
         for (int j = blockIdx.x, slot; (j = next_unit(a, j, units, &slot, nullptr)) < units; j += grid) {
@@ -679,13 +700,20 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
     }
 
     // ---- state warps ----
-    // Warp w owns rows r0 .. r0 + 15; lane l holds rows r0 + 8 (l >> 4) + m (m < 8), and of each
-    // row the column chunks 64 k + 4 (l & 15) .. + 3 (k < D / 64), so a row's dot product is spread
-    // over the 16 lanes of a half-warp and every shared or global access of a half-warp to one row
-    // is 256 contiguous bytes.
+    // Warp w owns rows r0 .. r0 + RW - 1; lane l holds rows r0 + RPH (l >> 4) + m (m < RPH), and of
+    // each row the column chunks 64 k + 4 (l & 15) .. + 3 (k < D / 64), so a row's dot product is
+    // spread over the 16 lanes of a half-warp and every shared or global access of a half-warp to
+    // one row is 256 contiguous bytes.  After the reductions, the lanes of a half-warp with the
+    // same l mod RPH hold one row: bit RPH tells s_r . W from s_r . (e^G q), the bits above it
+    // number the copies, which share that row's output stores.
+    if constexpr (L::kRegSplit) ptx::reg_dealloc<L::kRegsState>();
+    constexpr int RW = L::kRowsPerStateWarp, RPH = RW / 2, V = 2 * RPH;
     constexpr int CH = D / 64, CPL = 4 * CH;  // float4 chunks and columns per lane and row
-    const int r0 = warp * kRowsPerWarp, hf = lane >> 4, cs = lane & 15;
-    const int rl = 8 * hf + (lane & 7);       // the row whose V_new and y this lane forms
+    constexpr int kGroups = 16 / RPH;         // lanes of a half-warp that share a row
+    const int r0 = warp * RW, hf = lane >> 4, cs = lane & 15;
+    const int rl = RPH * hf + (lane & (RPH - 1));  // the row whose V_new and y this lane forms
+    const bool wside = (lane & RPH) == 0;
+    const int grpid = cs / RPH;                    // 0 .. kGroups - 1
     float* part = reinterpret_cast<float*>(sm + L::oPart);
     auto ld_cols = [&](const float* row, float* o) {  // this lane's columns of a row in shared memory
 #pragma unroll
@@ -710,14 +738,14 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
 
     int ui = 0, b = 0;
     bool bad = false;
-    float s[8][CPL];
+    float s[RPH][CPL];
     for (int j = blockIdx.x, slot; (j = next_unit(a, j, units, &slot, nullptr)) < units; j += grid, ++ui) {
         const int n = j / a.H, h = j % a.H, st = ui % L::kStages;
         const bool landed = !bad && ptx::mbar_wait(&sfull[st], (ui / L::kStages) & 1, kWaitNs);
         if (landed) {
-            const float* src = reinterpret_cast<const float*>(sm + st * L::kState) + (r0 + 8 * hf) * D;
+            const float* src = reinterpret_cast<const float*>(sm + st * L::kState) + (r0 + RPH * hf) * D;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) ld_cols(src + m * D, s[m]);
+            for (int m = 0; m < RPH; ++m) ld_cols(src + m * D, s[m]);
         }
         // every state warp has its rows (the stage is free), or all stop together
         if (ptx::bar_sync_or(1, WS * 32, !landed)) {
@@ -744,9 +772,9 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
                     float wv[CPL], qd[CPL];
                     ld_cols(Ws + i * D, wv);
                     ld_cols(Qs + i * D, qd);
-                    float x[16];
+                    float x[V];
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
+                    for (int m = 0; m < RPH; ++m) {
                         float2 pk = make_float2(0.f, 0.f), pq = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < CPL; e += 2) {
@@ -755,50 +783,52 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
                             pq = __ffma2_rn(sv, make_float2(qd[e], qd[e + 1]), pq);
                         }
                         x[m] = pk.x + pk.y;
-                        x[8 + m] = pq.x + pq.y;
+                        x[RPH + m] = pq.x + pq.y;
                     }
-                    // lane l: (l & 15) < 8: s_r . W_i, else s_r . Qd_i, of row r0 + 8 hf + (l & 7)
-                    dd[i] = transpose_reduce_half(x, lane);
+                    dd[i] = transpose_reduce_half<V>(x, lane);
                 }
-                // both lanes of a row get both of its products, then V_new and y of that row
+                // both sides of a row get both of its products, then V_new and y of that row
                 float vn[NB];
 #pragma unroll
                 for (int i = 0; i < NB; ++i) {
-                    const float other = __shfl_xor_sync(0xffffffffu, dd[i], 8);
-                    const float sw = (lane & 8) ? other : dd[i];
-                    const float sq = (lane & 8) ? dd[i] : other;
+                    const float other = __shfl_xor_sync(0xffffffffu, dd[i], RPH);
+                    const float sw = wside ? dd[i] : other;
+                    const float sq = wside ? other : dd[i];
                     vn[i] = Us[i * D + r0 + rl] - sw;
                     float y = sq;
 #pragma unroll
                     for (int j2 = 0; j2 <= i; ++j2) y += Ms[i * NB + j2] * vn[j2];
                     yv[i] = y;
                 }
-                // s_r <- e^G_last . s_r + sum_j V_new[j][r] (e^(G_last - G_j) . k_j)
+                // s_r <- e^G_last . s_r + sum_j V_new[j][r] (e^(G_last - G_j) . k_j), a column pair at a time
                 const float* Ks = reinterpret_cast<const float*>(sl + L::oKd);
-                float gl[CPL], kd[NB][CPL];
-                ld_cols(reinterpret_cast<const float*>(sl + L::oGL), gl);
+                const float* GLs = reinterpret_cast<const float*>(sl + L::oGL);
+                float vj[RPH][NB];
 #pragma unroll
-                for (int j2 = 0; j2 < NB; ++j2) ld_cols(Ks + j2 * D, kd[j2]);
+                for (int m = 0; m < RPH; ++m)
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    float vj[NB];
+                    for (int j2 = 0; j2 < NB; ++j2) vj[m][j2] = __shfl_sync(0xffffffffu, vn[j2], (lane & 16) | m);
 #pragma unroll
-                    for (int j2 = 0; j2 < NB; ++j2) vj[j2] = __shfl_sync(0xffffffffu, vn[j2], (lane & 16) | m);
+                for (int e = 0; e < CPL; e += 2) {
+                    const int col = 64 * (e / 4) + 4 * cs + (e & 3);
+                    const float2 g2 = *reinterpret_cast<const float2*>(GLs + col);
+                    float2 k2[NB];
 #pragma unroll
-                    for (int e = 0; e < CPL; e += 2) {
-                        float2 acc = __fmul2_rn(make_float2(gl[e], gl[e + 1]), make_float2(s[m][e], s[m][e + 1]));
+                    for (int j2 = 0; j2 < NB; ++j2) k2[j2] = *reinterpret_cast<const float2*>(Ks + j2 * D + col);
 #pragma unroll
-                        for (int j2 = 0; j2 < NB; ++j2)
-                            acc = __ffma2_rn(make_float2(vj[j2], vj[j2]), make_float2(kd[j2][e], kd[j2][e + 1]), acc);
+                    for (int m = 0; m < RPH; ++m) {
+                        float2 acc = __fmul2_rn(g2, make_float2(s[m][e], s[m][e + 1]));
+#pragma unroll
+                        for (int j2 = 0; j2 < NB; ++j2) acc = __ffma2_rn(make_float2(vj[m][j2], vj[m][j2]), k2[j2], acc);
                         s[m][e] = acc.x;
                         s[m][e + 1] = acc.y;
                     }
                 }
-                if constexpr (!GATE) {  // lanes l and l ^ 8 hold the same row: each stores half the tokens
+                if constexpr (!GATE) {  // the kGroups copies of a row share its tokens' stores
 #pragma unroll
                     for (int i = 0; i < NB; ++i) {
                         const int t = t0 + i;
-                        if (t < a.T && ((lane >> 3) & 1) == (i & 1))
+                        if (t < a.T && grpid == i % kGroups)
                             store_out(a.out, (((long)n * a.T + t) * a.H + h) * D + r0 + rl, a.out_dtype, yv[i]);
                     }
                 }
@@ -809,19 +839,19 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
                 float* pp = part + (b & 1) * NB * WS;
 #pragma unroll
                 for (int i = 0; i < NB; ++i) {
-                    float sq = ready && !(lane & 8) ? yv[i] * yv[i] : 0.f;
+                    float sq = ready && grpid == 0 ? yv[i] * yv[i] : 0.f;
                     sq = warp_sum(sq);
                     if (lane == 0) pp[i * WS + warp] = sq;
                 }
                 ptx::bar_sync(2, WS * 32);
-                if (ready && !(lane & 8)) {
+                if (ready) {
                     const float* Zs = reinterpret_cast<const float*>(sl + L::oZ);
                     const int r = r0 + rl;
                     const float wr = a.w ? a.w[r] : 1.0f;
 #pragma unroll
                     for (int i = 0; i < NB; ++i) {
                         const int t = t0 + i;
-                        if (t < a.T) {
+                        if (t < a.T && grpid == i % kGroups) {
                             float ss = 0.f;
 #pragma unroll
                             for (int ww = 0; ww < WS; ++ww) ss += pp[i * WS + ww];
@@ -837,18 +867,40 @@ __global__ void __launch_bounds__(StreamShape<D, NB, GATE>::kThreads, StreamShap
                 if (lane == 0) ptx::mbar_arrive(&pempty[w]);
             }
         }
-        if (!bad) {
-            float* S = a.state + ((long)slot * a.H + h) * D * D + (long)(r0 + 8 * hf) * D + 4 * cs;
+        if constexpr (L::kOutBuf) {
+            // the rows go through the output buffer and leave by bulk stores
+            if (tid == 0) ptx::bulk_wait_read();  // the previous unit's rows have left the buffer
+            if (ptx::bar_sync_or(3, WS * 32, bad)) {
+                bad = true;
+                continue;
+            }
+            float* ob = reinterpret_cast<float*>(sm + L::oOut) + (r0 + RPH * hf) * D + 4 * cs;
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
+            for (int m = 0; m < RPH; ++m)
+#pragma unroll
+                for (int k = 0; k < CH; ++k) sts_vec<4>(ob + m * D + 64 * k, s[m] + 4 * k);
+            ptx::fence_async_smem();
+            ptx::bar_sync(3, WS * 32);
+            if (tid == 0) {
+                uint8_t* S = reinterpret_cast<uint8_t*>(a.state + ((long)slot * a.H + h) * D * D);
+#pragma unroll
+                for (uint32_t o = 0; o < L::kState; o += L::kCopy) ptx::bulk_store(S + o, sm + L::oOut + o, L::kCopy);
+                ptx::bulk_commit();
+            }
+        } else if (!bad) {
+            float* S = a.state + ((long)slot * a.H + h) * D * D + (long)(r0 + RPH * hf) * D + 4 * cs;
+#pragma unroll
+            for (int m = 0; m < RPH; ++m)
 #pragma unroll
                 for (int k = 0; k < CH; ++k) StateVec<4>::store(S + (long)m * D + 64 * k, s[m] + 4 * k);
         }
     }
     if (bad && lane == 0) record_error(a.err, GDN_ERR_TIMEOUT);
     // requests not consumed (only after a timeout) are waited for before the CTA exits
-    if (tid == 0)
+    if (tid == 0) {
         for (int k = ui; k < issued; ++k) ptx::mbar_wait(&sfull[k % L::kStages], (k / L::kStages) & 1, kWaitNs);
+        if constexpr (L::kOutBuf) ptx::bulk_wait_all();  // the last rows are written before the CTA exits
+    }
 }
 
 template <int D, typename TIn, bool GATE, bool CONV, int NB>
