@@ -715,7 +715,8 @@ def run_gdn(args):
                            "peak_source": f"{peak_src} hbm_gbs"},
               "multi_token": {"tokens_per_s": dc["N"] * dc["multi_T"] * world / (dc["multi_ms"] / 1e3),
                               "ms": dc["multi_ms"], "T": dc["multi_T"], "pool_slots": dc["multi_slots"],
-                              "entry_point": "gdn_recurrent_multi_step",
+                              "entry_point": "gdn_recurrent_multi_step", "kernel": "decode_stream_kernel",
+                              "traffic": traffic_record("decode_stream_kernel[multi_token]"),
                               "hbm_gbs": dc["multi_bytes"] / (dc["multi_ms"] / 1e3) / 1e9,
                               "frac": dc["multi_bytes"] / (dc["multi_ms"] / 1e3) / 1e9 / peaks["hbm_gbs"]}}
     line = {
