@@ -533,9 +533,12 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
     const int i0 = 4 * I, j0 = 4 * J;
     const int dr = 4 * (tid >> 3), cg = tid & 7; // diagonal block at row dr; channels e * 8 + cg
 
-    float accA[16], accQ[16], dA[6], dQ[10];
+    // accA2[2 r + h] = (acc[r][2 h], acc[r][2 h + 1]): the 4 x 4 block in column pairs, so that the
+    // products run on the packed two-wide FMA (each lane rounds as fmaf does)
+    float2 accA2[8], accQ2[8];
+    float dA[6], dQ[10];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) { accA[e] = 0.f; accQ[e] = 0.f; }
+    for (int e = 0; e < 8; ++e) { accA2[e] = make_float2(0.f, 0.f); accQ2[e] = make_float2(0.f, 0.f); }
 #pragma unroll
     for (int e = 0; e < 6; ++e) dA[e] = 0.f;
 #pragma unroll
@@ -606,17 +609,16 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
                 const float ei[4] = {1.f, ex2_approx(Gi.y - Gi.x), ex2_approx(Gi.z - Gi.x), ex2_approx(Gi.w - Gi.x)};
                 const float ej[4] = {ex2_approx(Gi.x - Gj.x), ex2_approx(Gi.x - Gj.y), ex2_approx(Gi.x - Gj.z),
                                      ex2_approx(Gi.x - Gj.w)};
-                float kje[4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) kje[b] = kj[b] * ej[b];
+                const float2 kje01 = __fmul2_rn(make_float2(kj[0], kj[1]), make_float2(ej[0], ej[1]));
+                const float2 kje23 = __fmul2_rn(make_float2(kj[2], kj[3]), make_float2(ej[2], ej[3]));
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const float kie = ki[r] * ei[r], qie = qi[r] * ei[r];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        accA[r * 4 + b] = fmaf(kie, kje[b], accA[r * 4 + b]);
-                        accQ[r * 4 + b] = fmaf(qie, kje[b], accQ[r * 4 + b]);
-                    }
+                    const float2 e = __fmul2_rn(make_float2(ki[r], qi[r]), make_float2(ei[r], ei[r]));  // (k, q) . e_i
+                    const float2 kk = make_float2(e.x, e.x), qq = make_float2(e.y, e.y);
+                    accA2[2 * r] = __ffma2_rn(kk, kje01, accA2[2 * r]);
+                    accA2[2 * r + 1] = __ffma2_rn(kk, kje23, accA2[2 * r + 1]);
+                    accQ2[2 * r] = __ffma2_rn(qq, kje01, accQ2[2 * r]);
+                    accQ2[2 * r + 1] = __ffma2_rn(qq, kje23, accQ2[2 * r + 1]);
                 }
             }
         }
@@ -655,8 +657,9 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int i = i0 + r, j = j0 + b;
-                Af[i * LDA + j] = bts[i] * kinv[i] * kinv[j] * accA[r * 4 + b];
-                Tf[i * LD + j] = qsv[i] * kinv[j] * accQ[r * 4 + b];
+                const float2 pa = accA2[2 * r + (b >> 1)], pq = accQ2[2 * r + (b >> 1)];
+                Af[i * LDA + j] = bts[i] * kinv[i] * kinv[j] * ((b & 1) ? pa.y : pa.x);
+                Tf[i * LD + j] = qsv[i] * kinv[j] * ((b & 1) ? pq.y : pq.x);
             }
     }
     if (cg == 0) {
