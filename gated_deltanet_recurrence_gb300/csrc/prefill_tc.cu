@@ -598,7 +598,7 @@ __device__ void pc_products(uint8_t* sm, const TcArgs& a, long gh, int h, long t
         gb.sync();
         // (c) products over this half's 64 channels
         if (off) {
-#pragma unroll 2
+#pragma unroll 4
             for (int cl = 0; cl < 64; ++cl) {
                 const float4 Gi = *reinterpret_cast<const float4*>(GT + cl * LG + i0);
                 const float4 Gj = *reinterpret_cast<const float4*>(GT + cl * LG + j0);
