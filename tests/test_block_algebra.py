@@ -1,4 +1,5 @@
-"""The block form of multi-token decode, checked as algebra on the CPU (fp64, numpy).
+"""The block form of multi-token decode (the streamed decode kernel's blocks of four tokens), checked
+as algebra on the CPU (fp64, numpy).
 
 The multi-token decode kernel takes a unit's tokens in blocks of four in the chunked form of
 "[LLM Algorithms-2] Gated DeltaNet" section 4, with G_t the block's cumulative log decay (per key

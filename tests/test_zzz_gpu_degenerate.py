@@ -83,7 +83,7 @@ def test_decode_degenerate_values(mode):
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("T", [4, 7])
 def test_multi_token_decode_degenerate_values(mode, T):
-    """Pooled multi-token decode; T = 4 and T = 7 take the block form (blocks of four tokens, the
+    """Pooled multi-token decode; T = 4 and T = 7 take the streamed form (blocks of four tokens, the
     last one padded with one token at T = 7)."""
     N, H, d, slots = 6, 4, 128, 9
     gen = torch.Generator().manual_seed(97 + T)

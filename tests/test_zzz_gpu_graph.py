@@ -47,7 +47,7 @@ def test_decode_step_replays_from_a_cuda_graph():
 
 
 def test_multi_token_decode_replays_from_a_cuda_graph():
-    T = 4                                      # the block form
+    T = 4                                      # the streamed form (blocks of four tokens)
     q, k, v, g, b, pool = _decode_inputs(T)
     idx = torch.arange(q.shape[0] - 1, -1, -1, dtype=torch.int32, device="cuda")
     out = torch.empty(q.shape[0], T, v.shape[2], v.shape[3], device="cuda", dtype=torch.float32)
