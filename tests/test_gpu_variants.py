@@ -201,7 +201,7 @@ def _decode_oracle(q, k, v, g, beta, S0, w, cs, z):
     if w is not None:
         qf, kf, vf, st = oracle_conv_qkv(qf, kf, vf, w, cs, cu)
     y, S = oracle.recurrence(qf, kf, vf, flat(g), flat(beta), cu_seqlens=cu, initial_state=S0)
-    o = oracle.gate_rmsnorm_silu(y, flat(z))
+    o = oracle.gate_rmsnorm_silu(y, flat(z)) if z is not None else y
     return o.reshape(N, T, H, d), S, st
 
 
@@ -252,6 +252,43 @@ def test_multi_step_options(H, Hk, d, dtype, pc, conv, T):
                                        gate_z=z.to(DEV), out_dtype=torch.float32)
     assert gdn.gdn_get_device_error() == 0
     o_ref, S_ref, st_ref = _decode_oracle(q, k, v, g, beta, S0, w, cs, z)
+    tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
+    y = out.cpu().double().numpy()
+    err = (np.linalg.norm((y - o_ref).transpose(0, 2, 1, 3).reshape(N * H, -1), axis=1)
+           / np.linalg.norm(o_ref.transpose(0, 2, 1, 3).reshape(N * H, -1), axis=1))
+    assert err.max() <= tol
+    assert rel_l2_states(pool_gpu.cpu()[idx.long()], S_ref) <= tol
+    if conv:
+        np.testing.assert_array_equal(cout.cpu()[idx.long()].double().numpy(), st_ref)
+
+
+@pytest.mark.parametrize("H,Hk,d,dtype,pc,conv,T", [
+    (4, 4, 128, torch.bfloat16, False, True, 1), (8, 4, 128, torch.bfloat16, True, True, 1),
+    (4, 4, 128, torch.bfloat16, True, False, 4), (4, 2, 128, torch.bfloat16, False, True, 5),
+    (4, 4, 128, torch.float32, True, True, 2), (4, 4, 64, torch.float32, True, True, 6)])
+def test_multi_step_without_gate(H, Hk, d, dtype, pc, conv, T):
+    """The raw output y (no gate): at d = 128 the streamed form's 16-warp layout of the state rows,
+    with a decay per key channel, the convolution and grouped heads, one-token blocks (T = 1) and
+    four-token blocks; at d = 64 the 4-warp layout.  Outputs, states and the convolution history
+    against the oracle."""
+    N, slots = 13, 20
+    q, k, v, g, beta, S0, w, cs, _ = _decode_case(N, T, H, Hk, d, dtype, pc, conv, seed=140 + T + H)
+    idx = torch.randperm(slots, generator=torch.Generator().manual_seed(9))[:N].to(torch.int32)
+    pool = torch.zeros(slots, H, d, d)
+    pool[idx.long()] = S0
+    C = synthetic.conv_dim(H, Hk, d)
+    cpool = torch.zeros(slots, C, 3)
+    if conv:
+        cpool[idx.long()] = cs
+    pool_gpu = pool.to(DEV)
+    cin = cpool.to(DEV)
+    cout = torch.full_like(cin, 5.0)
+    out = gdn.gdn_recurrent_multi_step(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), pool_gpu,
+                                       state_indices=idx.to(DEV), conv_weight=w.to(DEV) if conv else None,
+                                       conv_state=cin if conv else None, conv_state_out=cout if conv else None,
+                                       out_dtype=torch.float32)
+    assert gdn.gdn_get_device_error() == 0
+    o_ref, S_ref, st_ref = _decode_oracle(q, k, v, g, beta, S0, w, cs, None)
     tol = TOL_F32 if dtype == torch.float32 else TOL_BF16
     y = out.cpu().double().numpy()
     err = (np.linalg.norm((y - o_ref).transpose(0, 2, 1, 3).reshape(N * H, -1), axis=1)
