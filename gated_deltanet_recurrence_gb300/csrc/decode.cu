@@ -12,15 +12,13 @@
 // which is the decay / predict / write / read sequence of the recurrence with the read folded
 // into the same pass, so the state is read once and written once.
 //
-// HBM-bound: per (sequence, head) the kernel moves 2 * d_v * d_k * 4 bytes of state plus a few
-// hundred bytes of q, k, v, y per token.  Layout of the work: one CTA per (sequence, head); warp
+// HBM-bound: per (sequence, head) a call moves 2 * d_v * d_k * 4 bytes of state plus a few
+// hundred bytes of q, k, v, y per token.  decode_kernel's layout: one CTA per (sequence, head); warp
 // w owns 16 consecutive state rows; lane l holds d_k/32 consecutive columns of each row, so every
 // row is one fully coalesced 128-bit (d_k = 128) or 64-bit (d_k = 64) access per lane.  All 16
 // rows are loaded before any arithmetic (16 x 16 B in flight per lane).  The 32 dot products of
 // a warp (16 rows x {k, q}) are reduced with a transposing butterfly: 31 shuffles leave dot
 // product j on lane j, instead of 5 shuffles per dot product.
-#include <stdlib.h>
-
 #include "gdn_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -325,14 +323,13 @@ __global__ void __launch_bounds__(D * 2, 2) decode_kernel(DecodeArgs a) {
 // Layout of the work.  Persistent CTAs (one per SM for d = 128, two for d = 64) take the (sequence,
 // head) units with the grid as stride.  Each unit's state (64 KB at d = 128) is requested from HBM
 // by bulk copies into a shared-memory stage kStages units ahead, so later units' reads are in
-// flight while the current one computes.  The state warps (16 rows each, lanes over the columns as
-// in decode_kernel) take the rows into registers, which frees the stage for the next request, run
-// the unit's blocks and write the rows back to HBM from registers (for one-token blocks through an
-// output buffer and bulk stores).  The block operands (W, U,
-// e^G q, e^(G_last - G) k, e^G_last, M) depend on the inputs alone, so four preparing warps form
-// them ahead of the state warps: block number b of the CTA (counted over its units) goes to
-// preparing warp b mod 4, which writes it into a shared-memory slot of its own and so is never
-// more than one use of that slot ahead.  Every wait is bounded; on a timeout the kernel records
+// flight while the current one computes.  The state warps (8 or 16 rows each, a row's columns over
+// a half-warp) take the rows into registers, which frees the stage for the next request, run the
+// unit's blocks and write the rows back to HBM from registers (for one-token blocks through an
+// output buffer and bulk stores).  The block operands (W, U, e^G q, e^(G_last - G) k, e^G_last, M)
+// depend on the inputs alone, so four preparing warps form them ahead of the state warps: block
+// number b of the CTA (counted over its units) goes to preparing warp b mod 4, which writes it
+// into a shared-memory slot of its own and so is never more than one use of that slot ahead.  Every wait is bounded; on a timeout the kernel records
 // GDN_ERR_TIMEOUT, the state warps agree at the next unit to stop, and the requests still in
 // flight are waited for (bounded) before the CTA exits.
 constexpr int kBlk = 4;                      // tokens per block when a unit has several tokens
