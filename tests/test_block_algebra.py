@@ -1,7 +1,7 @@
-"""The block form of multi-token decode (the streamed decode kernel's blocks of four tokens), checked
-as algebra on the CPU (fp64, numpy).
+"""The block form of multi-token decode (the streamed decode kernel's blocks of four tokens, and its
+one-token blocks at T = 1), checked as algebra on the CPU (fp64, numpy).
 
-The multi-token decode kernel takes a unit's tokens in blocks of four in the chunked form of
+The multi-token decode kernel takes a unit's tokens in blocks of four (one at T = 1) in the chunked form of
 "[LLM Algorithms-2] Gated DeltaNet" section 4, with G_t the block's cumulative log decay (per key
 channel, or one value per head), padding tokens (k = q = v = 0, beta = 0, no decay) after the last
 one, and, per state row r:
@@ -21,9 +21,9 @@ import oracle
 BLK = 4
 
 
-def _block_form(q, k, v, g, beta, S0):
+def _block_form(q, k, v, g, beta, S0, BLK=BLK):
     """One (sequence, head): q, k [T, dk] already normalised and scaled; v [T, dv]; g [T, dk] log decay;
-    beta [T]; S0 [dv, dk].  Returns y [T, dv], S [dv, dk]."""
+    beta [T]; S0 [dv, dk]; blocks of BLK tokens.  Returns y [T, dv], S [dv, dk]."""
     T, dk = k.shape
     S = S0.copy()
     ys = []
@@ -58,9 +58,10 @@ def _block_form(q, k, v, g, beta, S0):
     return np.concatenate(ys, axis=0), S
 
 
-@pytest.mark.parametrize("T,per_channel", [(1, False), (3, False), (4, False), (9, False), (4, True),
-                                           (7, True)])
-def test_block_form_equals_the_recurrence(T, per_channel):
+@pytest.mark.parametrize("T,per_channel,blk", [(1, False, 4), (3, False, 4), (4, False, 4), (9, False, 4),
+                                               (4, True, 4), (7, True, 4), (1, False, 1), (1, True, 1),
+                                               (5, True, 1)])
+def test_block_form_equals_the_recurrence(T, per_channel, blk):
     rng = np.random.default_rng(100 + T + 10 * per_channel)
     dk, dv = 16, 12
     q = rng.standard_normal((T, 1, dk))
@@ -74,7 +75,7 @@ def test_block_form_equals_the_recurrence(T, per_channel):
     qn = q[:, 0] / np.sqrt((q[:, 0] ** 2).sum(1, keepdims=True) + 1e-6) / np.sqrt(dk)
     kn = k[:, 0] / np.sqrt((k[:, 0] ** 2).sum(1, keepdims=True) + 1e-6)
     gc = g[:, 0] if per_channel else np.repeat(g[:, :1], dk, axis=1)
-    y, S = _block_form(qn, kn, v[:, 0], gc, beta[:, 0], S0[0, 0])
+    y, S = _block_form(qn, kn, v[:, 0], gc, beta[:, 0], S0[0, 0], BLK=blk)
     np.testing.assert_allclose(y, y_ref[:, 0], rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(S, S_ref[0, 0], rtol=1e-10, atol=1e-12)
 
