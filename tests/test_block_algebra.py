@@ -21,7 +21,7 @@ import oracle
 BLK = 4
 
 
-def _block_form(q, k, v, g, beta, S0, BLK=BLK):
+def _block_form(q, k, v, g, beta, S0, BLK=BLK, drop_update_decay=False):
     """One (sequence, head): q, k [T, dk] already normalised and scaled; v [T, dv]; g [T, dk] log decay;
     beta [T]; S0 [dv, dk]; blocks of BLK tokens.  Returns y [T, dv], S [dv, dk]."""
     T, dk = k.shape
@@ -53,7 +53,7 @@ def _block_form(q, k, v, g, beta, S0, BLK=BLK):
         Vn = U - W @ S.T                                            # [BLK, dv]
         Y = (np.exp(G) * qb) @ S.T + M @ Vn                         # [BLK, dv]
         Kd = np.exp(G[-1][None, :] - G) * kb                        # [BLK, dk]
-        S = S * np.exp(G[-1])[None, :] + Vn.T @ Kd
+        S = (S if drop_update_decay else S * np.exp(G[-1])[None, :]) + Vn.T @ Kd
         ys.append(Y[:n])
     return np.concatenate(ys, axis=0), S
 
@@ -96,3 +96,22 @@ def test_padding_tokens_change_nothing():
     y1b, S1b = _block_form(q[1:], k[1:], v[1:], g[1:], beta[1:], S1)
     np.testing.assert_allclose(S2, S1b, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(y2, np.concatenate([y1a, y1b]), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("blk", [1, 4])
+def test_planted_mistake_is_caught(blk):
+    """The same comparison with the decay left out of the state update (s_r <- s_r + ...) fails:
+    the pin distinguishes the regrouping from a plausible wrong one."""
+    rng = np.random.default_rng(7)
+    T, dk, dv = 6, 16, 12
+    q, k, v = rng.standard_normal((T, 1, dk)), rng.standard_normal((T, 1, dk)), rng.standard_normal((T, 1, dv))
+    g = -rng.uniform(0.1, 2.0, (T, 1))
+    beta = rng.uniform(0.0, 1.0, (T, 1))
+    S0 = rng.standard_normal((1, 1, dv, dk)) * 0.3
+    y_ref, S_ref = oracle.recurrence(q, k, v, g, beta, batch=1, initial_state=S0)
+    qn = q[:, 0] / np.sqrt((q[:, 0] ** 2).sum(1, keepdims=True) + 1e-6) / np.sqrt(dk)
+    kn = k[:, 0] / np.sqrt((k[:, 0] ** 2).sum(1, keepdims=True) + 1e-6)
+    gc = np.repeat(g[:, :1], dk, axis=1)
+    y, S = _block_form(qn, kn, v[:, 0], gc, beta[:, 0], S0[0, 0], BLK=blk, drop_update_decay=True)
+    assert not np.allclose(S, S_ref[0, 0], rtol=1e-6, atol=1e-8)
+    assert not np.allclose(y, y_ref[:, 0], rtol=1e-6, atol=1e-8)
